@@ -1,0 +1,189 @@
+/*
+ * moe.h — C ABI of libmoe.so: the forward pass of one Mixture-of-Experts
+ * layer on one NVIDIA B300 (sm_103a).
+ *
+ * The layer follows "MoE 模型原理：路由、专家负载、容量、通信与推理成本"
+ * (wrblog.cn), cited below as [MoE 模型原理 §n]:
+ *
+ *   route    §2.1–§2.2  s_t = W_r x_t + b_r, p_t = softmax(s_t),
+ *                       S_t = TopK(p_t, k), weights p̃ (optionally renormalised)
+ *   dispatch §4.1–§4.3, §5  capacity C = ceil(c·T·k/E); slots take expert
+ *                       positions first come in (token, rank) order; overflow
+ *                       is dropped; kept rows are packed expert by expert
+ *   experts  §1         E_i(x) = W2 σ(W1 x + b1) + b2, as grouped GEMMs over
+ *                       the ragged per-expert row ranges
+ *   combine  §2.2, §5   y_t = Σ_{kept r} p̃_{t,r} E_{S_t[r]}(x_t), token order
+ *   aux      §3.2       f_i = counts_i/T, p̄_i = Σ_t p_{t,i}/T,
+ *                       L_aux = α·E·Σ_i f_i p̄_i
+ *
+ * Conventions for every call:
+ *  - Pointers named as tensors are DEVICE pointers to caller-owned memory;
+ *    `cfg`, `status` and `bytes` are host pointers.  The library never
+ *    allocates device memory and never synchronises the stream; every call
+ *    only enqueues kernels on `stream` (a cudaStream_t; NULL is the legacy
+ *    default stream) and returns.
+ *  - Layouts are dense row-major.  "act" tensors (x, xd, H, yd, y, and the
+ *    weights W_r, W1, W2) have element type cfg->dtype: MOE_DT_F32 (fp32) or
+ *    MOE_DT_BF16 (bf16).  Biases, logits, weights of the combine, psum and
+ *    the statistics are fp32; ids, counts and indices are int32.
+ *  - Sizes that depend on the routing stay on the device: offsets[E] is the
+ *    number of kept rows; rows at or beyond it in xd, H, yd are not written.
+ *  - Synchronous errors (returned): MOE_ERR_INVALID_ARG for a NULL tensor or
+ *    a shape outside the limits below; MOE_ERR_UNSUPPORTED for an unbuilt
+ *    combination; MOE_ERR_WORKSPACE if ws_bytes < moe_workspace_size();
+ *    MOE_ERR_CUDA if a launch fails.  moe_last_error() gives a message.
+ *  - Asynchronous errors: kernels record the first error code in a status
+ *    word inside the workspace (an out-of-range expert id -> INVALID_ARG; a
+ *    bounded wait that gave up -> TIMEOUT).  Read it with
+ *    moe_get_device_status() after synchronising.
+ *  - Limits: T >= 1, T*k < 2^31; 1 <= k <= 16; k <= E <= 1024; d and d_ff
+ *    multiples of 8 (rows are moved as 16-byte vectors); 2^-30 <= c <= 2^30.
+ *  - NaN or Inf inputs give unspecified results.
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t moe_status_t;
+enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,
+  MOE_ERR_UNSUPPORTED = 2,
+  MOE_ERR_CUDA = 3,
+  MOE_ERR_WORKSPACE = 4,
+  MOE_ERR_TIMEOUT = 5
+};
+
+enum { MOE_DT_F32 = 0, MOE_DT_BF16 = 1 };
+enum { MOE_ACT_RELU = 0, MOE_ACT_GELU_TANH = 1 };
+
+/* Layer configuration; plain fields so any FFI can build it. */
+typedef struct moe_config {
+  int64_t T;                /* tokens in this call (the capacity group, §4.1) */
+  int32_t d;                /* model width */
+  int32_t d_ff;             /* expert hidden width */
+  int32_t E;                /* experts */
+  int32_t k;                /* experts per token */
+  double capacity_factor;   /* c in C = ceil(c·T·k/E) */
+  int32_t renormalize;      /* 1: p̃ = p/Σ_{S_t} p (§2.2); 0: raw p */
+  int32_t act;              /* MOE_ACT_* : σ of the expert FFN */
+  int32_t dtype;            /* MOE_DT_* : x, weights, xd, H, yd, y */
+  int32_t write_logits;     /* 1: moe_route also writes fp32 logits[T,E] */
+} moe_config_t;
+
+/* Every tensor of one forward pass (all device pointers). */
+typedef struct moe_tensors {
+  /* inputs */
+  const void* x;        /* [T, d]                                     */
+  const void* Wr;       /* [E, d]      router, row i scores expert i  */
+  const float* br;      /* [E]         router bias                    */
+  const void* W1;       /* [E, d_ff, d]  maps d -> d_ff               */
+  const float* b1;      /* [E, d_ff]                                  */
+  const void* W2;       /* [E, d, d_ff]  maps d_ff -> d               */
+  const float* b2;      /* [E, d]                                     */
+  /* routing outputs */
+  float* logits;        /* [T, E]  written only if cfg->write_logits  */
+  int32_t* topk_ids;    /* [T, k]  descending score, ties to lower id */
+  float* topk_w;        /* [T, k]  combine weights p̃                  */
+  float* psum;          /* [E]     Σ_t p_{t,i}                         */
+  /* dispatch outputs */
+  int32_t* counts;      /* [E]     slots routed to expert (pre-capacity) */
+  int32_t* kept;        /* [E]     min(counts, C)                     */
+  int32_t* offsets;     /* [E+1]   exclusive scan of kept             */
+  int32_t* slot_row;    /* [T, k]  row in xd of slot (t,r), -1 if dropped */
+  int32_t* row_token;   /* [R]     token of each kept row, R = moe_max_rows() */
+  void* xd;             /* [R, d]  per-expert contiguous token rows   */
+  /* expert outputs */
+  void* H;              /* [R, d_ff] hidden activations σ(W1 x + b1)  */
+  void* yd;             /* [R, d]    expert outputs                   */
+  /* layer outputs */
+  void* y;              /* [T, d]  combined output (no residual add)  */
+  float* f;             /* [E]     f_i                                */
+  float* pbar;          /* [E]     p̄_i                                */
+  float* l_aux;         /* [1]     L_aux                              */
+} moe_tensors_t;
+
+/* [MoE 模型原理 §4.1] Capacity C = ceil(c·T·k/E), exact for the binary value
+ * of c.  Host only, pure.  Returns -1 if cfg is invalid. */
+int64_t moe_capacity(const moe_config_t* cfg);
+
+/* Rows of the dispatch buffer to allocate: min(T·k, E·C).  -1 if invalid. */
+int64_t moe_max_rows(const moe_config_t* cfg);
+
+/* Bytes of scratch workspace the stage calls need (status word, per-chunk
+ * histograms, per-tile probability partial sums).  Host only. */
+moe_status_t moe_workspace_size(const moe_config_t* cfg, size_t* bytes);
+
+/* Clear the workspace's device status word (enqueued on stream).  Call once
+ * after allocating a workspace, and after reading a nonzero status. */
+moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, void* stream);
+
+/* [MoE 模型原理 §2.1–§2.2] Router: logits s = x W_rᵀ + b_r (fp32 accumulate),
+ * softmax, top-k with ties to the lower expert index, combine weights
+ * (renormalised over the selected set iff cfg->renormalize), and the column
+ * sums psum[i] = Σ_t p_{t,i} in a fixed reduction order.  logits may be NULL
+ * unless cfg->write_logits. */
+moe_status_t moe_route(const moe_config_t* cfg, const void* x, const void* Wr, const float* br,
+                       float* logits, int32_t* topk_ids, float* topk_w, float* psum, void* ws,
+                       size_t ws_bytes, void* stream);
+
+/* [MoE 模型原理 §4.1–§4.3, §5] Histogram, capacity, first-come positions in
+ * (token, rank) order, and the permutation xd[slot_row[t,r]] = x[t] for
+ * every kept slot.  Writes counts, kept, offsets, slot_row, row_token, xd. */
+moe_status_t moe_dispatch(const moe_config_t* cfg, const void* x, const int32_t* topk_ids,
+                          int32_t* counts, int32_t* kept, int32_t* offsets, int32_t* slot_row,
+                          int32_t* row_token, void* xd, void* ws, size_t ws_bytes, void* stream);
+
+/* [MoE 模型原理 §1] First expert GEMM over the ragged groups given by
+ * offsets: H[rows of e] = σ(xd[rows of e] W1[e]ᵀ + b1[e]). */
+moe_status_t moe_ffn_up(const moe_config_t* cfg, const void* xd, const int32_t* offsets,
+                        const void* W1, const float* b1, void* H, void* ws, size_t ws_bytes,
+                        void* stream);
+
+/* [MoE 模型原理 §1] Second expert GEMM: yd[rows of e] = H W2[e]ᵀ + b2[e]. */
+moe_status_t moe_ffn_down(const moe_config_t* cfg, const void* H, const int32_t* offsets,
+                          const void* W2, const float* b2, void* yd, void* ws, size_t ws_bytes,
+                          void* stream);
+
+/* moe_ffn_up followed by moe_ffn_down. */
+moe_status_t moe_expert_ffn(const moe_config_t* cfg, const void* xd, const int32_t* offsets,
+                            const void* W1, const float* b1, const void* W2, const float* b2,
+                            void* H, void* yd, void* ws, size_t ws_bytes, void* stream);
+
+/* [MoE 模型原理 §2.2, §5] y[t] = Σ_{r: slot_row[t,r] >= 0} topk_w[t,r]·yd[slot_row[t,r]],
+ * summed in rank order in fp32; 0 for a token whose slots were all dropped.
+ * Deterministic (no atomics). */
+moe_status_t moe_combine(const moe_config_t* cfg, const void* yd, const int32_t* slot_row,
+                         const float* topk_w, void* y, void* stream);
+
+/* [MoE 模型原理 §3.2] f = counts/T, p̄ = psum/T, L_aux = α·E·Σ f·p̄. */
+moe_status_t moe_aux_stats(const moe_config_t* cfg, const int32_t* counts, const float* psum,
+                           float alpha, float* f, float* pbar, float* l_aux, void* stream);
+
+/* The whole layer: route, dispatch, expert FFN, combine, aux. */
+moe_status_t moe_forward(const moe_config_t* cfg, const moe_tensors_t* t, float alpha, void* ws,
+                         size_t ws_bytes, void* stream);
+
+/* Read the workspace's device status word (a blocking copy; call after the
+ * stream that used ws has been synchronised).  *status is MOE_OK or the
+ * first asynchronous error recorded. */
+moe_status_t moe_get_device_status(const void* ws, int32_t* status);
+
+/* Kernel launches this library has issued since load (all threads). */
+int64_t moe_launch_count(void);
+
+const char* moe_status_string(moe_status_t s);
+
+/* Message for the last synchronous error on the calling thread ("" if none). */
+const char* moe_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_H_ */

@@ -7,14 +7,12 @@ tensors for device memory and streams) into that library; importing this
 package does not load it until a binding is used.
 """
 
-__all__ = ["inputs", "moe"]
+import importlib
+
+__all__ = ["inputs", "moe", "build"]
 
 
 def __getattr__(name):
-    if name == "moe":
-        from . import moe as _moe
-        return _moe
-    if name == "inputs":
-        from . import inputs as _inputs
-        return _inputs
+    if name in __all__:
+        return importlib.import_module(f"{__name__}.{name}")
     raise AttributeError(name)

@@ -1,0 +1,297 @@
+// C ABI of libmoe.so: argument checks, workspace layout, and the order of the
+// kernel launches for each stage.  See include/moe.h for the contract.
+#include <atomic>
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <string>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+static std::atomic<int64_t> g_launches{0};
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+static thread_local std::string g_last_error;
+
+static moe_status_t fail(moe_status_t code, const std::string& msg) {
+  g_last_error = msg;
+  return code;
+}
+
+static moe_status_t cuda_fail(cudaError_t e, const char* where) {
+  return fail(MOE_ERR_CUDA, std::string(where) + ": " + cudaGetErrorString(e));
+}
+
+// [MoE 模型原理 §4.1] C = ceil(c·T·k/E) for the exact binary value of c:
+// write c = m·2^p with m a 53-bit integer; then C = ceil(m·T·k·2^p / E),
+// evaluated in unsigned 128-bit integers.
+static int64_t capacity_of(int64_t T, int32_t k, int32_t E, double c) {
+  if (!(c >= std::ldexp(1.0, -30) && c <= std::ldexp(1.0, 30))) return -1;
+  int p = 0;
+  const double frac = std::frexp(c, &p);                 // c = frac·2^p, frac in [0.5, 1)
+  unsigned long long m = (unsigned long long)std::ldexp(frac, 53);
+  p -= 53;                                               // c = m·2^p
+  const int tz = __builtin_ctzll(m);
+  m >>= tz;
+  p += tz;
+  unsigned __int128 num = (unsigned __int128)m * (unsigned long long)T * (unsigned long long)k;
+  unsigned __int128 den = (unsigned long long)E;
+  if (p > 0) num <<= p;
+  if (p < 0) den <<= -p;
+  return (int64_t)(num / den + (num % den != 0 ? 1 : 0));
+}
+
+static moe_status_t check_cfg(const moe_config_t* c) {
+  if (!c) return fail(MOE_ERR_INVALID_ARG, "cfg is NULL");
+  if (c->T < 1) return fail(MOE_ERR_INVALID_ARG, "T must be >= 1");
+  if (c->E < 1 || c->E > 1024) return fail(MOE_ERR_INVALID_ARG, "E must be in [1, 1024]");
+  if (c->k < 1 || c->k > 16 || c->k > c->E)
+    return fail(MOE_ERR_INVALID_ARG, "k must be in [1, min(16, E)]");
+  if (c->T * int64_t(c->k) >= (int64_t(1) << 31))
+    return fail(MOE_ERR_INVALID_ARG, "T*k must be < 2^31");
+  if (c->d < 8 || c->d % 8 != 0) return fail(MOE_ERR_INVALID_ARG, "d must be a multiple of 8");
+  if (c->d_ff < 8 || c->d_ff % 8 != 0)
+    return fail(MOE_ERR_INVALID_ARG, "d_ff must be a multiple of 8");
+  if (!(c->capacity_factor >= std::ldexp(1.0, -30) && c->capacity_factor <= std::ldexp(1.0, 30)))
+    return fail(MOE_ERR_INVALID_ARG, "capacity_factor must be in [2^-30, 2^30]");
+  if (c->dtype != MOE_DT_F32 && c->dtype != MOE_DT_BF16)
+    return fail(MOE_ERR_UNSUPPORTED, "dtype must be MOE_DT_F32 or MOE_DT_BF16");
+  if (c->act != MOE_ACT_RELU && c->act != MOE_ACT_GELU_TANH)
+    return fail(MOE_ERR_UNSUPPORTED, "act must be MOE_ACT_RELU or MOE_ACT_GELU_TANH");
+  return MOE_OK;
+}
+
+static size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+static WsLayout layout_of(const moe_config_t& c) {
+  WsLayout L{};
+  L.n_chunks = (c.T + kChunkTokens - 1) / kChunkTokens;
+  const int64_t rb_simt = (c.T + kRouteTokensSimt - 1) / kRouteTokensSimt;
+  const int64_t rb_tc = (c.T + kRouteTileM - 1) / kRouteTileM;
+  L.n_route_blocks = rb_simt > rb_tc ? rb_simt : rb_tc;
+  size_t off = 0;
+  L.status = off;
+  off += 256;
+  L.chunk_counts = off;
+  off += align256(size_t(L.n_chunks) * c.E * sizeof(int32_t));
+  L.psum_partial = off;
+  off += align256(size_t(L.n_route_blocks) * c.E * sizeof(float));
+  L.total = off;
+  return L;
+}
+
+struct Ws {
+  int32_t* status;
+  int32_t* chunk_counts;
+  float* psum_partial;
+};
+
+static moe_status_t get_ws(const moe_config_t& c, void* ws, size_t ws_bytes, Ws* out) {
+  const WsLayout L = layout_of(c);
+  if (!ws) return fail(MOE_ERR_INVALID_ARG, "workspace is NULL");
+  if ((reinterpret_cast<uintptr_t>(ws) & 255) != 0)
+    return fail(MOE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  if (ws_bytes < L.total)
+    return fail(MOE_ERR_WORKSPACE, "workspace smaller than moe_workspace_size()");
+  char* b = static_cast<char*>(ws);
+  out->status = reinterpret_cast<int32_t*>(b + L.status);
+  out->chunk_counts = reinterpret_cast<int32_t*>(b + L.chunk_counts);
+  out->psum_partial = reinterpret_cast<float*>(b + L.psum_partial);
+  return MOE_OK;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// Which expert GEMM runs for bf16 layers: the tcgen05 kernel by default;
+// MOE_FFN_IMPL=simt selects the CUDA-core kernel (a cross-check in tests).
+static bool use_tc_gemm(const moe_config_t& c) {
+  if (c.dtype != MOE_DT_BF16) return false;
+  const char* v = std::getenv("MOE_FFN_IMPL");
+  return !(v && std::strcmp(v, "simt") == 0);
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int64_t moe_capacity(const moe_config_t* cfg) {
+  if (check_cfg(cfg) != MOE_OK) return -1;
+  return capacity_of(cfg->T, cfg->k, cfg->E, cfg->capacity_factor);
+}
+
+int64_t moe_max_rows(const moe_config_t* cfg) {
+  const int64_t C = moe_capacity(cfg);
+  if (C < 0) return -1;
+  const int64_t a = cfg->T * cfg->k, b = C * cfg->E;
+  return a < b ? a : b;
+}
+
+moe_status_t moe_workspace_size(const moe_config_t* cfg, size_t* bytes) {
+  moe_status_t s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  if (!bytes) return fail(MOE_ERR_INVALID_ARG, "bytes is NULL");
+  *bytes = layout_of(*cfg).total;
+  return MOE_OK;
+}
+
+moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, void* stream) {
+  if (!ws || ws_bytes < 256) return fail(MOE_ERR_INVALID_ARG, "workspace too small");
+  cudaError_t e = cudaMemsetAsync(ws, 0, 256, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_workspace_init");
+}
+
+moe_status_t moe_route(const moe_config_t* cfg, const void* x, const void* Wr, const float* br,
+                       float* logits, int32_t* topk_ids, float* topk_w, float* psum, void* ws,
+                       size_t ws_bytes, void* stream) {
+  moe_status_t s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  if (!x || !Wr || !br || !topk_ids || !topk_w || !psum)
+    return fail(MOE_ERR_INVALID_ARG, "moe_route: NULL tensor");
+  if (cfg->write_logits && !logits)
+    return fail(MOE_ERR_INVALID_ARG, "moe_route: write_logits set but logits is NULL");
+  Ws w;
+  if ((s = get_ws(*cfg, ws, ws_bytes, &w)) != MOE_OK) return s;
+  cudaError_t e = launch_route_simt(*cfg, x, Wr, br, cfg->write_logits ? logits : nullptr,
+                                    topk_ids, topk_w, w.psum_partial, psum,
+                                    static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_route");
+}
+
+moe_status_t moe_dispatch(const moe_config_t* cfg, const void* x, const int32_t* topk_ids,
+                          int32_t* counts, int32_t* kept, int32_t* offsets, int32_t* slot_row,
+                          int32_t* row_token, void* xd, void* ws, size_t ws_bytes, void* stream) {
+  moe_status_t s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  if (!x || !topk_ids || !counts || !kept || !offsets || !slot_row || !row_token || !xd)
+    return fail(MOE_ERR_INVALID_ARG, "moe_dispatch: NULL tensor");
+  if (!aligned16(x) || !aligned16(xd))
+    return fail(MOE_ERR_INVALID_ARG, "moe_dispatch: x and xd must be 16-byte aligned");
+  Ws w;
+  if ((s = get_ws(*cfg, ws, ws_bytes, &w)) != MOE_OK) return s;
+  const int64_t C = capacity_of(cfg->T, cfg->k, cfg->E, cfg->capacity_factor);
+  cudaError_t e = launch_dispatch(*cfg, C, x, topk_ids, counts, kept, offsets, slot_row,
+                                  row_token, xd, w.chunk_counts, w.status,
+                                  static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_dispatch");
+}
+
+moe_status_t moe_ffn_up(const moe_config_t* cfg, const void* xd, const int32_t* offsets,
+                        const void* W1, const float* b1, void* H, void* ws, size_t ws_bytes,
+                        void* stream) {
+  moe_status_t s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  if (!xd || !offsets || !W1 || !b1 || !H)
+    return fail(MOE_ERR_INVALID_ARG, "moe_ffn_up: NULL tensor");
+  if (!aligned16(xd) || !aligned16(W1) || !aligned16(H))
+    return fail(MOE_ERR_INVALID_ARG, "moe_ffn_up: xd, W1, H must be 16-byte aligned");
+  Ws w;
+  if ((s = get_ws(*cfg, ws, ws_bytes, &w)) != MOE_OK) return s;
+  const int64_t R = moe_max_rows(cfg);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = use_tc_gemm(*cfg)
+                      ? launch_gemm_tc(cfg->E, cfg->d_ff, cfg->d, R, offsets, xd, W1, b1,
+                                       cfg->act, H, w.status, st)
+                      : launch_gemm_simt(cfg->dtype, cfg->E, cfg->d_ff, cfg->d, R, offsets, xd,
+                                         W1, b1, cfg->act, H, st);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_ffn_up");
+}
+
+moe_status_t moe_ffn_down(const moe_config_t* cfg, const void* H, const int32_t* offsets,
+                          const void* W2, const float* b2, void* yd, void* ws, size_t ws_bytes,
+                          void* stream) {
+  moe_status_t s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  if (!H || !offsets || !W2 || !b2 || !yd)
+    return fail(MOE_ERR_INVALID_ARG, "moe_ffn_down: NULL tensor");
+  if (!aligned16(H) || !aligned16(W2) || !aligned16(yd))
+    return fail(MOE_ERR_INVALID_ARG, "moe_ffn_down: H, W2, yd must be 16-byte aligned");
+  Ws w;
+  if ((s = get_ws(*cfg, ws, ws_bytes, &w)) != MOE_OK) return s;
+  const int64_t R = moe_max_rows(cfg);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = use_tc_gemm(*cfg)
+                      ? launch_gemm_tc(cfg->E, cfg->d, cfg->d_ff, R, offsets, H, W2, b2, -1, yd,
+                                       w.status, st)
+                      : launch_gemm_simt(cfg->dtype, cfg->E, cfg->d, cfg->d_ff, R, offsets, H,
+                                         W2, b2, -1, yd, st);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_ffn_down");
+}
+
+moe_status_t moe_expert_ffn(const moe_config_t* cfg, const void* xd, const int32_t* offsets,
+                            const void* W1, const float* b1, const void* W2, const float* b2,
+                            void* H, void* yd, void* ws, size_t ws_bytes, void* stream) {
+  moe_status_t s = moe_ffn_up(cfg, xd, offsets, W1, b1, H, ws, ws_bytes, stream);
+  if (s != MOE_OK) return s;
+  return moe_ffn_down(cfg, H, offsets, W2, b2, yd, ws, ws_bytes, stream);
+}
+
+moe_status_t moe_combine(const moe_config_t* cfg, const void* yd, const int32_t* slot_row,
+                         const float* topk_w, void* y, void* stream) {
+  moe_status_t s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  if (!yd || !slot_row || !topk_w || !y)
+    return fail(MOE_ERR_INVALID_ARG, "moe_combine: NULL tensor");
+  if (!aligned16(yd) || !aligned16(y))
+    return fail(MOE_ERR_INVALID_ARG, "moe_combine: yd and y must be 16-byte aligned");
+  cudaError_t e = launch_combine(*cfg, moe_max_rows(cfg), yd, slot_row, topk_w, y,
+                                 static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_combine");
+}
+
+moe_status_t moe_aux_stats(const moe_config_t* cfg, const int32_t* counts, const float* psum,
+                           float alpha, float* f, float* pbar, float* l_aux, void* stream) {
+  moe_status_t s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  if (!counts || !psum || !f || !pbar || !l_aux)
+    return fail(MOE_ERR_INVALID_ARG, "moe_aux_stats: NULL tensor");
+  cudaError_t e = launch_aux(*cfg, counts, psum, alpha, f, pbar, l_aux,
+                             static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_aux_stats");
+}
+
+moe_status_t moe_forward(const moe_config_t* cfg, const moe_tensors_t* t, float alpha, void* ws,
+                         size_t ws_bytes, void* stream) {
+  if (!t) return fail(MOE_ERR_INVALID_ARG, "moe_forward: tensors is NULL");
+  moe_status_t s;
+  if ((s = moe_route(cfg, t->x, t->Wr, t->br, t->logits, t->topk_ids, t->topk_w, t->psum, ws,
+                     ws_bytes, stream)) != MOE_OK)
+    return s;
+  if ((s = moe_dispatch(cfg, t->x, t->topk_ids, t->counts, t->kept, t->offsets, t->slot_row,
+                        t->row_token, t->xd, ws, ws_bytes, stream)) != MOE_OK)
+    return s;
+  if ((s = moe_expert_ffn(cfg, t->xd, t->offsets, t->W1, t->b1, t->W2, t->b2, t->H, t->yd, ws,
+                          ws_bytes, stream)) != MOE_OK)
+    return s;
+  if ((s = moe_combine(cfg, t->yd, t->slot_row, t->topk_w, t->y, stream)) != MOE_OK) return s;
+  return moe_aux_stats(cfg, t->counts, t->psum, alpha, t->f, t->pbar, t->l_aux, stream);
+}
+
+moe_status_t moe_get_device_status(const void* ws, int32_t* status) {
+  if (!ws || !status) return fail(MOE_ERR_INVALID_ARG, "moe_get_device_status: NULL argument");
+  cudaError_t e = cudaMemcpy(status, ws, sizeof(int32_t), cudaMemcpyDeviceToHost);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_get_device_status");
+}
+
+int64_t moe_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+const char* moe_status_string(moe_status_t s) {
+  switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+    default: return "MOE_ERR_UNKNOWN";
+  }
+}
+
+const char* moe_last_error(void) { return g_last_error.c_str(); }
+
+}  // extern "C"

@@ -1,0 +1,145 @@
+// Combine and load statistics.
+//
+// [MoE 模型原理 §2.2] y_t = Σ_{i∈S_t} p̃_{t,i} E_i(x_t); [MoE 模型原理 §5] the
+// expert outputs return to token order and are merged with the routing
+// weights.  Dropped slots contribute nothing and the kept weights are not
+// renormalised; a token with every slot dropped gets 0 (the caller adds the
+// residual).  One warp per token, 16-byte vectors, fp32 sums in rank order —
+// no atomics, so the result is deterministic.
+//
+// [MoE 模型原理 §3.2] f_i = counts_i/T, p̄_i = Σ_t p_{t,i}/T,
+// L_aux = α·E·Σ_i f_i p̄_i.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+constexpr int kMaxK = 16;  // largest k the library accepts
+
+template <typename T>
+struct Vec;
+template <>
+struct Vec<__nv_bfloat16> {
+  static constexpr int N = 8;
+  __device__ static void unpack(const uint4& v, float* f) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float2 p = __bfloat1622float2(h[i]);
+      f[2 * i] = p.x;
+      f[2 * i + 1] = p.y;
+    }
+  }
+  __device__ static uint4 pack(const float* f) {
+    uint4 v;
+    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+    return v;
+  }
+};
+template <>
+struct Vec<float> {
+  static constexpr int N = 4;
+  __device__ static void unpack(const uint4& v, float* f) {
+    f[0] = __uint_as_float(v.x);
+    f[1] = __uint_as_float(v.y);
+    f[2] = __uint_as_float(v.z);
+    f[3] = __uint_as_float(v.w);
+  }
+  __device__ static uint4 pack(const float* f) {
+    return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                      __float_as_uint(f[3]));
+  }
+};
+
+template <typename T>
+__global__ void __launch_bounds__(256)
+    combine_kernel(int64_t n_tok, int k, int64_t row_vecs, int64_t max_rows,
+                   const uint4* __restrict__ yd,
+                   const int32_t* __restrict__ slot_row, const float* __restrict__ w,
+                   uint4* __restrict__ y) {
+  constexpr int NV = Vec<T>::N;
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = int64_t(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t t = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); t < n_tok;
+       t += warps) {
+    const int32_t my_row = lane < k ? slot_row[t * k + lane] : -1;
+    const float my_w = lane < k ? w[t * k + lane] : 0.f;
+    int32_t rows[kMaxK];
+    float wts[kMaxK];
+#pragma unroll
+    for (int r = 0; r < kMaxK; ++r) {
+      rows[r] = __shfl_sync(0xffffffffu, my_row, r);
+      wts[r] = __shfl_sync(0xffffffffu, my_w, r);
+    }
+    for (int64_t v = lane; v < row_vecs; v += 32) {
+      float acc[NV];
+#pragma unroll
+      for (int i = 0; i < NV; ++i) acc[i] = 0.f;
+#pragma unroll
+      for (int r = 0; r < kMaxK; ++r) {
+        if (r < k && rows[r] >= 0 && rows[r] < max_rows) {
+          float f[NV];
+          Vec<T>::unpack(yd[int64_t(rows[r]) * row_vecs + v], f);
+#pragma unroll
+          for (int i = 0; i < NV; ++i) acc[i] = fmaf(wts[r], f[i], acc[i]);
+        }
+      }
+      y[t * row_vecs + v] = Vec<T>::pack(acc);
+    }
+  }
+}
+
+// One CTA; thread i handles expert i (E <= 1024), then a fixed-shape tree sum.
+__global__ void __launch_bounds__(1024)
+    aux_kernel(int E, int64_t T, float alpha, const int32_t* __restrict__ counts,
+               const float* __restrict__ psum, float* f, float* pbar, float* l_aux) {
+  __shared__ float red[1024];
+  const int i = threadIdx.x;
+  float prod = 0.f;
+  if (i < E) {
+    const float fi = float(counts[i]) / float(T);
+    const float pi = psum[i] / float(T);
+    f[i] = fi;
+    pbar[i] = pi;
+    prod = fi * pi;
+  }
+  red[i] = prod;
+  __syncthreads();
+  for (int s = 512; s > 0; s >>= 1) {
+    if (i < s) red[i] += red[i + s];
+    __syncthreads();
+  }
+  if (i == 0) *l_aux = alpha * float(E) * red[0];
+}
+
+cudaError_t launch_combine(const moe_config_t& c, int64_t max_rows, const void* yd,
+                           const int32_t* slot_row, const float* w, void* y, cudaStream_t st) {
+  const int elem = c.dtype == MOE_DT_BF16 ? 2 : 4;
+  const int64_t row_vecs = int64_t(c.d) * elem / 16;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t want = (c.T + 7) / 8;
+  const unsigned grid = unsigned(want < int64_t(sms) * 8 ? want : int64_t(sms) * 8);
+  if (c.dtype == MOE_DT_BF16)
+    combine_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(c.T, c.k, row_vecs, max_rows,
+                                                        static_cast<const uint4*>(yd), slot_row,
+                                                        w, static_cast<uint4*>(y));
+  else
+    combine_kernel<float><<<grid, 256, 0, st>>>(c.T, c.k, row_vecs, max_rows,
+                                                static_cast<const uint4*>(yd),
+                                                slot_row, w, static_cast<uint4*>(y));
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_aux(const moe_config_t& c, const int32_t* counts, const float* psum,
+                       float alpha, float* f, float* pbar, float* l_aux, cudaStream_t st) {
+  aux_kernel<<<1, 1024, 0, st>>>(c.E, c.T, alpha, counts, psum, f, pbar, l_aux);
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,239 @@
+// Dispatch: expert histogram, capacity, first-come positions and the token
+// permutation into the per-expert buffer.
+//
+// [MoE 模型原理 §4.1] C = ceil(c·T·k/E).
+// [MoE 模型原理 §4.2] each expert keeps at most C slots, the earliest ones;
+//   capacity is per expert and never moves to another expert.
+// [MoE 模型原理 §4.3] overflow slots are dropped (the residual path).
+// [MoE 模型原理 §5]   kept slots are gathered into one contiguous buffer,
+//   expert by expert ("dispatch_mask or an equivalent index").
+//
+// Position of slot (t, r) routed to expert e = number of earlier tokens t' < t
+// that also routed to e (a token selects each expert at most once, so the
+// (token, rank) order within an expert is plain token order).  It is built in
+// three integer passes and never materialises a T×E one-hot mask:
+//   1. histogram per chunk of 256 tokens         chunk_counts[chunk][e]
+//   2. per-expert exclusive scan over chunks     chunk_counts -> chunk bases,
+//      counts[e], kept[e] = min(counts[e], C)
+//   3. per chunk: expert offsets (scan of kept), per-warp bases, then each
+//      warp walks its 32 tokens in order: slot_row, row_token
+// and a fourth, bandwidth-bound pass copies each token row once from x and
+// writes it to every kept slot with 16-byte vectors.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+constexpr int kDispatchThreads = 256;  // 8 warps × 32 tokens = one chunk
+static_assert(kDispatchThreads == kChunkTokens, "one token per thread in a chunk");
+
+__global__ void __launch_bounds__(kDispatchThreads)
+    histogram_kernel(int64_t T, int E, int k, const int32_t* __restrict__ ids,
+                     int32_t* __restrict__ chunk_counts, int32_t* status) {
+  extern __shared__ int32_t hist[];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+  __syncthreads();
+  const int64_t t = int64_t(blockIdx.x) * kChunkTokens + threadIdx.x;
+  if (t < T) {
+    for (int r = 0; r < k; ++r) {
+      const int e = ids[t * k + r];
+      if (e >= 0 && e < E)
+        atomicAdd(&hist[e], 1);
+      else
+        set_status(status, MOE_ERR_INVALID_ARG);
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    chunk_counts[int64_t(blockIdx.x) * E + e] = hist[e];
+}
+
+// One CTA per expert: exclusive scan of that expert's chunk counts (in place),
+// total count and kept = min(count, C).
+__global__ void __launch_bounds__(256)
+    expert_scan_kernel(int64_t n_chunks, int E, int64_t C, int32_t* __restrict__ chunk_counts,
+                       int32_t* __restrict__ counts, int32_t* __restrict__ kept) {
+  __shared__ int32_t warp_tot[8];
+  __shared__ int32_t carry;
+  const int e = blockIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) carry = 0;
+  __syncthreads();
+  for (int64_t base = 0; base < n_chunks; base += blockDim.x) {
+    const int64_t ch = base + threadIdx.x;
+    const int32_t v = ch < n_chunks ? chunk_counts[ch * E + e] : 0;
+    int32_t incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int32_t u = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += u;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    int32_t before = carry;
+    for (int w = 0; w < warp; ++w) before += warp_tot[w];
+    if (ch < n_chunks) chunk_counts[ch * E + e] = before + incl - v;
+    __syncthreads();
+    if (threadIdx.x == blockDim.x - 1) carry = before + incl;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    counts[e] = carry;
+    kept[e] = int32_t(carry < C ? carry : C);
+  }
+}
+
+// One CTA per chunk of 256 tokens; warp w owns tokens [32w, 32w+32) of it.
+// Dynamic shared memory: off[E+1] | wbase[8][E].
+__global__ void __launch_bounds__(kDispatchThreads)
+    assign_kernel(int64_t T, int E, int k, int64_t C, const int32_t* __restrict__ ids,
+                  const int32_t* __restrict__ chunk_base, const int32_t* __restrict__ kept,
+                  int32_t* __restrict__ offsets, int32_t* __restrict__ slot_row,
+                  int32_t* __restrict__ row_token) {
+  extern __shared__ int32_t sm[];
+  int32_t* off = sm;              // [E+1]
+  int32_t* wbase = sm + E + 1;    // [8][E]
+  __shared__ int32_t part[kDispatchThreads];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+  // Expert offsets: exclusive scan of kept[0..E).  Thread i sums a run of
+  // consecutive experts, then a scan over the 256 run totals.
+  const int per = (E + kDispatchThreads - 1) / kDispatchThreads;
+  const int lo = tid * per, hi = min(E, lo + per);
+  int32_t run = 0;
+  for (int e = lo; e < hi; ++e) run += kept[e];
+  part[tid] = run;
+  __syncthreads();
+  if (tid == 0) {
+    int32_t acc = 0;
+    for (int i = 0; i < kDispatchThreads; ++i) {
+      int32_t v = part[i];
+      part[i] = acc;
+      acc += v;
+    }
+    off[E] = acc;
+  }
+  __syncthreads();
+  {
+    int32_t acc = part[tid];
+    for (int e = lo; e < hi; ++e) {
+      off[e] = acc;
+      acc += kept[e];
+    }
+  }
+  for (int i = tid; i < 8 * E; i += kDispatchThreads) wbase[i] = 0;
+  __syncthreads();
+  if (blockIdx.x == 0)
+    for (int e = tid; e <= E; e += kDispatchThreads) offsets[e] = off[e];
+
+  // Per-warp histograms of this chunk.
+  const int64_t chunk0 = int64_t(blockIdx.x) * kChunkTokens;
+  const int64_t t_own = chunk0 + tid;
+  if (t_own < T)
+    for (int r = 0; r < k; ++r) {
+      const int e = ids[t_own * k + r];
+      if (e >= 0 && e < E) atomicAdd(&wbase[warp * E + e], 1);
+    }
+  __syncthreads();
+  // wbase[w][e] <- chunk base of e + counts of e in warps before w.
+  for (int e = tid; e < E; e += kDispatchThreads) {
+    int32_t acc = chunk_base[int64_t(blockIdx.x) * E + e];
+    for (int w = 0; w < 8; ++w) {
+      const int32_t v = wbase[w * E + e];
+      wbase[w * E + e] = acc;
+      acc += v;
+    }
+  }
+  __syncthreads();
+  // Walk the warp's tokens in order; lane r handles rank r of the token.
+  int32_t* my = wbase + warp * E;
+  for (int j = 0; j < 32; ++j) {
+    const int64_t t = chunk0 + warp * 32 + j;
+    if (t >= T) break;
+    if (lane < k) {
+      const int e = ids[t * k + lane];
+      int32_t row = -1;
+      if (e >= 0 && e < E) {
+        const int32_t pos = my[e]++;
+        if (pos < C) {
+          row = off[e] + pos;
+          row_token[row] = int32_t(t);
+        }
+      }
+      slot_row[t * k + lane] = row;
+    }
+    __syncwarp();
+  }
+}
+
+// xd[slot_row[t,r]] = x[t] for every kept slot; one warp per token, the row
+// is read once (16-byte vectors, 4 in flight per lane) and written k times.
+__global__ void __launch_bounds__(256)
+    scatter_rows_kernel(int64_t T, int k, int64_t row_vecs, const uint4* __restrict__ x,
+                        const int32_t* __restrict__ slot_row, uint4* __restrict__ xd) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = int64_t(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t t = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T;
+       t += warps) {
+    const int32_t my_row = lane < k ? slot_row[t * k + lane] : -1;
+    const unsigned kept_mask = __ballot_sync(0xffffffffu, my_row >= 0);
+    if (kept_mask == 0) continue;
+    const uint4* src = x + t * row_vecs;
+    for (int64_t v0 = 0; v0 < row_vecs; v0 += 4 * 32) {
+      uint4 buf[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int64_t v = v0 + u * 32 + lane;
+        if (v < row_vecs) buf[u] = __ldcs(src + v);
+      }
+      unsigned m = kept_mask;
+      while (m) {
+        const int r = __ffs(m) - 1;
+        m &= m - 1;
+        const int32_t row = __shfl_sync(0xffffffffu, my_row, r);
+        uint4* dst = xd + int64_t(row) * row_vecs;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int64_t v = v0 + u * 32 + lane;
+          if (v < row_vecs) dst[v] = buf[u];
+        }
+      }
+    }
+  }
+}
+
+cudaError_t launch_dispatch(const moe_config_t& c, int64_t C, const void* x,
+                            const int32_t* ids, int32_t* counts, int32_t* kept,
+                            int32_t* offsets, int32_t* slot_row, int32_t* row_token, void* xd,
+                            int32_t* chunk_counts, int32_t* status, cudaStream_t st) {
+  const int64_t n_chunks = (c.T + kChunkTokens - 1) / kChunkTokens;
+  cudaError_t err;
+  histogram_kernel<<<unsigned(n_chunks), kDispatchThreads, size_t(c.E) * 4, st>>>(
+      c.T, c.E, c.k, ids, chunk_counts, status);
+  count_launch();
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  expert_scan_kernel<<<unsigned(c.E), 256, 0, st>>>(n_chunks, c.E, C, chunk_counts, counts, kept);
+  count_launch();
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  const size_t smem = size_t(c.E + 1 + 8 * c.E) * 4;
+  err = cudaFuncSetAttribute(assign_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(smem));
+  if (err != cudaSuccess) return err;
+  assign_kernel<<<unsigned(n_chunks), kDispatchThreads, smem, st>>>(
+      c.T, c.E, c.k, C, ids, chunk_counts, kept, offsets, slot_row, row_token);
+  count_launch();
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  const int elem = c.dtype == MOE_DT_BF16 ? 2 : 4;
+  const int64_t row_vecs = int64_t(c.d) * elem / 16;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t want = (c.T + 7) / 8;
+  const unsigned grid = unsigned(want < int64_t(sms) * 8 ? want : int64_t(sms) * 8);
+  scatter_rows_kernel<<<grid, 256, 0, st>>>(c.T, c.k, row_vecs, static_cast<const uint4*>(x),
+                                            slot_row, static_cast<uint4*>(xd));
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,351 @@
+// Grouped expert GEMM on the sm_103a tensor cores (tcgen05 + TMA + TMEM).
+//
+// [MoE 模型原理 §1] E_i(x) = W2 σ(W1 x + b1) + b2; the experts' GEMMs run as
+// one grouped GEMM over the ragged row ranges of the dispatch buffer
+// (offsets[e] .. offsets[e+1]), so only kept rows are computed — no padding
+// to a fixed capacity ([MoE 模型原理 §8.4]).
+//
+//   out[rows of e, n] = epi( Σ_k A[row, k] · B[e, n, k] + bias[e, n] )
+//   A [R, K] bf16 (K contiguous), B [E, N, K] bf16 (K contiguous),
+//   epi = σ then round to bf16 (first GEMM) or round to bf16 (second GEMM).
+//
+// Design: a persistent kernel, one CTA per SM, 6 warps:
+//   warp 0     TMA producer: 128×64 A tile + BN×64 B tile per stage, 128-byte
+//              swizzle, kStages-deep ring of shared-memory stages
+//   warp 1     TMEM allocator and MMA issuer: tcgen05.mma M=128, N=BN, K=16,
+//              fp32 accumulators in tensor memory, two accumulator buffers so
+//              the epilogue of one tile overlaps the main loop of the next
+//   warps 2-5  epilogue: tcgen05.ld one row per thread, bias, σ, bf16,
+//              masked 16-byte stores (rows past the expert's end are skipped)
+// Tiles never straddle two experts.  Tile order is expert-major, and within
+// an expert m-fastest, so a wave of CTAs shares the weight tile B[e, n-tile]
+// through L2 while the expert's A rows stay L2-resident across n-tiles.
+// Every wait is bounded: on a timeout the kernel records MOE_ERR_TIMEOUT,
+// drains its own copies and MMAs, frees its tensor memory and returns.
+#include <cstdio>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kTileM = 128;
+constexpr int kTileK = 64;              // 64 bf16 = one 128-byte swizzle row
+constexpr int kStages = 4;
+constexpr int kThreads = 192;
+constexpr int kEpiWarp0 = 2;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kAccCols = 256;           // each of the two accumulators owns 256 columns
+constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s
+constexpr int kMaxExperts = 1024;
+
+struct TileCoord {
+  int e, m0, m_end, n0;
+};
+
+__device__ __forceinline__ TileCoord tile_coord(int64_t i, const int* mt_prefix, int E, int n_tn,
+                                                const int32_t* offsets_s, int BN) {
+  // Find e with mt_prefix[e]*n_tn <= i < mt_prefix[e+1]*n_tn.
+  int lo = 0, hi = E;  // invariant: prefix[lo]*n_tn <= i < prefix[hi]*n_tn
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (int64_t(mt_prefix[mid]) * n_tn <= i)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  const int e = lo;
+  const int mts = mt_prefix[e + 1] - mt_prefix[e];
+  const int64_t local = i - int64_t(mt_prefix[e]) * n_tn;
+  const int nt = int(local / mts), mt = int(local % mts);
+  TileCoord c;
+  c.e = e;
+  c.m0 = offsets_s[e] + mt * kTileM;
+  c.m_end = offsets_s[e + 1] > offsets_s[e] ? offsets_s[e + 1] : offsets_s[e];
+  c.n0 = nt * BN;
+  return c;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   int E, int N, int K, int BN, const int32_t* __restrict__ offsets,
+                   const float* __restrict__ bias, int act, __nv_bfloat16* __restrict__ out,
+                   int64_t max_rows, int32_t* status) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  __shared__ uint64_t full_bar[kStages], empty_bar[kStages];
+  __shared__ uint64_t tfull_bar[2], tempty_bar[2], drain_bar;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  __shared__ int s_mt[kMaxExperts + 1];
+  __shared__ int32_t s_off[kMaxExperts + 1];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const uint32_t a_bytes = kTileM * kTileK * 2;
+  const uint32_t b_bytes = uint32_t(BN) * kTileK * 2;
+  uint8_t* sA = smem;                       // kStages × a_bytes
+  uint8_t* sB = smem + kStages * a_bytes;   // kStages × b_bytes
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      tc::mbar_init(&full_bar[s], 1);
+      tc::mbar_init(&empty_bar[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      tc::mbar_init(&tfull_bar[a], 1);
+      tc::mbar_init(&tempty_bar[a], 4 * 32);
+    }
+    tc::mbar_init(&drain_bar, 1);
+    s_abort = 0;
+    tc::fence_mbar_init();
+    tc::prefetch_tmap(&tmA);
+    tc::prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(&s_tmem, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  // Per-expert m-tile prefix: warp 0 scans runs of experts, one run per lane.
+  // Row offsets are clamped to [0, max_rows] so that no tile can reach
+  // outside the buffers, whatever offsets holds.
+  if (warp == 0) {
+    auto clamp_row = [&](int e) {
+      const int32_t v = offsets[e];
+      return int32_t(v < 0 ? 0 : (int64_t(v) > max_rows ? max_rows : v));
+    };
+    const int per = (E + 31) / 32;
+    const int lo = lane * per, hi = min(E, lo + per);
+    int run = 0;
+    for (int e = lo; e < hi; ++e) {
+      const int32_t a = clamp_row(e), b = clamp_row(e + 1);
+      s_off[e] = a;
+      run += b > a ? (b - a + kTileM - 1) / kTileM : 0;
+    }
+    if (lane == 31) s_off[E] = clamp_row(E);
+    int incl = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += u;
+    }
+    int acc = incl - run;
+    for (int e = lo; e < hi; ++e) {
+      s_mt[e] = acc;
+      const int32_t a = clamp_row(e), b = clamp_row(e + 1);
+      acc += b > a ? (b - a + kTileM - 1) / kTileM : 0;
+    }
+    if (lane == 31) s_mt[E] = incl;
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem_base = s_tmem;
+
+  const int n_tn = (N + BN - 1) / BN;
+  const int64_t total = int64_t(s_mt[E]) * n_tn;
+  const int nk = (K + kTileK - 1) / kTileK;
+  volatile int* abort_flag = &s_abort;
+
+  auto give_up = [&]() {
+    *abort_flag = 1;
+    set_status(status, MOE_ERR_TIMEOUT);
+  };
+
+  if (warp == 0 && lane == 0) {
+    // ---------------- TMA producer ----------------
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t armed_phase[kStages];
+    bool armed[kStages];
+    for (int s = 0; s < kStages; ++s) armed[s] = false, armed_phase[s] = 0;
+    bool ok = true;
+    for (int64_t i = blockIdx.x; i < total && ok; i += gridDim.x) {
+      const TileCoord c = tile_coord(i, s_mt, E, n_tn, s_off, BN);
+      for (int kb = 0; kb < nk; ++kb) {
+        if (!tc::mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, kWaitLimitNs)) {
+          give_up();
+          ok = false;
+          break;
+        }
+        tc::mbar_arrive_expect_tx(&full_bar[stage], a_bytes + b_bytes);
+        tc::tma_load_2d(&tmA, &full_bar[stage], sA + stage * a_bytes, kb * kTileK, c.m0);
+        tc::tma_load_3d(&tmB, &full_bar[stage], sB + stage * b_bytes, kb * kTileK, c.n0, c.e);
+        armed[stage] = true;
+        armed_phase[stage] = phase;
+        if (++stage == kStages) stage = 0, phase ^= 1u;
+      }
+    }
+    // Drain: every copy this thread issued must land before the CTA exits
+    // (already true on the normal path, where the MMA issuer consumed them).
+    for (int s = 0; s < kStages; ++s)
+      if (armed[s]) tc::mbar_wait(&full_bar[s], armed_phase[s], nullptr, kWaitLimitNs);
+  } else if (warp == 1 && lane == 0) {
+    // ---------------- MMA issuer ----------------
+    const uint32_t idesc = tc::idesc_bf16_f32(kTileM, BN);
+    int stage = 0;
+    uint32_t phase = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int64_t i = blockIdx.x; i < total && ok; i += gridDim.x) {
+      if (!tc::mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort_flag, kWaitLimitNs)) {
+        give_up();
+        break;
+      }
+      tc::fence_after_sync();
+      const uint32_t d_tmem = tmem_base + uint32_t(acc * kAccCols);
+      for (int kb = 0; kb < nk; ++kb) {
+        if (!tc::mbar_wait(&full_bar[stage], phase, abort_flag, kWaitLimitNs)) {
+          give_up();
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+        const uint32_t a0 = tc::smem_u32(sA + stage * a_bytes);
+        const uint32_t b0 = tc::smem_u32(sB + stage * b_bytes);
+#pragma unroll
+        for (int j = 0; j < kTileK / 16; ++j)
+          tc::mma_bf16(d_tmem, tc::sdesc_kmajor_sw128(a0 + j * 32),
+                       tc::sdesc_kmajor_sw128(b0 + j * 32), idesc, (kb | j) != 0);
+        tc::mma_commit(&empty_bar[stage]);
+        if (++stage == kStages) stage = 0, phase ^= 1u;
+      }
+      if (!ok) break;
+      tc::mma_commit(&tfull_bar[acc]);
+      if (++acc == 2) acc = 0, acc_phase ^= 1u;
+    }
+    // Drain: wait until every MMA this thread issued has completed.
+    tc::mma_commit(&drain_bar);
+    tc::mbar_wait(&drain_bar, 0, nullptr, kWaitLimitNs);
+  } else if (warp >= kEpiWarp0) {
+    // ---------------- epilogue ----------------
+    const int quarter = warp & 3;  // TMEM lanes [32·quarter, 32·quarter+32)
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int64_t i = blockIdx.x; i < total; i += gridDim.x) {
+      const TileCoord c = tile_coord(i, s_mt, E, n_tn, s_off, BN);
+      if (!tc::mbar_wait(&tfull_bar[acc], acc_phase, abort_flag, kWaitLimitNs)) {
+        give_up();
+        break;
+      }
+      tc::fence_after_sync();
+      const int row = c.m0 + quarter * 32 + lane;
+      const bool row_ok = row < c.m_end;
+      const int ncols = min(BN, N - c.n0);
+      const float* bias_e = bias + int64_t(c.e) * N + c.n0;
+      __nv_bfloat16* out_row = out + int64_t(row) * N + c.n0;
+      const uint32_t t_row = tmem_base + (uint32_t(quarter * 32) << 16) + uint32_t(acc * kAccCols);
+      for (int c0 = 0; c0 < ncols; c0 += 16) {
+        uint32_t r[16];
+        tc::tmem_ld_x16(t_row + uint32_t(c0), r);
+        tc::tmem_ld_wait();
+        if (row_ok) {
+          float v[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            float u = __uint_as_float(r[j]) + (c0 + j < ncols ? __ldg(bias_e + c0 + j) : 0.f);
+            if (act == MOE_ACT_RELU)
+              u = u > 0.f ? u : 0.f;
+            else if (act == MOE_ACT_GELU_TANH)
+              u = 0.5f * u * (1.f + tc::tanh_fast(0.7978845608028654f * (u + 0.044715f * u * u * u)));
+            v[j] = u;
+          }
+          uint4 p[2];
+          __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(p);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) h[j] = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
+          // N is a multiple of 8, so a chunk holds 8 or 16 valid columns.
+          uint4* dst = reinterpret_cast<uint4*>(out_row + c0);
+          dst[0] = p[0];
+          if (c0 + 16 <= ncols) dst[1] = p[1];
+        }
+      }
+      tc::fence_before_sync();
+      tc::mbar_arrive(&tempty_bar[acc]);
+      if (++acc == 2) acc = 0, acc_phase ^= 1u;
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (warp == 1) {
+    __syncwarp();
+    tc::tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode() {
+  static EncodeTiledFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+// Column-tile width: the widest multiple of 16 (<= 256) dividing N, else 256.
+int pick_bn(int N) {
+  for (int bn = 256; bn >= 128; bn -= 16)
+    if (N % bn == 0) return bn;
+  return N < 256 ? ((N + 15) / 16) * 16 : 256;
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_tc(int E, int N, int K, int64_t max_rows, const int32_t* offsets,
+                           const void* A, const void* B, const float* bias, int act, void* out,
+                           int32_t* status, cudaStream_t st) {
+  if (E > kMaxExperts) return cudaErrorInvalidValue;
+  EncodeTiledFn encode = get_encode();
+  if (!encode) return cudaErrorNotSupported;
+  const int BN = pick_bn(N);
+  CUtensorMap tmA, tmB;
+  {
+    const cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(max_rows)};
+    const cuuint64_t strides[1] = {cuuint64_t(K) * 2};
+    const cuuint32_t box[2] = {kTileK, kTileM};
+    const cuuint32_t es[2] = {1, 1};
+    if (encode(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(A), dims, strides, box,
+               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t dims[3] = {cuuint64_t(K), cuuint64_t(N), cuuint64_t(E)};
+    const cuuint64_t strides[2] = {cuuint64_t(K) * 2, cuuint64_t(N) * K * 2};
+    const cuuint32_t box[3] = {kTileK, cuuint32_t(BN), 1};
+    const cuuint32_t es[3] = {1, 1, 1};
+    if (encode(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(B), dims, strides, box,
+               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  const size_t smem = 1024 + size_t(kStages) * (kTileM * kTileK * 2 + size_t(BN) * kTileK * 2);
+  cudaError_t err =
+      cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (err != cudaSuccess) return err;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  gemm_tc_kernel<<<unsigned(sms), kThreads, smem, st>>>(
+      tmA, tmB, E, N, K, BN, offsets, bias, act, static_cast<__nv_bfloat16*>(out), max_rows, status);
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,46 @@
+// Internal launchers of the MoE-layer kernels (not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+namespace moe {
+
+// Counts every kernel launch the library makes (reported by moe_launch_count).
+void count_launch();
+
+// Router on CUDA cores (fp32 or bf16): logits, softmax, top-k, weights, psum.
+cudaError_t launch_route_simt(const moe_config_t& c, const void* x, const void* Wr,
+                              const float* br, float* logits, int32_t* ids, float* w,
+                              float* psum_partial, float* psum, cudaStream_t st);
+
+// Dispatch: histogram per chunk, per-expert scan + capacity, positions, row copy.
+cudaError_t launch_dispatch(const moe_config_t& c, int64_t C, const void* x,
+                            const int32_t* ids, int32_t* counts, int32_t* kept,
+                            int32_t* offsets, int32_t* slot_row, int32_t* row_token, void* xd,
+                            int32_t* chunk_counts, int32_t* status, cudaStream_t st);
+
+// Grouped GEMM on CUDA cores over ragged expert row ranges (fp32 or bf16):
+//   out[rows of e] = epi(A[rows of e] · B[e]ᵀ + bias[e]),  A [R,K], B [E,N,K].
+// act < 0: no activation.  max_rows bounds the rows (R).
+cudaError_t launch_gemm_simt(int dtype, int E, int N, int K, int64_t max_rows,
+                             const int32_t* offsets, const void* A, const void* B,
+                             const float* bias, int act, void* out, cudaStream_t st);
+
+// Grouped GEMM on the tcgen05 tensor cores (bf16 in, fp32 accumulate, bf16 out).
+cudaError_t launch_gemm_tc(int E, int N, int K, int64_t max_rows, const int32_t* offsets,
+                           const void* A, const void* B, const float* bias, int act,
+                           void* out, int32_t* status, cudaStream_t st);
+
+// Combine: y[t] = Σ_r w[t,r]·yd[slot_row[t,r]] (kept slots, rank order, fp32).
+// Rows outside [0, max_rows) are treated as dropped.
+cudaError_t launch_combine(const moe_config_t& c, int64_t max_rows, const void* yd,
+                           const int32_t* slot_row, const float* w, void* y, cudaStream_t st);
+
+// f, p̄, L_aux from counts and psum.
+cudaError_t launch_aux(const moe_config_t& c, const int32_t* counts, const float* psum,
+                       float alpha, float* f, float* pbar, float* l_aux, cudaStream_t st);
+
+}  // namespace moe

@@ -1,0 +1,119 @@
+"""The C-ABI library loads and exports every declared entry point; its
+host-only functions (capacity, buffer sizes, argument checks) behave as the
+header states.  CPU only: nothing here launches a kernel."""
+
+import ctypes
+import math
+import os
+import re
+from fractions import Fraction
+
+import pytest
+
+import oracle
+from routing_dispatch_expert_06_b300 import build as moe_build
+from routing_dispatch_expert_06_b300 import moe
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    moe_build.build()
+    return moe.load()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ["moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_forward",
+                     "moe_aux_stats"]:
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def cfg_for(T, d, d_ff, E, k, c, **kw):
+    return moe.config(T, d, d_ff, E, k, c, **kw)
+
+
+@pytest.mark.parametrize("T,k,E,c", [(8, 1, 2, 1.0), (8, 1, 2, 1.5), (1024, 1, 8, 1.25),
+                                     (1024, 1, 8, 2.0), (512, 2, 8, 1.0), (4096, 2, 8, 1.25),
+                                     (16384, 1, 8, 1.0), (8192, 6, 64, 1.0),
+                                     (32768, 8, 256, 1.25), (10, 1, 1, 1.1), (7, 3, 5, 0.3)])
+def test_capacity_matches_definition(lib, T, k, E, c):
+    cfg = cfg_for(T, 64, 64, E, k, c)
+    C = moe.capacity(cfg)
+    assert C == math.ceil(Fraction(c) * T * k / E)
+    assert C == oracle.capacity(T, k, E, c)
+    assert moe.max_rows(cfg) == min(T * k, E * C)
+
+
+def test_workspace_size_positive_and_aligned(lib):
+    for T, E in [(1, 1), (512, 8), (32768, 256), (100000, 1024)]:
+        n = moe.workspace_size(cfg_for(T, 64, 64, E, 1, 1.0))
+        assert n > 0 and n % 256 == 0
+
+
+@pytest.mark.parametrize("bad", [
+    dict(T=0), dict(E=0), dict(E=1025), dict(k=0), dict(k=17), dict(E=4, k=5), dict(d=12),
+    dict(d_ff=20), dict(capacity_factor=0.0), dict(capacity_factor=-1.0),
+    dict(T=1 << 28, k=8)])
+def test_invalid_config_rejected(lib, bad):
+    base = dict(T=64, d=64, d_ff=64, E=8, k=2, capacity_factor=1.0)
+    base.update(bad)
+    cfg = moe.config(**base)
+    n = ctypes.c_size_t(0)
+    assert lib.moe_workspace_size(ctypes.byref(cfg), ctypes.byref(n)) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_capacity(ctypes.byref(cfg)) == -1
+    assert lib.moe_last_error().decode() != ""
+
+
+def test_unsupported_dtype_and_act(lib):
+    cfg = cfg_for(64, 64, 64, 8, 2, 1.0)
+    cfg.dtype = 7
+    n = ctypes.c_size_t(0)
+    assert lib.moe_workspace_size(ctypes.byref(cfg), ctypes.byref(n)) == moe.MOE_ERR_UNSUPPORTED
+    cfg = cfg_for(64, 64, 64, 8, 2, 1.0)
+    cfg.act = 9
+    assert lib.moe_workspace_size(ctypes.byref(cfg), ctypes.byref(n)) == moe.MOE_ERR_UNSUPPORTED
+
+
+def test_null_tensors_rejected_before_any_launch(lib):
+    cfg = cfg_for(64, 64, 64, 8, 2, 1.0)
+    P = ctypes.c_void_p
+    ws = P(256)  # never dereferenced: the NULL check comes first
+    assert lib.moe_route(ctypes.byref(cfg), None, None, None, None, None, None, None, ws, 1 << 20,
+                         None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_dispatch(ctypes.byref(cfg), None, None, None, None, None, None, None, None, ws,
+                            1 << 20, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_combine(ctypes.byref(cfg), None, None, None, None, None) == \
+        moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_aux_stats(ctypes.byref(cfg), None, None, 1.0, None, None, None, None) == \
+        moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_forward(ctypes.byref(cfg), None, 1.0, ws, 1 << 20, None) == \
+        moe.MOE_ERR_INVALID_ARG
+
+
+def test_small_workspace_rejected(lib):
+    cfg = cfg_for(4096, 64, 64, 8, 2, 1.0)
+    P = ctypes.c_void_p
+    need = moe.workspace_size(cfg)
+    fake = P(1 << 12)  # aligned, never dereferenced
+    r = lib.moe_route(ctypes.byref(cfg), P(16), P(16), P(16), None, P(16), P(16), P(16), fake,
+                      need - 256, None)
+    assert r == moe.MOE_ERR_WORKSPACE
+
+
+def test_status_strings(lib):
+    for code, name in [(0, "MOE_OK"), (1, "MOE_ERR_INVALID_ARG"), (5, "MOE_ERR_TIMEOUT")]:
+        assert lib.moe_status_string(code).decode() == name
