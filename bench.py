@@ -1,0 +1,384 @@
+"""Benchmark: forward pass of one MoE layer on B300, tokens/s.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference] [--no-cpu-baseline]
+
+One step = one forward pass of the whole layer (route, dispatch, grouped
+expert FFN, combine, aux statistics) over one batch of T synthetic tokens,
+inputs already resident in HBM.  Each step is timed with CUDA events on the
+launching stream, with the L2 cache flushed between steps (a 512 MiB write,
+outside the events).  Rank 0 prints one JSON line.
+
+Multi-GPU: the layer does not shard in this design (replicas only), so under
+torchrun every rank runs an independent replica on its own batch and
+``value`` is the tokens of all ranks / the slowest rank's time.
+
+``--impl reference`` times the CPU oracle (the plain C++ implementation the
+tests compare against) on the host cores, on a bounded sample of the same
+workload, and prints the same JSON line with "impl": "reference".
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+from routing_dispatch_expert_06_b300 import inputs
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+PROFILES = os.path.join(ROOT, "profiles")
+STAGES = ["route", "dispatch", "ffn_up", "ffn_down", "combine", "aux"]
+METRIC = "MoE-layer fwd tokens/s on 1 B300; grouped-FFN TC util %; dispatch HBM GB/s"
+
+
+# ---------------------------------------------------------------- helpers ----
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm=float(p["hbm_gbs"]), bf16=float(p["bf16_tflops"]),
+                    bf16_sustained=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                    source="measured")
+    except (OSError, KeyError, ValueError):
+        return dict(hbm=6400.0, bf16=1800.0, bf16_sustained=1400.0, source="fallback")
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=5)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[3:]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return dict(sm_mhz=statistics.median(sm), sm_max_mhz=max(mx), reasons=sorted(reasons),
+                    samples=len(sm))
+
+
+def kernel_traffic(kernel: str, workload: str, src_file: str):
+    """DRAM bytes per launch from the committed ncu summary, if it still
+    describes the current kernel source (sha256 match), else None."""
+    path = os.path.join(PROFILES, f"{kernel}_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m_t = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    m_h = re.search(r"kernel_source_sha256:\s*([0-9a-f]{64})", text)
+    if not (m_t and m_h):
+        return None
+    with open(src_file, "rb") as f:
+        if hashlib.sha256(f.read()).hexdigest() != m_h.group(1):
+            return None
+    return float(m_t.group(1))
+
+
+def algorithmic(wl, n_kept: int, t_kept: int):
+    """Bytes / FLOPs the method must move or compute per forward pass."""
+    b = 2 if wl.dtype == "bf16" else 4
+    T, d, d_ff, E, k = wl.T, wl.d, wl.d_ff, wl.E, wl.k
+    return dict(
+        route_bytes=T * d * b + E * d * b + T * k * 8,
+        route_flops=2 * T * d * E,
+        dispatch_bytes=t_kept * d * b + n_kept * d * b + T * k * 8 + n_kept * 4,
+        ffn_up_flops=2 * n_kept * d * d_ff,
+        ffn_down_flops=2 * n_kept * d * d_ff,
+        combine_bytes=n_kept * d * b + T * k * 8 + T * d * b,
+    )
+
+
+# ------------------------------------------------------------ CPU oracle ----
+
+def host_inputs(wl, inp=None, max_tokens=8192):
+    """Host copies (numpy; bf16 as uint16 bits) of a workload's tensors: the
+    given device tensors, or a fresh CPU draw with the same recipe."""
+    if inp is None:
+        inp = inputs.make_inputs(wl.replace(T=min(wl.T, max_tokens)), "cpu")
+    out = {k: inputs.to_numpy(v) for k, v in inp.items() if k != "x"}
+    out["x"] = inputs.to_numpy(inp["x"][:max_tokens])
+    return out
+
+
+def cpu_oracle_sample(wl, host, budget_s: float = 15.0, seed_tokens: int = 8):
+    """Time the oracle's forward on a batch of S tokens of this workload (same
+    weights and input distribution; capacity scope = the S tokens).  S is
+    grown from a small probe until one run takes about budget_s / 4, so the
+    whole measurement stays within about budget_s.  Returns tokens/s."""
+    import oracle  # test infrastructure: only this CPU-baseline leg runs it
+
+    act = oracle.ACT_RELU if wl.act == "relu" else oracle.ACT_GELU_TANH
+
+    def run(S):
+        t0 = time.perf_counter()
+        oracle.forward(host["x"][:S], host["Wr"], host["br"], host["W1"], host["b1"], host["W2"],
+                       host["b2"], k=wl.k, capacity_factor=wl.capacity_factor,
+                       renormalize=wl.renormalize, act=act)
+        return time.perf_counter() - t0
+
+    S = min(seed_tokens, host["x"].shape[0])
+    dt = run(S)
+    total = dt
+    cap = host["x"].shape[0]
+    while dt < budget_s / 4 and S < cap and total < budget_s:
+        S = min(cap, max(S * 2, int(S * (budget_s / 4) / max(dt, 1e-3))))
+        dt = run(S)
+        total += dt
+    return dict(value=S / dt, unit="tokens/s", cores=oracle.num_threads(), kind="oracle",
+                sample=f"one forward of the C++ oracle over a batch of {S} tokens of the "
+                       f"{wl.name} layer (same weights and x distribution; capacity over the "
+                       f"{S} tokens); {dt:.2f} s")
+
+
+def run_reference(args, wl, rank, world):
+    if rank != 0:
+        return 0
+    import oracle
+
+    host = host_inputs(wl)
+    vals = []
+    info = None
+    for _ in range(args.steps):  # the oracle keeps no state, so warm-up steps are skipped
+        info = cpu_oracle_sample(wl, host, budget_s=max(4.0, 60.0 / max(args.steps, 1)))
+        vals.append(info["value"])
+    v = statistics.median(vals)
+    line = dict(metric=METRIC, value=v, unit="tokens/s", n_gpus=world, steps=args.steps,
+                warmup=args.warmup, ms_per_step=1e3 * wl.T / v, higher_is_better=True,
+                scaling="weak", vs_baseline=None, dtype="f64", data="synthetic",
+                config=dict(workload=wl.name, T=wl.T, d=wl.d, d_ff=wl.d_ff, E=wl.E, k=wl.k,
+                            capacity_factor=wl.capacity_factor, l2="n/a (CPU)"),
+                impl="reference",
+                cpu_baseline=dict(value=v, unit="tokens/s", cores=oracle.num_threads(),
+                                  kind="oracle", sample=info["sample"]),
+                e2e=dict(value=v, unit="tokens/s", h2d_bytes_per_step=0, d2h_bytes_per_step=0))
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------- GPU bench ----
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=inputs.DEFAULT_BENCH, choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--alpha", type=float, default=0.01)
+    args = ap.parse_args()
+    wl = inputs.WORKLOADS[args.workload]
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, wl, rank, world)
+
+    from routing_dispatch_expert_06_b300 import build, moe
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    if rank == 0:
+        build.build()
+    if dist is not None:
+        dist.barrier()
+    moe.load()
+
+    dev = torch.device("cuda", local_rank)
+    inp = inputs.make_inputs(wl, dev)
+    if world > 1:  # each replica routes its own batch
+        g = torch.Generator(device=dev).manual_seed(wl.seed * 1000 + rank)
+        inp["x"] = torch.randn(inp["x"].shape, generator=g, device=dev).to(inp["x"].dtype)
+    cfg = moe.config_from_workload(wl, write_logits=False)
+    ws = moe.workspace(cfg, dev)
+    out = moe.allocate(cfg, dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+
+    for _ in range(max(args.warmup, 3)):
+        moe.forward_stages(cfg, inp, out, ws, args.alpha, stream)
+    torch.cuda.synchronize(dev)
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    launches0 = moe.launch_count()
+    with ClockSampler(local_rank) as clocks:
+        for s in range(args.steps):
+            flush.zero_()  # evict L2 between steps (outside the timed events)
+            moe.forward_stages(cfg, inp, out, ws, args.alpha, stream, events=evs[s])
+        torch.cuda.synchronize(dev)
+    launches = moe.launch_count() - launches0
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    assert moe.device_status(ws) == moe.MOE_OK
+
+    stage_ms = {name: 0.0 for name in STAGES}
+    total_ms = 0.0
+    for e in evs:
+        total_ms += e[0].elapsed_time(e[6])
+        for i, name in enumerate(STAGES):
+            stage_ms[name] += e[i].elapsed_time(e[i + 1])
+    t = torch.tensor([total_ms], dtype=torch.float64)
+    if dist is not None:
+        t = t.to(dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    max_ms = float(t.item())
+
+    offsets = out["offsets"].cpu()
+    n_kept = int(offsets[-1])
+    slot = out["slot_row"].cpu()
+    t_kept = int((slot >= 0).any(dim=1).sum())
+    alg = algorithmic(wl, n_kept, t_kept)
+    K = args.steps
+    peaks = load_peaks()
+    mean = {k: v / K for k, v in stage_ms.items()}
+    ffn_ms = mean["ffn_up"] + mean["ffn_down"]
+    dom = "ffn_up" if mean["ffn_up"] >= mean["ffn_down"] else "ffn_down"
+    dom_tflops = alg[f"{dom}_flops"] / (mean[dom] * 1e-3) / 1e12
+    traffic = kernel_traffic(dom, wl.name, os.path.join(ROOT, "routing_dispatch_expert_06_b300",
+                                                        "csrc", "ffn_tc.cu"))
+
+    # e2e: the public call with host buffers, H2D of x and D2H of y inside
+    x_host = inp["x"].cpu().pin_memory()
+    y_host = torch.empty(out["y"].shape, dtype=out["y"].dtype).pin_memory()
+    l_host = torch.empty(1, dtype=torch.float32).pin_memory()
+    x_dev = inp["x"]
+    inp_e2e = dict(inp)
+    e2e_steps = max(3, min(K, 10))
+    for _ in range(2):
+        x_dev.copy_(x_host, non_blocking=True)
+        moe.forward(cfg, inp_e2e, out, ws, args.alpha, stream)
+        y_host.copy_(out["y"], non_blocking=True)
+    torch.cuda.synchronize(dev)
+    e_start = torch.cuda.Event(enable_timing=True)
+    e_end = torch.cuda.Event(enable_timing=True)
+    e2e_ms = 0.0
+    for _ in range(e2e_steps):
+        flush.zero_()
+        e_start.record(stream)
+        x_dev.copy_(x_host, non_blocking=True)
+        moe.forward(cfg, inp_e2e, out, ws, args.alpha, stream)
+        y_host.copy_(out["y"], non_blocking=True)
+        l_host.copy_(out["l_aux"], non_blocking=True)
+        e_end.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms += e_start.elapsed_time(e_end)
+    e2e_ms /= e2e_steps
+    te = torch.tensor([e2e_ms], dtype=torch.float64)
+    if dist is not None:
+        te = te.to(dev)
+        dist.all_reduce(te, op=dist.ReduceOp.MAX)
+    e2e_ms = float(te.item())
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
+
+    value = world * wl.T * K / (max_ms * 1e-3)
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_oracle_sample(wl, host_inputs(wl, inp))
+    b = 2 if wl.dtype == "bf16" else 4
+    line = dict(
+        metric=METRIC, value=value, unit="tokens/s", n_gpus=world, steps=K, warmup=args.warmup,
+        ms_per_step=max_ms / K, higher_is_better=True, scaling="weak", vs_baseline=None,
+        dtype="bf16" if wl.dtype == "bf16" else "f32", data="synthetic",
+        config=dict(workload=wl.name, T=wl.T, d=wl.d, d_ff=wl.d_ff, E=wl.E, k=wl.k,
+                    capacity_factor=wl.capacity_factor, renormalize=wl.renormalize,
+                    act=wl.act, parallelism=f"replicas{world}" if world > 1 else "single",
+                    l2="flushed between steps (512 MiB write)"),
+        roofline=dict(bound="tensor", kernel=f"{dom} (tcgen05 grouped GEMM)",
+                      achieved=dom_tflops, peak=peaks["bf16"], unit="TFLOP/s",
+                      frac=dom_tflops / peaks["bf16"], traffic=traffic,
+                      peak_source=f"{peaks['source']} bf16 burst"),
+        cpu_baseline=cpu,
+        e2e=dict(value=world * wl.T / (e2e_ms * 1e-3), unit="tokens/s",
+                 h2d_bytes_per_step=wl.T * wl.d * b, d2h_bytes_per_step=wl.T * wl.d * b + 4),
+        gpu_launches=launches,
+        clocks=clocks.summary(),
+        stages_ms={k: round(v, 5) for k, v in mean.items()},
+        ffn_tflops=alg["ffn_up_flops"] * 2 / (ffn_ms * 1e-3) / 1e12,
+        ffn_tc_frac=alg["ffn_up_flops"] * 2 / (ffn_ms * 1e-3) / 1e12 / peaks["bf16"],
+        dispatch_gbs=alg["dispatch_bytes"] / (mean["dispatch"] * 1e-3) / 1e9,
+        combine_gbs=alg["combine_bytes"] / (mean["combine"] * 1e-3) / 1e9,
+        route_gbs=alg["route_bytes"] / (mean["route"] * 1e-3) / 1e9,
+        hbm_peak_gbs=peaks["hbm"],
+        kept_rows=n_kept,
+    )
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
