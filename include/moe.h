@@ -140,6 +140,27 @@ moe_status_t moe_dispatch(const moe_config_t* cfg, const void* x, const int32_t*
                           int32_t* counts, int32_t* kept, int32_t* offsets, int32_t* slot_row,
                           int32_t* row_token, void* xd, void* ws, size_t ws_bytes, void* stream);
 
+/* The dispatch stage for callers that cannot allocate device memory (for
+ * example a plugin inside a host framework whose memory pool owns the whole
+ * device, or a latency-critical path that may not take cudaMalloc's implicit
+ * synchronisation), so cannot provide the workspace moe_dispatch needs.
+ * This call has no counterpart in the paper: it is an interface choice.
+ * Same outputs as moe_dispatch; the per-chunk histogram lives in a fixed
+ * 1 MiB device array inside the library (held by every GPU that loads the
+ * library until exit), so this call allocates nothing.
+ *  - requires ceil(T/256)·E <= 262144, else MOE_ERR_INVALID_ARG (no launch);
+ *  - status: optional device int32 (may be NULL) that receives
+ *    MOE_ERR_INVALID_ARG if an expert id is out of range; the caller zeroes
+ *    it; it is written only on error;
+ *  - all calls on a device share the array: calls that overlap on the GPU
+ *    race; calls ordered on one stream do not (nothing carries over);
+ *  - the first call on each device looks up the array's address; make that
+ *    call before any stream capture. */
+moe_status_t moe_dispatch_noalloc(const moe_config_t* cfg, const void* x,
+                                  const int32_t* topk_ids, int32_t* counts, int32_t* kept,
+                                  int32_t* offsets, int32_t* slot_row, int32_t* row_token,
+                                  void* xd, int32_t* status, void* stream);
+
 /* [MoE 模型原理 §1] First expert GEMM over the ragged groups given by
  * offsets: H[rows of e] = σ(xd[rows of e] W1[e]ᵀ + b1[e]). */
 moe_status_t moe_ffn_up(const moe_config_t* cfg, const void* xd, const int32_t* offsets,

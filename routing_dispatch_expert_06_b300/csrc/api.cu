@@ -22,6 +22,8 @@ static moe_status_t fail(moe_status_t code, const std::string& msg) {
   return code;
 }
 
+moe_status_t report_error(moe_status_t code, const char* msg) { return fail(code, msg); }
+
 static moe_status_t cuda_fail(cudaError_t e, const char* where) {
   return fail(MOE_ERR_CUDA, std::string(where) + ": " + cudaGetErrorString(e));
 }

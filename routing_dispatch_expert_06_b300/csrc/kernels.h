@@ -11,6 +11,9 @@ namespace moe {
 // Counts every kernel launch the library makes (reported by moe_launch_count).
 void count_launch();
 
+// Records msg as the calling thread's moe_last_error() text; returns code.
+moe_status_t report_error(moe_status_t code, const char* msg);
+
 // Router on CUDA cores (fp32 or bf16): logits, softmax, top-k, weights, psum.
 cudaError_t launch_route_simt(const moe_config_t& c, const void* x, const void* Wr,
                               const float* br, float* logits, int32_t* ids, float* w,

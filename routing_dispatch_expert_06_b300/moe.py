@@ -71,6 +71,7 @@ def load():
         "moe_workspace_init": (st, [_P, sz, _P]),
         "moe_route": (st, [cfgp, _P, _P, _P, _P, _P, _P, _P, _P, sz, _P]),
         "moe_dispatch": (st, [cfgp, _P, _P, _P, _P, _P, _P, _P, _P, _P, sz, _P]),
+        "moe_dispatch_noalloc": (st, [cfgp, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
         "moe_ffn_up": (st, [cfgp, _P, _P, _P, _P, _P, _P, sz, _P]),
         "moe_ffn_down": (st, [cfgp, _P, _P, _P, _P, _P, _P, sz, _P]),
         "moe_expert_ffn": (st, [cfgp, _P, _P, _P, _P, _P, _P, _P, _P, _P, sz, _P]),
@@ -200,6 +201,15 @@ def dispatch(cfg, x, topk_ids, out, ws, stream=None):
                                _ptr(out["kept"]), _ptr(out["offsets"]), _ptr(out["slot_row"]),
                                _ptr(out["row_token"]), _ptr(out["xd"]), _ptr(ws), ws.numel(),
                                _stream(stream)))
+
+
+def dispatch_noalloc(cfg, x, topk_ids, out, status=None, stream=None):
+    """moe_dispatch without a workspace (scratch in a fixed library array)."""
+    _check(load().moe_dispatch_noalloc(ctypes.byref(cfg), _ptr(x), _ptr(topk_ids),
+                                       _ptr(out["counts"]), _ptr(out["kept"]),
+                                       _ptr(out["offsets"]), _ptr(out["slot_row"]),
+                                       _ptr(out["row_token"]), _ptr(out["xd"]), _ptr(status),
+                                       _stream(stream)))
 
 
 def ffn_up(cfg, xd, offsets, W1, b1, H, ws, stream=None):
