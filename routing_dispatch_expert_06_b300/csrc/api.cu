@@ -116,6 +116,15 @@ static bool use_tc_gemm(const moe_config_t& c) {
   return !(v && std::strcmp(v, "simt") == 0);
 }
 
+// Which router runs: the tcgen05 kernel for bf16 layers with E <= 256, else
+// the CUDA-core kernel; MOE_ROUTE_IMPL=simt selects the CUDA-core kernel
+// (a cross-check in tests).
+static bool use_tc_router(const moe_config_t& c) {
+  if (!route_tc_supported(c)) return false;
+  const char* v = std::getenv("MOE_ROUTE_IMPL");
+  return !(v && std::strcmp(v, "simt") == 0);
+}
+
 }  // namespace moe
 
 using namespace moe;
@@ -159,9 +168,12 @@ moe_status_t moe_route(const moe_config_t* cfg, const void* x, const void* Wr, c
     return fail(MOE_ERR_INVALID_ARG, "moe_route: write_logits set but logits is NULL");
   Ws w;
   if ((s = get_ws(*cfg, ws, ws_bytes, &w)) != MOE_OK) return s;
-  cudaError_t e = launch_route_simt(*cfg, x, Wr, br, cfg->write_logits ? logits : nullptr,
-                                    topk_ids, topk_w, w.psum_partial, psum,
-                                    static_cast<cudaStream_t>(stream));
+  float* lg = cfg->write_logits ? logits : nullptr;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = use_tc_router(*cfg) ? launch_route_tc(*cfg, x, Wr, br, lg, topk_ids, topk_w,
+                                                        w.psum_partial, psum, w.status, st)
+                                      : launch_route_simt(*cfg, x, Wr, br, lg, topk_ids, topk_w,
+                                                          w.psum_partial, psum, st);
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_route");
 }
 

@@ -228,7 +228,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t acc_phase = 0;
     for (int64_t i = blockIdx.x; i < total; i += gridDim.x) {
       const TileCoord c = tile_coord(i, s_mt, E, n_tn, s_off, BN);
-      if (!tc::mbar_wait(&tfull_bar[acc], acc_phase, abort_flag, kWaitLimitNs)) {
+      // The tensor-memory loads below are warp-collective: the whole warp
+      // takes the same branch.
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(&tfull_bar[acc], acc_phase, abort_flag,
+                                                 kWaitLimitNs))) {
         give_up();
         break;
       }

@@ -19,6 +19,17 @@ cudaError_t launch_route_simt(const moe_config_t& c, const void* x, const void* 
                               const float* br, float* logits, int32_t* ids, float* w,
                               float* psum_partial, float* psum, cudaStream_t st);
 
+// psum[i] = Σ_b psum_partial[b][i] over nblk router blocks, b ascending.
+cudaError_t launch_psum_reduce(int64_t nblk, int E, const float* psum_partial, float* psum,
+                               cudaStream_t st);
+
+// Router on the tcgen05 tensor cores (bf16, E <= 256): same outputs as the
+// CUDA-core router; psum_partial holds one row per 128-token tile.
+bool route_tc_supported(const moe_config_t& c);
+cudaError_t launch_route_tc(const moe_config_t& c, const void* x, const void* Wr,
+                            const float* br, float* logits, int32_t* ids, float* w,
+                            float* psum_partial, float* psum, int32_t* status, cudaStream_t st);
+
 // Dispatch: histogram per chunk, per-expert scan + capacity, positions, row copy.
 cudaError_t launch_dispatch(const moe_config_t& c, int64_t C, const void* x,
                             const int32_t* ids, int32_t* counts, int32_t* kept,

@@ -169,7 +169,12 @@ cudaError_t launch_route_simt(const moe_config_t& c, const void* x, const void* 
   count_launch();
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  psum_reduce_kernel<<<unsigned((c.E + 255) / 256), 256, 0, st>>>(nblk, c.E, psum_partial, psum);
+  return launch_psum_reduce(nblk, c.E, psum_partial, psum, st);
+}
+
+cudaError_t launch_psum_reduce(int64_t nblk, int E, const float* psum_partial, float* psum,
+                               cudaStream_t st) {
+  psum_reduce_kernel<<<unsigned((E + 255) / 256), 256, 0, st>>>(nblk, E, psum_partial, psum);
   count_launch();
   return cudaGetLastError();
 }

@@ -1,0 +1,466 @@
+// Router on the sm_103a tensor cores: logits by tcgen05 MMA into tensor
+// memory, then softmax, top-k, combine weights and per-tile probability
+// column sums in the epilogue, all in one persistent kernel.
+//
+// [MoE 模型原理 §2.1] s_t = W_r x_t + b_r, p_t = softmax(s_t);
+// [MoE 模型原理 §2.2] S_t = TopK(p_t, k), p̃ = p/Σ_{S_t} p (or raw p);
+// [MoE 模型原理 §3.2] the column sums Σ_t p_{t,i} feed p̄_i.
+//
+// Tiles of 128 tokens; a CTA walks tiles b, b + grid, ...  Warps:
+//   warp 0     TMA producer: x tile [128 × 64] and W_r tile [NP × 64] per
+//              stage (NP = E rounded up to a power of two >= 32; rows past E
+//              and columns past d arrive as zeros from the copy engine's
+//              out-of-bounds fill)
+//   warp 1     TMEM allocator and MMA issuer: tcgen05.mma M=128, N=NP, K=16,
+//              bf16 in, fp32 accumulate, into one of two TMEM buffers
+//   warps 2-9  epilogue: one token row and half of the NP columns per thread
+//
+// Precision.  The tensor cores' fp32 accumulation over a long K chain drifts
+// (about 2e-5 relative over d = 7168, above the 1e-5 logit tolerance), so
+// the reduction over d is cut into segments of kSegBlocks k-blocks: each
+// segment starts a fresh accumulator, and the epilogue adds the segment sums
+// into fp32 registers while the MMA fills the other buffer.  Short chains over
+// small partial sums keep the logits close to the exact dot product.
+//
+// After the last segment of a tile the epilogue has the logits in registers:
+// bias, logits out, max and a sorted top-k list per half row, merged through
+// shared memory (ties go to the lower expert index: insertion into a sorted
+// list that only a strictly larger value passes, lower half first), then
+// Σ exp, weights, and the tile's column sums of p by a transposing warp
+// butterfly.  Every wait is bounded (4 s); on a timeout the kernel records
+// MOE_ERR_TIMEOUT, drains its copies and MMAs, frees its tensor memory and
+// returns.
+#include "common.cuh"
+#include "kernels.h"
+#include "tc.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kTileM = kRouteTileM;  // 128 tokens per tile
+constexpr int kTileK = 64;           // one 128-byte swizzle row of bf16
+constexpr int kSegBlocks = 4;        // k-blocks per accumulation segment (K = 256)
+constexpr int kEpiWarps = 8;
+constexpr int kEpiThreads = kEpiWarps * 32;
+constexpr int kThreads = 64 + kEpiThreads;
+constexpr int kMaxStages = 8;
+constexpr uint64_t kWaitLimitNs = 4000000000ull;
+constexpr int kMaxNP = 256;
+constexpr size_t kMinSmem = 120 * 1024;  // one CTA per SM (it may take all of TMEM)
+
+struct RouteTcArgs {
+  int64_t T;
+  int d, E, NP, k, renorm, stages;
+  uint32_t tmem_cols;
+  const float* br;
+  float* logits;
+  int32_t* ids;
+  float* w;
+  float* psum_partial;
+  int32_t* status;
+};
+
+__device__ __forceinline__ void bar_epi() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
+}
+
+// Insert (v, i) into a list sorted by descending value; only a strictly
+// larger value moves past an entry, so among equal values the one inserted
+// first (the lower expert index) stays ahead.
+template <int KMAX>
+__device__ __forceinline__ void topk_insert(float* tv, int* ti, float v, int i) {
+#pragma unroll
+  for (int r = 0; r < KMAX; ++r) {
+    const bool gt = v > tv[r];
+    const float ov = tv[r];
+    const int oi = ti[r];
+    tv[r] = gt ? v : ov;
+    ti[r] = gt ? i : oi;
+    v = gt ? ov : v;
+    i = gt ? oi : i;
+  }
+}
+
+// NPH = NP / 2 columns per epilogue thread.
+template <int NPH, int KMAX>
+__global__ void __launch_bounds__(kThreads, 1)
+    route_tc_kernel(const __grid_constant__ CUtensorMap tmX,
+                    const __grid_constant__ CUtensorMap tmW, const RouteTcArgs a) {
+  constexpr int NP = 2 * NPH;
+  constexpr int CH = (NPH < 32 || NPH >= 128) ? 16 : 32;  // columns per tensor-memory load
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages];
+  __shared__ uint64_t tfull_bar[2], tempty_bar[2], drain_bar;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  __shared__ float s_bias[NP];
+  __shared__ float s_red[4][NP];
+  __shared__ float s_hmax[kTileM], s_hz[kTileM], s_M[kTileM], s_invz[kTileM];
+  __shared__ float s_htv[KMAX][kTileM];
+  __shared__ int s_hti[KMAX][kTileM];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const uint32_t a_bytes = kTileM * kTileK * 2;
+  const uint32_t b_bytes = uint32_t(NP) * kTileK * 2;
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + a.stages * a_bytes;
+  const int nk = (a.d + kTileK - 1) / kTileK;
+  const int nseg = (nk + kSegBlocks - 1) / kSegBlocks;
+  const int64_t n_tiles = (a.T + kTileM - 1) / kTileM;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < a.stages; ++s) {
+      tc::mbar_init(&full_bar[s], 1);
+      tc::mbar_init(&empty_bar[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&tfull_bar[b], 1);
+      tc::mbar_init(&tempty_bar[b], kEpiThreads);
+    }
+    tc::mbar_init(&drain_bar, 1);
+    s_abort = 0;
+    tc::fence_mbar_init();
+    tc::prefetch_tmap(&tmX);
+    tc::prefetch_tmap(&tmW);
+  }
+  for (int e = threadIdx.x; e < NP; e += blockDim.x) s_bias[e] = e < a.E ? a.br[e] : 0.f;
+  if (warp == 1) {
+    tc::tmem_alloc(&s_tmem, a.tmem_cols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem_base = s_tmem;
+  volatile int* abort_flag = &s_abort;
+  auto give_up = [&]() {
+    *abort_flag = 1;
+    set_status(a.status, MOE_ERR_TIMEOUT);
+  };
+
+  if (warp == 0 && lane == 0) {
+    // ---------------- TMA producer ----------------
+    int stage = 0;
+    uint32_t phase = 0;
+    int64_t issued = 0;
+    bool ok = true;
+    for (int64_t tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+      const int32_t m0 = int32_t(tile * kTileM);
+      for (int kb = 0; kb < nk; ++kb) {
+        if (!tc::mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, kWaitLimitNs)) {
+          give_up();
+          ok = false;
+          break;
+        }
+        tc::mbar_arrive_expect_tx(&full_bar[stage], a_bytes + b_bytes);
+        tc::tma_load_2d(&tmX, &full_bar[stage], sA + stage * a_bytes, kb * kTileK, m0);
+        tc::tma_load_2d(&tmW, &full_bar[stage], sB + stage * b_bytes, kb * kTileK, 0);
+        ++issued;
+        if (++stage == a.stages) stage = 0, phase ^= 1u;
+      }
+    }
+    // Drain: the last `stages` copies this thread issued must land before the
+    // CTA exits (on the normal path the MMA issuer has consumed them all).
+    const int64_t first = issued > a.stages ? issued - a.stages : 0;
+    for (int64_t i = first; i < issued; ++i)
+      tc::mbar_wait(&full_bar[i % a.stages], uint32_t((i / a.stages) & 1), nullptr, kWaitLimitNs);
+  } else if (warp == 1 && lane == 0) {
+    // ---------------- MMA issuer ----------------
+    const uint32_t idesc = tc::idesc_bf16_f32(kTileM, NP);
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t seg_count = 0;  // segments issued by this CTA (all tiles)
+    bool ok = true;
+    for (int64_t tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+      for (int sg = 0; sg < nseg && ok; ++sg, ++seg_count) {
+        const uint32_t buf = seg_count & 1u;
+        if (!tc::mbar_wait(&tempty_bar[buf], ((seg_count >> 1) & 1u) ^ 1u, abort_flag,
+                           kWaitLimitNs)) {
+          give_up();
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+        const uint32_t d_tmem = tmem_base + buf * uint32_t(NP);
+        const int kb_end = min(nk, (sg + 1) * kSegBlocks);
+        for (int kb = sg * kSegBlocks; kb < kb_end; ++kb) {
+          if (!tc::mbar_wait(&full_bar[stage], phase, abort_flag, kWaitLimitNs)) {
+            give_up();
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint32_t a0 = tc::smem_u32(sA + stage * a_bytes);
+          const uint32_t b0 = tc::smem_u32(sB + stage * b_bytes);
+          const bool first = kb == sg * kSegBlocks;
+#pragma unroll
+          for (int j = 0; j < kTileK / 16; ++j)
+            tc::mma_bf16(d_tmem, tc::sdesc_kmajor_sw128(a0 + j * 32),
+                         tc::sdesc_kmajor_sw128(b0 + j * 32), idesc, (first && j == 0) ? 0u : 1u);
+          tc::mma_commit(&empty_bar[stage]);
+          if (++stage == a.stages) stage = 0, phase ^= 1u;
+        }
+        if (ok) tc::mma_commit(&tfull_bar[buf]);
+      }
+    }
+    // Drain: every MMA this thread issued completes before TMEM is freed.
+    tc::mma_commit(&drain_bar);
+    tc::mbar_wait(&drain_bar, 0, nullptr, kWaitLimitNs);
+  } else if (warp >= 2) {
+    // ---------------- epilogue ----------------
+    const int quarter = warp & 3;        // TMEM lanes [32·quarter, 32·quarter + 32)
+    const int h = (warp - 2) >> 2;       // column half: [h·NPH, h·NPH + NPH)
+    const int row = quarter * 32 + lane;
+    const int E = a.E;
+    const int col_of_lane =
+        ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
+    const uint32_t t_lane = tmem_base + (uint32_t(quarter * 32) << 16) + uint32_t(h * NPH);
+    uint32_t seg_count = 0;
+    bool ok = true;
+    for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+      const int64_t t = tile * kTileM + row;
+      const bool valid = t < a.T;
+      float v[NPH];
+#pragma unroll
+      for (int j = 0; j < NPH; ++j) v[j] = 0.f;
+      for (int sg = 0; sg < nseg; ++sg, ++seg_count) {
+        const uint32_t buf = seg_count & 1u;
+        if (ok) {
+          // The tensor-memory loads are warp-collective: the whole warp takes
+          // the same branch.
+          ok = __all_sync(0xffffffffu, tc::mbar_wait(&tfull_bar[buf], (seg_count >> 1) & 1u,
+                                                     abort_flag, kWaitLimitNs));
+          if (!ok) give_up();
+        }
+        if (ok) {
+          tc::fence_after_sync();
+#pragma unroll
+          for (int c0 = 0; c0 < NPH; c0 += CH) {
+            uint32_t r[CH];
+            if constexpr (CH == 32)
+              tc::tmem_ld_x32(t_lane + buf * uint32_t(NP) + uint32_t(c0), r);
+            else
+              tc::tmem_ld_x16(t_lane + buf * uint32_t(NP) + uint32_t(c0), r);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < CH; ++j) v[c0 + j] += __uint_as_float(r[j]);
+          }
+          tc::fence_before_sync();
+          tc::mbar_arrive(&tempty_bar[buf]);
+        }
+      }
+      // Logits, this half's max and top-k.
+      float hmax = -INFINITY;
+      float tv[KMAX];
+      int ti[KMAX];
+#pragma unroll
+      for (int r = 0; r < KMAX; ++r) tv[r] = -INFINITY, ti[r] = 0x7fffffff;
+#pragma unroll
+      for (int j = 0; j < NPH; ++j) {
+        const int e = h * NPH + j;
+        v[j] += s_bias[e];
+        if (e < E) {
+          hmax = fmaxf(hmax, v[j]);
+          topk_insert<KMAX>(tv, ti, v[j], e);
+        }
+      }
+      if (valid && ok && a.logits && h * NPH < E) {
+        float* lrow = a.logits + t * E + h * NPH;
+        const int ncol = min(NPH, E - h * NPH);
+        if ((E & 3) == 0) {
+#pragma unroll
+          for (int j = 0; j < NPH; j += 4)
+            if (j < ncol)
+              *reinterpret_cast<float4*>(lrow + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < NPH; ++j)
+            if (j < ncol) lrow[j] = v[j];
+        }
+      }
+      // Merge the upper half into the lower half's list.
+      if (h == 1) {
+        s_hmax[row] = hmax;
+#pragma unroll
+        for (int r = 0; r < KMAX; ++r) s_htv[r][row] = tv[r], s_hti[r][row] = ti[r];
+      }
+      bar_epi();
+      if (h == 0) {
+        const float M = fmaxf(hmax, s_hmax[row]);
+#pragma unroll
+        for (int r = 0; r < KMAX; ++r) topk_insert<KMAX>(tv, ti, s_htv[r][row], s_hti[r][row]);
+        s_M[row] = M;
+      }
+      bar_epi();
+      const float M = s_M[row];
+      float z = 0.f;
+#pragma unroll
+      for (int j = 0; j < NPH; ++j)
+        if (h * NPH + j < E) z += expf(v[j] - M);
+      if (h == 1) s_hz[row] = z;
+      bar_epi();
+      if (h == 0) {
+        z += s_hz[row];
+        const float inv_z = 1.f / z;
+        s_invz[row] = inv_z;
+        if (valid && ok) {
+          float sel = 0.f;
+#pragma unroll
+          for (int r = 0; r < KMAX; ++r)
+            if (r < a.k) sel += expf(tv[r] - M);
+          const float inv = a.renorm ? 1.f / sel : inv_z;
+#pragma unroll
+          for (int r = 0; r < KMAX; ++r)
+            if (r < a.k) {
+              a.ids[t * a.k + r] = ti[r];
+              a.w[t * a.k + r] = expf(tv[r] - M) * inv;
+            }
+        }
+      }
+      bar_epi();
+      // Column sums of p over the tile: per warp a transposing butterfly over
+      // 16 columns at a time (lane L, L even, ends with column col_of_lane),
+      // then the four lane quarters in order.
+      const float inv_z = s_invz[row];
+#pragma unroll
+      for (int c0 = 0; c0 < NPH; c0 += 16) {
+        float p[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          p[j] = (valid && ok && h * NPH + c0 + j < E) ? expf(v[c0 + j] - M) * inv_z : 0.f;
+#pragma unroll
+        for (int half = 8, o = 16; half >= 1; half >>= 1, o >>= 1) {
+          const bool upper = (lane & o) != 0;
+#pragma unroll
+          for (int j = 0; j < half; ++j) {
+            const float send = upper ? p[j] : p[j + half];
+            const float keep = upper ? p[j + half] : p[j];
+            p[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+          }
+        }
+        p[0] += __shfl_xor_sync(0xffffffffu, p[0], 1);
+        if ((lane & 1) == 0) s_red[quarter][h * NPH + c0 + col_of_lane] = p[0];
+      }
+      bar_epi();
+      for (int e = threadIdx.x - 64; e < E; e += kEpiThreads)
+        a.psum_partial[tile * E + e] = ((s_red[0][e] + s_red[1][e]) + s_red[2][e]) + s_red[3][e];
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (warp == 1) {
+    __syncwarp();
+    tc::tmem_dealloc(tmem_base, a.tmem_cols);
+  }
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode() {
+  static EncodeTiledFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+bool encode_2d(EncodeTiledFn encode, CUtensorMap* m, const void* base, int64_t inner,
+               int64_t outer, uint32_t box_inner, uint32_t box_outer) {
+  const cuuint64_t dims[2] = {cuuint64_t(inner), cuuint64_t(outer)};
+  const cuuint64_t strides[1] = {cuuint64_t(inner) * 2};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t es[2] = {1, 1};
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
+template <int NPH, int KMAX>
+cudaError_t launch_k(const CUtensorMap& tmX, const CUtensorMap& tmW, const RouteTcArgs& a,
+                     size_t smem, unsigned grid, cudaStream_t st) {
+  cudaError_t err = cudaFuncSetAttribute(route_tc_kernel<NPH, KMAX>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (err != cudaSuccess) return err;
+  route_tc_kernel<NPH, KMAX><<<grid, kThreads, smem, st>>>(tmX, tmW, a);
+  return cudaGetLastError();
+}
+
+template <int NPH>
+cudaError_t launch_np(int k, const CUtensorMap& tmX, const CUtensorMap& tmW,
+                      const RouteTcArgs& a, size_t smem, unsigned grid, cudaStream_t st) {
+  if (k <= 1) return launch_k<NPH, 1>(tmX, tmW, a, smem, grid, st);
+  if (k <= 2) return launch_k<NPH, 2>(tmX, tmW, a, smem, grid, st);
+  if (k <= 4) return launch_k<NPH, 4>(tmX, tmW, a, smem, grid, st);
+  if (k <= 8) return launch_k<NPH, 8>(tmX, tmW, a, smem, grid, st);
+  return launch_k<NPH, 16>(tmX, tmW, a, smem, grid, st);
+}
+
+}  // namespace
+
+bool route_tc_supported(const moe_config_t& c) {
+  return c.dtype == MOE_DT_BF16 && c.E <= kMaxNP && c.k <= 16;
+}
+
+cudaError_t launch_route_tc(const moe_config_t& c, const void* x, const void* Wr,
+                            const float* br, float* logits, int32_t* ids, float* w,
+                            float* psum_partial, float* psum, int32_t* status, cudaStream_t st) {
+  if (!route_tc_supported(c)) return cudaErrorInvalidValue;
+  EncodeTiledFn encode = get_encode();
+  if (!encode) return cudaErrorNotSupported;
+  RouteTcArgs a{};
+  a.T = c.T;
+  a.d = c.d;
+  a.E = c.E;
+  int NP = 32;
+  while (NP < c.E) NP <<= 1;
+  a.NP = NP;
+  a.k = c.k;
+  a.renorm = c.renormalize;
+  a.tmem_cols = uint32_t(2 * NP);  // two accumulator buffers
+  const size_t stage_bytes = size_t(kTileM) * kTileK * 2 + size_t(NP) * kTileK * 2;
+  int stages = int((192 * 1024) / stage_bytes);
+  if (stages > kMaxStages) stages = kMaxStages;
+  a.stages = stages;
+  a.br = br;
+  a.logits = logits;
+  a.ids = ids;
+  a.w = w;
+  a.psum_partial = psum_partial;
+  a.status = status;
+
+  CUtensorMap tmX, tmW;
+  if (!encode_2d(encode, &tmX, x, c.d, c.T, kTileK, kTileM)) return cudaErrorInvalidValue;
+  if (!encode_2d(encode, &tmW, Wr, c.d, c.E, kTileK, uint32_t(NP))) return cudaErrorInvalidValue;
+  size_t smem = 1024 + size_t(stages) * stage_bytes;
+  if (smem < kMinSmem) smem = kMinSmem;
+  const int64_t n_tiles = (c.T + kTileM - 1) / kTileM;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const unsigned grid = unsigned(n_tiles < sms ? n_tiles : sms);
+  cudaError_t err;
+  switch (NP) {
+    case 32: err = launch_np<16>(c.k, tmX, tmW, a, smem, grid, st); break;
+    case 64: err = launch_np<32>(c.k, tmX, tmW, a, smem, grid, st); break;
+    case 128: err = launch_np<64>(c.k, tmX, tmW, a, smem, grid, st); break;
+    default: err = launch_np<128>(c.k, tmX, tmW, a, smem, grid, st); break;
+  }
+  count_launch();
+  if (err != cudaSuccess) return err;
+  return launch_psum_reduce(n_tiles, c.E, psum_partial, psum, st);
+}
+
+}  // namespace moe

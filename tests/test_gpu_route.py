@@ -1,0 +1,112 @@
+"""Router parity on ragged shapes, through the C ABI (moe_route).
+
+Both routers are checked: the tensor-core router (bf16, E <= 256, the default
+for bf16 layers) and the CUDA-core router (MOE_ROUTE_IMPL=simt).  Against
+the oracle ("MoE 模型原理" §2.1–§2.2):
+
+* logits within 1e-5 · max(|ref|, rms(row)) of the double-precision router;
+* top-k ids bit-exact with the oracle's selection on the device's own fp32
+  logits (so both sides rank the same numbers), weights and Σ_t p within 1e-4.
+
+Shapes cover a ragged last token tile, d not a multiple of the 64-wide
+k-block, E not a multiple of 16, E = 1, k = E, k = 16, the widest E (256),
+and exact ties (equal logits must go to the lower expert index).
+"""
+
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from routing_dispatch_expert_06_b300 import build, inputs, moe
+
+from parity import assert_rel_rms, h
+
+pytestmark = pytest.mark.gpu
+
+# (T, d, E, k, renormalize, router bias)
+CASES = [
+    (300, 200, 20, 3, True, "normal:1.0"),
+    (129, 72, 1, 1, True, "zero"),
+    (1000, 520, 256, 16, False, "normal:1.0"),
+    (64, 64, 16, 16, True, "zipf:0.8"),
+    (5000, 1024, 8, 2, True, "zero"),
+    (777, 7168, 256, 8, False, "normal:1.0"),
+    (2, 8, 3, 2, True, "linear_skew"),
+    (4097, 2048, 64, 6, True, "zipf:0.8"),
+]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    build.build()
+    moe.load()
+
+
+def _workload(T, d, E, k, renorm, bias, seed=11):
+    return inputs.Workload(f"route_t{T}_d{d}_e{E}_top{k}", T, d, 8, E, k, 1.0, renorm,
+                           "gelu_tanh", "bf16", seed, bias)
+
+
+def _route(wl, inp, impl):
+    cfg = moe.config_from_workload(wl, write_logits=True)
+    ws = moe.workspace(cfg)
+    out = moe.allocate(cfg)
+    if impl == "simt":
+        os.environ["MOE_ROUTE_IMPL"] = "simt"
+    try:
+        moe.route(cfg, inp["x"], inp["Wr"], inp["br"], out, ws)
+        torch.cuda.synchronize()
+    finally:
+        os.environ.pop("MOE_ROUTE_IMPL", None)
+    assert moe.device_status(ws) == moe.MOE_OK
+    return out
+
+
+def _check(wl, inp, out):
+    logits = h(out["logits"])
+    ref = oracle.router_logits(h(inp["x"]), h(inp["Wr"]), h(inp["br"]))
+    assert_rel_rms(logits, ref, 1e-5, "logits")
+    ids, w, psum, _ = oracle.select(logits, wl.k, wl.renormalize)
+    np.testing.assert_array_equal(h(out["topk_ids"]), ids, "topk_ids")
+    assert_rel_rms(h(out["topk_w"]), w, 1e-4, "topk_w")
+    assert_rel_rms(h(out["psum"]), psum, 1e-4, "psum")
+
+
+@pytest.mark.parametrize("impl", ["tc", "simt"])
+@pytest.mark.parametrize("case", CASES, ids=lambda c: f"t{c[0]}_d{c[1]}_e{c[2]}_k{c[3]}")
+def test_router_matches_oracle(case, impl):
+    wl = _workload(*case)
+    inp = inputs.make_inputs(wl, "cuda")
+    _check(wl, inp, _route(wl, inp, impl))
+
+
+@pytest.mark.parametrize("impl", ["tc", "simt"])
+def test_router_ties_go_to_lower_index(impl):
+    # W_r = 0 makes every logit equal to its bias; the bias repeats values, so
+    # the ranking must break ties by the lower expert index.
+    T, d, E, k = 200, 128, 24, 5
+    wl = _workload(T, d, E, k, True, "zero")
+    inp = inputs.make_inputs(wl, "cuda")
+    inp["Wr"].zero_()
+    inp["br"].copy_(torch.tensor([0.5, 1.0, 1.0, 0.25, 1.0, 0.5] * 4, device="cuda"))
+    out = _route(wl, inp, impl)
+    ids = h(out["topk_ids"])
+    assert (ids == np.array([1, 2, 4, 7, 8], np.int32)).all()
+    _check(wl, inp, out)
+    np.testing.assert_allclose(h(out["topk_w"]), 0.2, rtol=1e-6)
+
+
+def test_tensor_core_router_agrees_with_cuda_core_router():
+    wl = _workload(3000, 2048, 64, 6, True, "zipf:0.8", seed=5)
+    inp = inputs.make_inputs(wl, "cuda")
+    a = _route(wl, inp, "tc")
+    b = _route(wl, inp, "simt")
+    la, lb = h(a["logits"]), h(b["logits"])
+    assert_rel_rms(la, lb.astype(np.float64), 2e-5, "tc vs simt logits")
+    same = (h(a["topk_ids"]) == h(b["topk_ids"])).all(axis=1)
+    # the two routers round differently, so a near-tie may rank differently;
+    # with these seeded inputs nearly every token must agree
+    assert same.mean() > 0.99
