@@ -9,14 +9,18 @@
 //   A [R, K] bf16 (K contiguous), B [E, N, K] bf16 (K contiguous),
 //   epi = σ then round to bf16 (first GEMM) or round to bf16 (second GEMM).
 //
-// Design: a persistent kernel, one CTA per SM, 6 warps:
+// Design: a persistent kernel, one CTA per SM, 10 warps:
 //   warp 0     TMA producer: 128×64 A tile + BN×64 B tile per stage, 128-byte
 //              swizzle, kStages-deep ring of shared-memory stages
 //   warp 1     TMEM allocator and MMA issuer: tcgen05.mma M=128, N=BN, K=16,
 //              fp32 accumulators in tensor memory, two accumulator buffers so
 //              the epilogue of one tile overlaps the main loop of the next
-//   warps 2-5  epilogue: tcgen05.ld one row per thread, bias, σ, bf16,
-//              masked 16-byte stores (rows past the expert's end are skipped)
+//   warps 2-9  epilogue, two warps per TMEM lane quarter (one per column
+//              half): tcgen05.ld 32 columns of one row per thread, bias
+//              (16-byte broadcast loads), σ, bf16, then a transpose through a
+//              2 KiB per-warp shared buffer so each store instruction writes
+//              8 rows × 64 contiguous bytes; rows past the expert's end and
+//              columns past N are masked
 // Tiles never straddle two experts.  Tile order is expert-major, and within
 // an expert m-fastest, so a wave of CTAs shares the weight tile B[e, n-tile]
 // through L2 while the expert's A rows stay L2-resident across n-tiles.
@@ -35,12 +39,15 @@ namespace {
 constexpr int kTileM = 128;
 constexpr int kTileK = 64;              // 64 bf16 = one 128-byte swizzle row
 constexpr int kStages = 4;
-constexpr int kThreads = 192;
 constexpr int kEpiWarp0 = 2;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
+constexpr int kEpiBufBytes = 32 * 64;   // per epilogue warp: 32 rows × 32 bf16
 constexpr uint32_t kTmemCols = 512;
 constexpr int kAccCols = 256;           // each of the two accumulators owns 256 columns
 constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s
 constexpr int kMaxExperts = 1024;
+enum { kActNone = -1 };
 
 struct TileCoord {
   int e, m0, m_end, n0;
@@ -69,10 +76,19 @@ __device__ __forceinline__ TileCoord tile_coord(int64_t i, const int* mt_prefix,
   return c;
 }
 
+template <int ACT>
+__device__ __forceinline__ float epi_act(float u) {
+  if constexpr (ACT == MOE_ACT_RELU) return u > 0.f ? u : 0.f;
+  if constexpr (ACT == MOE_ACT_GELU_TANH)
+    return 0.5f * u * (1.f + tc::tanh_fast(0.7978845608028654f * (u + 0.044715f * u * u * u)));
+  return u;
+}
+
+template <int ACT>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    int E, int N, int K, int BN, const int32_t* __restrict__ offsets,
-                   const float* __restrict__ bias, int act, __nv_bfloat16* __restrict__ out,
+                   const float* __restrict__ bias, __nv_bfloat16* __restrict__ out,
                    int64_t max_rows, int32_t* status) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ uint64_t full_bar[kStages], empty_bar[kStages];
@@ -89,6 +105,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t b_bytes = uint32_t(BN) * kTileK * 2;
   uint8_t* sA = smem;                       // kStages × a_bytes
   uint8_t* sB = smem + kStages * a_bytes;   // kStages × b_bytes
+  uint8_t* sE = sB + kStages * b_bytes;     // kEpiWarps × kEpiBufBytes
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -97,7 +114,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       tc::mbar_init(&tfull_bar[a], 1);
-      tc::mbar_init(&tempty_bar[a], 4 * 32);
+      tc::mbar_init(&tempty_bar[a], kEpiWarps * 32);
     }
     tc::mbar_init(&drain_bar, 1);
     s_abort = 0;
@@ -223,7 +240,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::mbar_wait(&drain_bar, 0, nullptr, kWaitLimitNs);
   } else if (warp >= kEpiWarp0) {
     // ---------------- epilogue ----------------
-    const int quarter = warp & 3;  // TMEM lanes [32·quarter, 32·quarter+32)
+    const int quarter = warp & 3;              // TMEM lanes [32·quarter, 32·quarter+32)
+    const int half = (warp - kEpiWarp0) >> 2;  // columns [c_lo, c_hi) of the tile
+    const int hb = ((BN / 2 + 15) / 16) * 16;
+    const int c_lo = half * hb, c_hi = min(BN, c_lo + hb);
+    uint8_t* buf = sE + (warp - kEpiWarp0) * kEpiBufBytes;
+    const uint32_t buf_s = tc::smem_u32(buf);
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int64_t i = blockIdx.x; i < total; i += gridDim.x) {
@@ -236,36 +258,60 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc::fence_after_sync();
-      const int row = c.m0 + quarter * 32 + lane;
-      const bool row_ok = row < c.m_end;
       const int ncols = min(BN, N - c.n0);
       const float* bias_e = bias + int64_t(c.e) * N + c.n0;
-      __nv_bfloat16* out_row = out + int64_t(row) * N + c.n0;
+      const int row0 = c.m0 + quarter * 32;
       const uint32_t t_row = tmem_base + (uint32_t(quarter * 32) << 16) + uint32_t(acc * kAccCols);
-      for (int c0 = 0; c0 < ncols; c0 += 16) {
-        uint32_t r[16];
-        tc::tmem_ld_x16(t_row + uint32_t(c0), r);
-        tc::tmem_ld_wait();
-        if (row_ok) {
-          float v[16];
+      for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
+        uint32_t r[32];
+        tc::tmem_ld_x32(t_row + uint32_t(c0), r);
+        float b[32];
+        if (c0 + 32 <= ncols) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            float u = __uint_as_float(r[j]) + (c0 + j < ncols ? __ldg(bias_e + c0 + j) : 0.f);
-            if (act == MOE_ACT_RELU)
-              u = u > 0.f ? u : 0.f;
-            else if (act == MOE_ACT_GELU_TANH)
-              u = 0.5f * u * (1.f + tc::tanh_fast(0.7978845608028654f * (u + 0.044715f * u * u * u)));
-            v[j] = u;
+          for (int j = 0; j < 32; j += 4) {
+            const float4 q = __ldg(reinterpret_cast<const float4*>(bias_e + c0 + j));
+            b[j] = q.x, b[j + 1] = q.y, b[j + 2] = q.z, b[j + 3] = q.w;
           }
-          uint4 p[2];
-          __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(p);
+        } else {
 #pragma unroll
-          for (int j = 0; j < 8; ++j) h[j] = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
-          // N is a multiple of 8, so a chunk holds 8 or 16 valid columns.
-          uint4* dst = reinterpret_cast<uint4*>(out_row + c0);
-          dst[0] = p[0];
-          if (c0 + 16 <= ncols) dst[1] = p[1];
+          for (int j = 0; j < 32; ++j) b[j] = c0 + j < ncols ? __ldg(bias_e + c0 + j) : 0.f;
         }
+        tc::tmem_ld_wait();
+        uint32_t pk[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float u0 = epi_act<ACT>(__uint_as_float(r[2 * j]) + b[2 * j]);
+          const float u1 = epi_act<ACT>(__uint_as_float(r[2 * j + 1]) + b[2 * j + 1]);
+          const __nv_bfloat162 h2 = __floats2bfloat162_rn(u0, u1);
+          pk[j] = *reinterpret_cast<const uint32_t*>(&h2);
+        }
+        // Row `lane` of the warp's 32×32 block -> shared buffer (64 bytes per
+        // row, 16-byte pieces XOR-swizzled by row so that each group of 8
+        // lanes hits distinct banks).
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t addr = buf_s + uint32_t(lane * 64 + ((q ^ ((lane >> 1) & 3)) * 16));
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[4 * q]),
+                       "r"(pk[4 * q + 1]), "r"(pk[4 * q + 2]), "r"(pk[4 * q + 3])
+                       : "memory");
+        }
+        __syncwarp();
+        // Read back 8 rows × 4 pieces per step: each store covers 8 rows of
+        // 64 contiguous bytes.
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+          const int rr = it * 8 + (lane >> 2), q = lane & 3;
+          const uint32_t addr = buf_s + uint32_t(rr * 64 + ((q ^ ((rr >> 1) & 3)) * 16));
+          uint4 v;
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                       : "r"(addr)
+                       : "memory");
+          const int grow = row0 + rr, gcol = c0 + q * 8;
+          if (grow < c.m_end && gcol < ncols)
+            *reinterpret_cast<uint4*>(out + int64_t(grow) * N + c.n0 + gcol) = v;
+        }
+        __syncwarp();
       }
       tc::fence_before_sync();
       tc::mbar_arrive(&tempty_bar[acc]);
@@ -338,15 +384,24 @@ cudaError_t launch_gemm_tc(int E, int N, int K, int64_t max_rows, const int32_t*
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  const size_t smem = 1024 + size_t(kStages) * (kTileM * kTileK * 2 + size_t(BN) * kTileK * 2);
-  cudaError_t err =
-      cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-  if (err != cudaSuccess) return err;
+  const size_t smem = 1024 + size_t(kStages) * (kTileM * kTileK * 2 + size_t(BN) * kTileK * 2) +
+                      size_t(kEpiWarps) * kEpiBufBytes;
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  gemm_tc_kernel<<<unsigned(sms), kThreads, smem, st>>>(
-      tmA, tmB, E, N, K, BN, offsets, bias, act, static_cast<__nv_bfloat16*>(out), max_rows, status);
+  auto run = [&](auto kernel) {
+    cudaError_t err =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (err != cudaSuccess) return err;
+    kernel<<<unsigned(sms), kThreads, smem, st>>>(tmA, tmB, E, N, K, BN, offsets, bias,
+                                                  static_cast<__nv_bfloat16*>(out), max_rows,
+                                                  status);
+    return cudaGetLastError();
+  };
+  cudaError_t err = act == MOE_ACT_RELU        ? run(gemm_tc_kernel<MOE_ACT_RELU>)
+                    : act == MOE_ACT_GELU_TANH ? run(gemm_tc_kernel<MOE_ACT_GELU_TANH>)
+                                               : run(gemm_tc_kernel<kActNone>);
+  if (err != cudaSuccess) return err;
   count_launch();
   return cudaGetLastError();
 }
