@@ -14,8 +14,6 @@
 
 namespace moe {
 
-constexpr int kMaxK = 16;  // largest k the library accepts
-
 template <typename T>
 struct Vec;
 template <>
@@ -53,7 +51,12 @@ struct Vec<float> {
   }
 };
 
-template <typename T>
+// One warp per token.  Lane r < k fetches slot r's row and weight; every
+// lane then holds all k (row, weight) pairs.  For each 16-byte column vector
+// the k row loads are issued together before any arithmetic, so a lane keeps
+// up to KMAX independent loads in flight; the weighted sum then runs in rank
+// order (a dropped slot adds 0·0, which leaves the fp32 sum unchanged).
+template <typename T, int KMAX>
 __global__ void __launch_bounds__(256)
     combine_kernel(int64_t n_tok, int k, int64_t row_vecs, int64_t max_rows,
                    const uint4* __restrict__ yd,
@@ -64,29 +67,40 @@ __global__ void __launch_bounds__(256)
   const int64_t warps = int64_t(gridDim.x) * (blockDim.x >> 5);
   for (int64_t t = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); t < n_tok;
        t += warps) {
-    const int32_t my_row = lane < k ? slot_row[t * k + lane] : -1;
+    int32_t my_row = lane < k ? slot_row[t * k + lane] : -1;
+    if (my_row >= max_rows) my_row = -1;
     const float my_w = lane < k ? w[t * k + lane] : 0.f;
-    int32_t rows[kMaxK];
-    float wts[kMaxK];
+    const uint4* src[KMAX];
+    float wts[KMAX];
+    bool kept[KMAX];
 #pragma unroll
-    for (int r = 0; r < kMaxK; ++r) {
-      rows[r] = __shfl_sync(0xffffffffu, my_row, r);
-      wts[r] = __shfl_sync(0xffffffffu, my_w, r);
+    for (int r = 0; r < KMAX; ++r) {
+      const int32_t row = __shfl_sync(0xffffffffu, my_row, r);
+      kept[r] = r < k && row >= 0;
+      wts[r] = kept[r] ? __shfl_sync(0xffffffffu, my_w, r) : 0.f;
+      src[r] = yd + (kept[r] ? int64_t(row) * row_vecs : 0);
     }
     for (int64_t v = lane; v < row_vecs; v += 32) {
+      uint4 buf[KMAX];
+#pragma unroll
+      for (int r = 0; r < KMAX; ++r)
+        if (kept[r]) buf[r] = __ldcs(src[r] + v);
       float acc[NV];
 #pragma unroll
       for (int i = 0; i < NV; ++i) acc[i] = 0.f;
 #pragma unroll
-      for (int r = 0; r < kMaxK; ++r) {
-        if (r < k && rows[r] >= 0 && rows[r] < max_rows) {
-          float f[NV];
-          Vec<T>::unpack(yd[int64_t(rows[r]) * row_vecs + v], f);
+      for (int r = 0; r < KMAX; ++r) {
+        float f[NV];
+        if (kept[r]) {
+          Vec<T>::unpack(buf[r], f);
+        } else {
 #pragma unroll
-          for (int i = 0; i < NV; ++i) acc[i] = fmaf(wts[r], f[i], acc[i]);
+          for (int i = 0; i < NV; ++i) f[i] = 0.f;
         }
+#pragma unroll
+        for (int i = 0; i < NV; ++i) acc[i] = fmaf(wts[r], f[i], acc[i]);
       }
-      y[t * row_vecs + v] = Vec<T>::pack(acc);
+      __stcs(y + t * row_vecs + v, Vec<T>::pack(acc));
     }
   }
 }
@@ -123,14 +137,21 @@ cudaError_t launch_combine(const moe_config_t& c, int64_t max_rows, const void* 
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int64_t want = (c.T + 7) / 8;
   const unsigned grid = unsigned(want < int64_t(sms) * 8 ? want : int64_t(sms) * 8);
-  if (c.dtype == MOE_DT_BF16)
-    combine_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(c.T, c.k, row_vecs, max_rows,
-                                                        static_cast<const uint4*>(yd), slot_row,
-                                                        w, static_cast<uint4*>(y));
-  else
-    combine_kernel<float><<<grid, 256, 0, st>>>(c.T, c.k, row_vecs, max_rows,
-                                                static_cast<const uint4*>(yd),
-                                                slot_row, w, static_cast<uint4*>(y));
+  auto run = [&](auto kernel) {
+    kernel<<<grid, 256, 0, st>>>(c.T, c.k, row_vecs, max_rows, static_cast<const uint4*>(yd),
+                                 slot_row, w, static_cast<uint4*>(y));
+  };
+  if (c.dtype == MOE_DT_BF16) {
+    if (c.k <= 2) run(combine_kernel<__nv_bfloat16, 2>);
+    else if (c.k <= 4) run(combine_kernel<__nv_bfloat16, 4>);
+    else if (c.k <= 8) run(combine_kernel<__nv_bfloat16, 8>);
+    else run(combine_kernel<__nv_bfloat16, 16>);
+  } else {
+    if (c.k <= 2) run(combine_kernel<float, 2>);
+    else if (c.k <= 4) run(combine_kernel<float, 4>);
+    else if (c.k <= 8) run(combine_kernel<float, 8>);
+    else run(combine_kernel<float, 16>);
+  }
   count_launch();
   return cudaGetLastError();
 }

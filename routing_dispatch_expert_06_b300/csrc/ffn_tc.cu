@@ -11,7 +11,8 @@
 //
 // Design: a persistent kernel, one CTA per SM, 10 warps:
 //   warp 0     TMA producer: 128×64 A tile + BN×64 B tile per stage, 128-byte
-//              swizzle, kStages-deep ring of shared-memory stages
+//              swizzle, a ring of as many shared-memory stages as fit (4 at
+//              BN = 256)
 //   warp 1     TMEM allocator and MMA issuer: tcgen05.mma M=128, N=BN, K=16,
 //              fp32 accumulators in tensor memory, two accumulator buffers so
 //              the epilogue of one tile overlaps the main loop of the next
@@ -38,7 +39,7 @@ namespace {
 
 constexpr int kTileM = 128;
 constexpr int kTileK = 64;              // 64 bf16 = one 128-byte swizzle row
-constexpr int kStages = 4;
+constexpr int kMaxStages = 8;
 constexpr int kEpiWarp0 = 2;
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
@@ -89,9 +90,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    int E, int N, int K, int BN, const int32_t* __restrict__ offsets,
                    const float* __restrict__ bias, __nv_bfloat16* __restrict__ out,
-                   int64_t max_rows, int32_t* status) {
+                   int64_t max_rows, int32_t* status, int stages) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  __shared__ uint64_t full_bar[kStages], empty_bar[kStages];
+  __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages];
   __shared__ uint64_t tfull_bar[2], tempty_bar[2], drain_bar;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
@@ -103,12 +104,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              ~uintptr_t(1023));
   const uint32_t a_bytes = kTileM * kTileK * 2;
   const uint32_t b_bytes = uint32_t(BN) * kTileK * 2;
-  uint8_t* sA = smem;                       // kStages × a_bytes
-  uint8_t* sB = smem + kStages * a_bytes;   // kStages × b_bytes
-  uint8_t* sE = sB + kStages * b_bytes;     // kEpiWarps × kEpiBufBytes
+  uint8_t* sA = smem;                      // stages × a_bytes
+  uint8_t* sB = smem + stages * a_bytes;   // stages × b_bytes
+  uint8_t* sE = sB + stages * b_bytes;     // kEpiWarps × kEpiBufBytes
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < stages; ++s) {
       tc::mbar_init(&full_bar[s], 1);
       tc::mbar_init(&empty_bar[s], 1);
     }
@@ -176,9 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- TMA producer ----------------
     int stage = 0;
     uint32_t phase = 0;
-    uint32_t armed_phase[kStages];
-    bool armed[kStages];
-    for (int s = 0; s < kStages; ++s) armed[s] = false, armed_phase[s] = 0;
+    int64_t issued = 0;
     bool ok = true;
     for (int64_t i = blockIdx.x; i < total && ok; i += gridDim.x) {
       const TileCoord c = tile_coord(i, s_mt, E, n_tn, s_off, BN);
@@ -191,15 +190,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::mbar_arrive_expect_tx(&full_bar[stage], a_bytes + b_bytes);
         tc::tma_load_2d(&tmA, &full_bar[stage], sA + stage * a_bytes, kb * kTileK, c.m0);
         tc::tma_load_3d(&tmB, &full_bar[stage], sB + stage * b_bytes, kb * kTileK, c.n0, c.e);
-        armed[stage] = true;
-        armed_phase[stage] = phase;
-        if (++stage == kStages) stage = 0, phase ^= 1u;
+        ++issued;
+        if (++stage == stages) stage = 0, phase ^= 1u;
       }
     }
-    // Drain: every copy this thread issued must land before the CTA exits
-    // (already true on the normal path, where the MMA issuer consumed them).
-    for (int s = 0; s < kStages; ++s)
-      if (armed[s]) tc::mbar_wait(&full_bar[s], armed_phase[s], nullptr, kWaitLimitNs);
+    // Drain: the last `stages` copies this thread issued must land before the
+    // CTA exits (on the normal path the MMA issuer has consumed them all).
+    const int64_t first = issued > stages ? issued - stages : 0;
+    for (int64_t j = first; j < issued; ++j)
+      tc::mbar_wait(&full_bar[j % stages], uint32_t((j / stages) & 1), nullptr, kWaitLimitNs);
   } else if (warp == 1 && lane == 0) {
     // ---------------- MMA issuer ----------------
     const uint32_t idesc = tc::idesc_bf16_f32(kTileM, BN);
@@ -229,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::mma_bf16(d_tmem, tc::sdesc_kmajor_sw128(a0 + j * 32),
                        tc::sdesc_kmajor_sw128(b0 + j * 32), idesc, (kb | j) != 0);
         tc::mma_commit(&empty_bar[stage]);
-        if (++stage == kStages) stage = 0, phase ^= 1u;
+        if (++stage == stages) stage = 0, phase ^= 1u;
       }
       if (!ok) break;
       tc::mma_commit(&tfull_bar[acc]);
@@ -384,21 +383,32 @@ cudaError_t launch_gemm_tc(int E, int N, int K, int64_t max_rows, const int32_t*
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  const size_t smem = 1024 + size_t(kStages) * (kTileM * kTileK * 2 + size_t(BN) * kTileK * 2) +
-                      size_t(kEpiWarps) * kEpiBufBytes;
-  int dev = 0, sms = 148;
+  int dev = 0, sms = 148, smem_optin = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  cudaFuncAttributes fa{};
+  cudaError_t err = cudaFuncGetAttributes(&fa, gemm_tc_kernel<kActNone>);
+  if (err != cudaSuccess) return err;
+  // As many pipeline stages as fit beside the epilogue buffers and the
+  // kernel's static shared memory.
+  const size_t stage_bytes = size_t(kTileM) * kTileK * 2 + size_t(BN) * kTileK * 2;
+  const size_t fixed = 1024 + size_t(kEpiWarps) * kEpiBufBytes;
+  const size_t budget = size_t(smem_optin) - fa.sharedSizeBytes;
+  int stages = budget > fixed ? int((budget - fixed) / stage_bytes) : 0;
+  if (stages > kMaxStages) stages = kMaxStages;
+  if (stages < 2) return cudaErrorInvalidValue;
+  const size_t smem = fixed + size_t(stages) * stage_bytes;
   auto run = [&](auto kernel) {
     cudaError_t err =
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (err != cudaSuccess) return err;
     kernel<<<unsigned(sms), kThreads, smem, st>>>(tmA, tmB, E, N, K, BN, offsets, bias,
                                                   static_cast<__nv_bfloat16*>(out), max_rows,
-                                                  status);
+                                                  status, stages);
     return cudaGetLastError();
   };
-  cudaError_t err = act == MOE_ACT_RELU        ? run(gemm_tc_kernel<MOE_ACT_RELU>)
+  err = act == MOE_ACT_RELU        ? run(gemm_tc_kernel<MOE_ACT_RELU>)
                     : act == MOE_ACT_GELU_TANH ? run(gemm_tc_kernel<MOE_ACT_GELU_TANH>)
                                                : run(gemm_tc_kernel<kActNone>);
   if (err != cudaSuccess) return err;
