@@ -9,13 +9,25 @@
 //   A [R, K] bf16 (K contiguous), B [E, N, K] bf16 (K contiguous),
 //   epi = σ then round to bf16 (first GEMM) or round to bf16 (second GEMM).
 //
-// Design: a persistent kernel, one CTA per SM, 10 warps:
-//   warp 0     TMA producer: 128×64 A tile + BN×64 B tile per stage, 128-byte
-//              swizzle, a ring of as many shared-memory stages as fit (4 at
-//              BN = 256)
-//   warp 1     TMEM allocator and MMA issuer: tcgen05.mma M=128, N=BN, K=16,
-//              fp32 accumulators in tensor memory, two accumulator buffers so
-//              the epilogue of one tile overlaps the main loop of the next
+// Design: a persistent kernel, one CTA per SM, 10 warps.  Two variants share
+// the code (template parameter PAIR):
+//
+//   PAIR = true (default): CTA pairs (clusters of 2) run the 2-SM MMA,
+//     tcgen05.mma.cta_group::2 with M = 256: each CTA stages its own 128 A
+//     rows and half of the BN-column B tile, and each SM's tensor core reads
+//     A from its own shared memory and B from both.  Per SM and k-block that
+//     is 16 KiB of A plus BN/2 rows of B instead of the whole B tile, which
+//     halves the shared-memory traffic for B (the 1-SM variant needs about
+//     192 B/clk of operand reads plus TMA writes per SM at full MMA rate, more
+//     than shared memory delivers) and leaves room for 6 stages at BN = 256.
+//   PAIR = false: one CTA per tile, tcgen05.mma.cta_group::1, M = 128.
+//
+//   warp 0     TMA producer: 128×64 A tile + (BN or BN/2)×64 B tile per stage,
+//              128-byte swizzle, a ring of as many stages as fit
+//   warp 1     TMEM allocator and (in the even CTA of a pair) MMA issuer:
+//              tcgen05.mma K=16, fp32 accumulators in tensor memory, two
+//              accumulator buffers so the epilogue of one tile overlaps the
+//              main loop of the next
 //   warps 2-9  epilogue, two warps per TMEM lane quarter (one per column
 //              half): tcgen05.ld 32 columns of one row per thread, bias
 //              (16-byte broadcast loads), σ, bf16, then a transpose through a
@@ -28,6 +40,8 @@
 // Every wait is bounded: on a timeout the kernel records MOE_ERR_TIMEOUT,
 // drains its own copies and MMAs, frees its tensor memory and returns.
 #include <cstdio>
+#include <cstdlib>
+#include <cstring>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -37,7 +51,7 @@ namespace moe {
 
 namespace {
 
-constexpr int kTileM = 128;
+constexpr int kTileM = 128;             // rows per CTA (a pair covers 256)
 constexpr int kTileK = 64;              // 64 bf16 = one 128-byte swizzle row
 constexpr int kMaxStages = 8;
 constexpr int kEpiWarp0 = 2;
@@ -54,8 +68,11 @@ struct TileCoord {
   int e, m0, m_end, n0;
 };
 
+// Tile i of the expert-major order.  rows_per_tile = 128 (one CTA) or 256
+// (a CTA pair; `rank` selects the pair's lower or upper 128 rows).
 __device__ __forceinline__ TileCoord tile_coord(int64_t i, const int* mt_prefix, int E, int n_tn,
-                                                const int32_t* offsets_s, int BN) {
+                                                const int32_t* offsets_s, int BN,
+                                                int rows_per_tile, int rank) {
   // Find e with mt_prefix[e]*n_tn <= i < mt_prefix[e+1]*n_tn.
   int lo = 0, hi = E;  // invariant: prefix[lo]*n_tn <= i < prefix[hi]*n_tn
   while (hi - lo > 1) {
@@ -71,7 +88,7 @@ __device__ __forceinline__ TileCoord tile_coord(int64_t i, const int* mt_prefix,
   const int nt = int(local / mts), mt = int(local % mts);
   TileCoord c;
   c.e = e;
-  c.m0 = offsets_s[e] + mt * kTileM;
+  c.m0 = offsets_s[e] + mt * rows_per_tile + rank * kTileM;
   c.m_end = offsets_s[e + 1] > offsets_s[e] ? offsets_s[e + 1] : offsets_s[e];
   c.n0 = nt * BN;
   return c;
@@ -85,7 +102,7 @@ __device__ __forceinline__ float epi_act(float u) {
   return u;
 }
 
-template <int ACT>
+template <int ACT, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    int E, int N, int K, int BN, const int32_t* __restrict__ offsets,
@@ -100,10 +117,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ int32_t s_off[kMaxExperts + 1];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = PAIR ? tc::cluster_ctarank() : 0u;  // 0 = the pair's MMA issuer
+  const int rows_per_tile = PAIR ? 2 * kTileM : kTileM;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
+  const int bn_cta = PAIR ? BN / 2 : BN;    // B rows staged by this CTA
   const uint32_t a_bytes = kTileM * kTileK * 2;
-  const uint32_t b_bytes = uint32_t(BN) * kTileK * 2;
+  const uint32_t b_bytes = uint32_t(bn_cta) * kTileK * 2;
   uint8_t* sA = smem;                      // stages × a_bytes
   uint8_t* sB = smem + stages * a_bytes;   // stages × b_bytes
   uint8_t* sE = sB + stages * b_bytes;     // kEpiWarps × kEpiBufBytes
@@ -115,7 +135,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       tc::mbar_init(&tfull_bar[a], 1);
-      tc::mbar_init(&tempty_bar[a], kEpiWarps * 32);
+      // One arrival per epilogue warp (of both CTAs of a pair).
+      tc::mbar_init(&tempty_bar[a], PAIR ? 2 * kEpiWarps : kEpiWarps);
     }
     tc::mbar_init(&drain_bar, 1);
     s_abort = 0;
@@ -123,9 +144,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::prefetch_tmap(&tmA);
     tc::prefetch_tmap(&tmB);
   }
+  // A pair allocates its tensor memory collectively (one warp in each CTA),
+  // and the peer's barriers must be initialised before any copy or commit of
+  // the pair can signal them: both need the peer CTA present.
+  if constexpr (PAIR) tc::cluster_sync();
   if (warp == 1) {
-    tc::tmem_alloc(&s_tmem, kTmemCols);
-    tc::tmem_relinquish();
+    if constexpr (PAIR) {
+      tc::tmem_alloc_pair(&s_tmem, kTmemCols);
+      tc::tmem_relinquish_pair();
+    } else {
+      tc::tmem_alloc(&s_tmem, kTmemCols);
+      tc::tmem_relinquish();
+    }
   }
   // Per-expert m-tile prefix: warp 0 scans runs of experts, one run per lane.
   // Row offsets are clamped to [0, max_rows] so that no tile can reach
@@ -141,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int e = lo; e < hi; ++e) {
       const int32_t a = clamp_row(e), b = clamp_row(e + 1);
       s_off[e] = a;
-      run += b > a ? (b - a + kTileM - 1) / kTileM : 0;
+      run += b > a ? (b - a + rows_per_tile - 1) / rows_per_tile : 0;
     }
     if (lane == 31) s_off[E] = clamp_row(E);
     int incl = run;
@@ -154,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int e = lo; e < hi; ++e) {
       s_mt[e] = acc;
       const int32_t a = clamp_row(e), b = clamp_row(e + 1);
-      acc += b > a ? (b - a + kTileM - 1) / kTileM : 0;
+      acc += b > a ? (b - a + rows_per_tile - 1) / rows_per_tile : 0;
     }
     if (lane == 31) s_mt[E] = incl;
   }
@@ -166,6 +196,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_tn = (N + BN - 1) / BN;
   const int64_t total = int64_t(s_mt[E]) * n_tn;
   const int nk = (K + kTileK - 1) / kTileK;
+  const int64_t first_tile = PAIR ? blockIdx.x / 2 : blockIdx.x;
+  const int64_t tile_step = PAIR ? gridDim.x / 2 : gridDim.x;
   volatile int* abort_flag = &s_abort;
 
   auto give_up = [&]() {
@@ -179,36 +211,53 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t phase = 0;
     int64_t issued = 0;
     bool ok = true;
-    for (int64_t i = blockIdx.x; i < total && ok; i += gridDim.x) {
-      const TileCoord c = tile_coord(i, s_mt, E, n_tn, s_off, BN);
+    for (int64_t i = first_tile; i < total && ok; i += tile_step) {
+      const TileCoord c = tile_coord(i, s_mt, E, n_tn, s_off, BN, rows_per_tile, int(rank));
       for (int kb = 0; kb < nk; ++kb) {
         if (!tc::mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, kWaitLimitNs)) {
           give_up();
           ok = false;
           break;
         }
-        tc::mbar_arrive_expect_tx(&full_bar[stage], a_bytes + b_bytes);
-        tc::tma_load_2d(&tmA, &full_bar[stage], sA + stage * a_bytes, kb * kTileK, c.m0);
-        tc::tma_load_3d(&tmB, &full_bar[stage], sB + stage * b_bytes, kb * kTileK, c.n0, c.e);
+        if constexpr (PAIR) {
+          // Both CTAs' copies complete on the even CTA's full barrier, which
+          // expects the bytes of the whole pair.
+          if (rank == 0) tc::mbar_arrive_expect_tx(&full_bar[stage], 2 * (a_bytes + b_bytes));
+          const uint32_t bar = tc::mapa(tc::smem_u32(&full_bar[stage]), 0);
+          tc::tma_load_2d_pair(&tmA, bar, sA + stage * a_bytes, kb * kTileK, c.m0);
+          tc::tma_load_3d_pair(&tmB, bar, sB + stage * b_bytes, kb * kTileK,
+                               c.n0 + int(rank) * bn_cta, c.e);
+        } else {
+          tc::mbar_arrive_expect_tx(&full_bar[stage], a_bytes + b_bytes);
+          tc::tma_load_2d(&tmA, &full_bar[stage], sA + stage * a_bytes, kb * kTileK, c.m0);
+          tc::tma_load_3d(&tmB, &full_bar[stage], sB + stage * b_bytes, kb * kTileK, c.n0, c.e);
+        }
         ++issued;
         if (++stage == stages) stage = 0, phase ^= 1u;
       }
     }
-    // Drain: the last `stages` copies this thread issued must land before the
-    // CTA exits (on the normal path the MMA issuer has consumed them all).
-    const int64_t first = issued > stages ? issued - stages : 0;
-    for (int64_t j = first; j < issued; ++j)
-      tc::mbar_wait(&full_bar[j % stages], uint32_t((j / stages) & 1), nullptr, kWaitLimitNs);
-  } else if (warp == 1 && lane == 0) {
+    // Drain: the last `stages` copies must land before the CTA exits (on the
+    // normal path the MMA issuer has consumed them all).  In a pair the even
+    // CTA's full barriers track the copies of both CTAs.
+    if (rank == 0) {
+      const int64_t first = issued > stages ? issued - stages : 0;
+      for (int64_t j = first; j < issued; ++j)
+        tc::mbar_wait(&full_bar[j % stages], uint32_t((j / stages) & 1), nullptr, kWaitLimitNs);
+    }
+  } else if (warp == 1 && lane == 0 && rank == 0) {
     // ---------------- MMA issuer ----------------
-    const uint32_t idesc = tc::idesc_bf16_f32(kTileM, BN);
+    const uint32_t idesc = tc::idesc_bf16_f32(rows_per_tile, BN);
     int stage = 0;
     uint32_t phase = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
-    for (int64_t i = blockIdx.x; i < total && ok; i += gridDim.x) {
-      if (!tc::mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort_flag, kWaitLimitNs)) {
+    for (int64_t i = first_tile; i < total && ok; i += tile_step) {
+      const bool free_acc = PAIR ? tc::mbar_wait_cluster(&tempty_bar[acc], acc_phase ^ 1u,
+                                                         abort_flag, kWaitLimitNs)
+                                 : tc::mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort_flag,
+                                                 kWaitLimitNs);
+      if (!free_acc) {
         give_up();
         break;
       }
@@ -224,18 +273,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t a0 = tc::smem_u32(sA + stage * a_bytes);
         const uint32_t b0 = tc::smem_u32(sB + stage * b_bytes);
 #pragma unroll
-        for (int j = 0; j < kTileK / 16; ++j)
-          tc::mma_bf16(d_tmem, tc::sdesc_kmajor_sw128(a0 + j * 32),
-                       tc::sdesc_kmajor_sw128(b0 + j * 32), idesc, (kb | j) != 0);
-        tc::mma_commit(&empty_bar[stage]);
+        for (int j = 0; j < kTileK / 16; ++j) {
+          const uint64_t ad = tc::sdesc_kmajor_sw128(a0 + j * 32);
+          const uint64_t bd = tc::sdesc_kmajor_sw128(b0 + j * 32);
+          if constexpr (PAIR)
+            tc::mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | j) != 0);
+          else
+            tc::mma_bf16(d_tmem, ad, bd, idesc, (kb | j) != 0);
+        }
+        if constexpr (PAIR)
+          tc::mma_commit_pair_mc(&empty_bar[stage], 0x3);
+        else
+          tc::mma_commit(&empty_bar[stage]);
         if (++stage == stages) stage = 0, phase ^= 1u;
       }
       if (!ok) break;
-      tc::mma_commit(&tfull_bar[acc]);
+      if constexpr (PAIR)
+        tc::mma_commit_pair_mc(&tfull_bar[acc], 0x3);
+      else
+        tc::mma_commit(&tfull_bar[acc]);
       if (++acc == 2) acc = 0, acc_phase ^= 1u;
     }
     // Drain: wait until every MMA this thread issued has completed.
-    tc::mma_commit(&drain_bar);
+    if constexpr (PAIR)
+      tc::mma_commit_pair(&drain_bar);
+    else
+      tc::mma_commit(&drain_bar);
     tc::mbar_wait(&drain_bar, 0, nullptr, kWaitLimitNs);
   } else if (warp >= kEpiWarp0) {
     // ---------------- epilogue ----------------
@@ -247,8 +310,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t buf_s = tc::smem_u32(buf);
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int64_t i = blockIdx.x; i < total; i += gridDim.x) {
-      const TileCoord c = tile_coord(i, s_mt, E, n_tn, s_off, BN);
+    for (int64_t i = first_tile; i < total; i += tile_step) {
+      const TileCoord c = tile_coord(i, s_mt, E, n_tn, s_off, BN, rows_per_tile, int(rank));
       // The tensor-memory loads below are warp-collective: the whole warp
       // takes the same branch.
       if (!__all_sync(0xffffffffu, tc::mbar_wait(&tfull_bar[acc], acc_phase, abort_flag,
@@ -312,17 +375,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
       }
+      // This warp is done reading the accumulator: one arrival per warp on
+      // the MMA issuer's barrier (in the even CTA of a pair).
       tc::fence_before_sync();
-      tc::mbar_arrive(&tempty_bar[acc]);
+      __syncwarp();
+      if (lane == 0) {
+        if constexpr (PAIR)
+          tc::mbar_arrive_cluster(tc::mapa(tc::smem_u32(&tempty_bar[acc]), 0));
+        else
+          tc::mbar_arrive(&tempty_bar[acc]);
+      }
       if (++acc == 2) acc = 0, acc_phase ^= 1u;
     }
   }
   tc::fence_before_sync();
   __syncthreads();
+  // Neither CTA of a pair leaves (or frees its tensor memory) while the other
+  // may still signal its barriers or feed its MMAs.
+  if constexpr (PAIR) tc::cluster_sync();
   tc::fence_after_sync();
   if (warp == 1) {
     __syncwarp();
-    tc::tmem_dealloc(tmem_base, kTmemCols);
+    if constexpr (PAIR)
+      tc::tmem_dealloc_pair(tmem_base, kTmemCols);
+    else
+      tc::tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
@@ -351,6 +428,70 @@ int pick_bn(int N) {
   return N < 256 ? ((N + 15) / 16) * 16 : 256;
 }
 
+// The 2-SM variant is the default; MOE_GEMM_PAIR=0 selects the 1-SM kernel
+// (a cross-check in tests).
+bool use_pair() {
+  const char* v = std::getenv("MOE_GEMM_PAIR");
+  return !(v && std::strcmp(v, "0") == 0);
+}
+
+template <bool PAIR>
+cudaError_t launch_variant(int act, const CUtensorMap& tmA, const CUtensorMap& tmB, int E, int N,
+                           int K, int BN, const int32_t* offsets, const float* bias, void* out,
+                           int64_t max_rows, int32_t* status, cudaStream_t st) {
+  int dev = 0, sms = 148, smem_optin = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  cudaFuncAttributes fa{};
+  cudaError_t err = cudaFuncGetAttributes(&fa, gemm_tc_kernel<kActNone, PAIR>);
+  if (err != cudaSuccess) return err;
+  // As many pipeline stages as fit beside the epilogue buffers and the
+  // kernel's static shared memory.
+  const int bn_cta = PAIR ? BN / 2 : BN;
+  const size_t stage_bytes = size_t(kTileM) * kTileK * 2 + size_t(bn_cta) * kTileK * 2;
+  const size_t fixed = 1024 + size_t(kEpiWarps) * kEpiBufBytes;
+  const size_t budget = size_t(smem_optin) - fa.sharedSizeBytes;
+  int stages = budget > fixed ? int((budget - fixed) / stage_bytes) : 0;
+  if (stages > kMaxStages) stages = kMaxStages;
+  if (stages < 2) return cudaErrorInvalidValue;
+  const size_t smem = fixed + size_t(stages) * stage_bytes;
+  auto run = [&](auto kernel) {
+    cudaError_t e =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return e;
+    unsigned grid = unsigned(sms);
+    cudaLaunchConfig_t cfg{};
+    cudaLaunchAttribute attr[1];
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    if constexpr (PAIR) {
+      // Persistent grid: as many CTA pairs as can be resident at once.
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      cfg.gridDim = dim3(2);
+      int clusters = 0;
+      e = cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg);
+      if (e != cudaSuccess) return e;
+      if (clusters < 1) return cudaErrorInvalidConfiguration;
+      grid = unsigned(2 * clusters);
+    }
+    cfg.gridDim = dim3(grid);
+    e = cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, E, N, K, BN, offsets, bias,
+                           static_cast<__nv_bfloat16*>(out), max_rows, status, stages);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+  };
+  return act == MOE_ACT_RELU        ? run(gemm_tc_kernel<MOE_ACT_RELU, PAIR>)
+         : act == MOE_ACT_GELU_TANH ? run(gemm_tc_kernel<MOE_ACT_GELU_TANH, PAIR>)
+                                    : run(gemm_tc_kernel<kActNone, PAIR>);
+}
+
 }  // namespace
 
 cudaError_t launch_gemm_tc(int E, int N, int K, int64_t max_rows, const int32_t* offsets,
@@ -360,6 +501,7 @@ cudaError_t launch_gemm_tc(int E, int N, int K, int64_t max_rows, const int32_t*
   EncodeTiledFn encode = get_encode();
   if (!encode) return cudaErrorNotSupported;
   const int BN = pick_bn(N);
+  const bool pair = use_pair();
   CUtensorMap tmA, tmB;
   {
     const cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(max_rows)};
@@ -375,7 +517,7 @@ cudaError_t launch_gemm_tc(int E, int N, int K, int64_t max_rows, const int32_t*
   {
     const cuuint64_t dims[3] = {cuuint64_t(K), cuuint64_t(N), cuuint64_t(E)};
     const cuuint64_t strides[2] = {cuuint64_t(K) * 2, cuuint64_t(N) * K * 2};
-    const cuuint32_t box[3] = {kTileK, cuuint32_t(BN), 1};
+    const cuuint32_t box[3] = {kTileK, cuuint32_t(pair ? BN / 2 : BN), 1};
     const cuuint32_t es[3] = {1, 1, 1};
     if (encode(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(B), dims, strides, box,
                es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -383,37 +525,13 @@ cudaError_t launch_gemm_tc(int E, int N, int K, int64_t max_rows, const int32_t*
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  int dev = 0, sms = 148, smem_optin = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-  cudaFuncAttributes fa{};
-  cudaError_t err = cudaFuncGetAttributes(&fa, gemm_tc_kernel<kActNone>);
-  if (err != cudaSuccess) return err;
-  // As many pipeline stages as fit beside the epilogue buffers and the
-  // kernel's static shared memory.
-  const size_t stage_bytes = size_t(kTileM) * kTileK * 2 + size_t(BN) * kTileK * 2;
-  const size_t fixed = 1024 + size_t(kEpiWarps) * kEpiBufBytes;
-  const size_t budget = size_t(smem_optin) - fa.sharedSizeBytes;
-  int stages = budget > fixed ? int((budget - fixed) / stage_bytes) : 0;
-  if (stages > kMaxStages) stages = kMaxStages;
-  if (stages < 2) return cudaErrorInvalidValue;
-  const size_t smem = fixed + size_t(stages) * stage_bytes;
-  auto run = [&](auto kernel) {
-    cudaError_t err =
-        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    if (err != cudaSuccess) return err;
-    kernel<<<unsigned(sms), kThreads, smem, st>>>(tmA, tmB, E, N, K, BN, offsets, bias,
-                                                  static_cast<__nv_bfloat16*>(out), max_rows,
-                                                  status, stages);
-    return cudaGetLastError();
-  };
-  err = act == MOE_ACT_RELU        ? run(gemm_tc_kernel<MOE_ACT_RELU>)
-                    : act == MOE_ACT_GELU_TANH ? run(gemm_tc_kernel<MOE_ACT_GELU_TANH>)
-                                               : run(gemm_tc_kernel<kActNone>);
+  cudaError_t err = pair ? launch_variant<true>(act, tmA, tmB, E, N, K, BN, offsets, bias, out,
+                                                max_rows, status, st)
+                         : launch_variant<false>(act, tmA, tmB, E, N, K, BN, offsets, bias, out,
+                                                 max_rows, status, st);
   if (err != cudaSuccess) return err;
   count_launch();
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
 }  // namespace moe

@@ -13,7 +13,8 @@
 //              out-of-bounds fill)
 //   warp 1     TMEM allocator and MMA issuer: tcgen05.mma M=128, N=NP, K=16,
 //              bf16 in, fp32 accumulate, into one of two TMEM buffers
-//   warps 2-9  epilogue: one token row and half of the NP columns per thread
+//   warps 2..  epilogue, G groups of four warps (G = 2 for NP = 32, else 4):
+//              one token row and NP/G columns per thread
 //
 // Precision.  The tensor cores' fp32 accumulation over a long K chain drifts
 // (about 2e-5 relative over d = 7168, above the 1e-5 logit tolerance), so
@@ -23,9 +24,10 @@
 // small partial sums keep the logits close to the exact dot product.
 //
 // After the last segment of a tile the epilogue has the logits in registers:
-// bias, logits out, max and a sorted top-k list per half row, merged through
-// shared memory (ties go to the lower expert index: insertion into a sorted
-// list that only a strictly larger value passes, lower half first), then
+// bias, logits out, max and a sorted top-k list per column group, merged
+// pairwise through shared memory, lower columns first (ties go to the lower
+// expert index: insertion into a sorted list that only a strictly larger
+// value passes, and higher indices are always inserted later), then
 // Σ exp, weights, and the tile's column sums of p by a transposing warp
 // butterfly.  Every wait is bounded (4 s); on a timeout the kernel records
 // MOE_ERR_TIMEOUT, drains its copies and MMAs, frees its tensor memory and
@@ -41,13 +43,13 @@ namespace {
 constexpr int kTileM = kRouteTileM;  // 128 tokens per tile
 constexpr int kTileK = 64;           // one 128-byte swizzle row of bf16
 constexpr int kSegBlocks = 4;        // k-blocks per accumulation segment (K = 256)
-constexpr int kEpiWarps = 8;
-constexpr int kEpiThreads = kEpiWarps * 32;
-constexpr int kThreads = 64 + kEpiThreads;
 constexpr int kMaxStages = 8;
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
 constexpr int kMaxNP = 256;
 constexpr size_t kMinSmem = 120 * 1024;  // one CTA per SM (it may take all of TMEM)
+
+template <int G>
+constexpr int epi_threads() { return 128 * G; }
 
 struct RouteTcArgs {
   int64_t T;
@@ -61,8 +63,9 @@ struct RouteTcArgs {
   int32_t* status;
 };
 
+template <int G>
 __device__ __forceinline__ void bar_epi() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
+  asm volatile("bar.sync 1, %0;" ::"n"(epi_threads<G>()) : "memory");
 }
 
 // Insert (v, i) into a list sorted by descending value; only a strictly
@@ -82,13 +85,14 @@ __device__ __forceinline__ void topk_insert(float* tv, int* ti, float v, int i) 
   }
 }
 
-// NPH = NP / 2 columns per epilogue thread.
-template <int NPH, int KMAX>
-__global__ void __launch_bounds__(kThreads, 1)
+// NPG = NP / G columns per epilogue thread.
+template <int NPG, int G, int KMAX>
+__global__ void __launch_bounds__(64 + 128 * G, 1)
     route_tc_kernel(const __grid_constant__ CUtensorMap tmX,
                     const __grid_constant__ CUtensorMap tmW, const RouteTcArgs a) {
-  constexpr int NP = 2 * NPH;
-  constexpr int CH = (NPH < 32 || NPH >= 128) ? 16 : 32;  // columns per tensor-memory load
+  constexpr int NP = G * NPG;
+  constexpr int CH = NPG < 32 ? 16 : 32;  // columns per tensor-memory load
+  constexpr int kEpiThreads = epi_threads<G>();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages];
   __shared__ uint64_t tfull_bar[2], tempty_bar[2], drain_bar;
@@ -96,9 +100,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ int s_abort;
   __shared__ float s_bias[NP];
   __shared__ float s_red[4][NP];
-  __shared__ float s_hmax[kTileM], s_hz[kTileM], s_M[kTileM], s_invz[kTileM];
-  __shared__ float s_htv[KMAX][kTileM];
-  __shared__ int s_hti[KMAX][kTileM];
+  __shared__ float s_M[kTileM], s_invz[kTileM];
+  __shared__ float s_gz[G - 1][kTileM];
+  __shared__ float s_xmax[G / 2][kTileM];
+  __shared__ float s_xtv[G / 2][KMAX][kTileM];
+  __shared__ int s_xti[G / 2][KMAX][kTileM];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -212,20 +218,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= 2) {
     // ---------------- epilogue ----------------
     const int quarter = warp & 3;        // TMEM lanes [32·quarter, 32·quarter + 32)
-    const int h = (warp - 2) >> 2;       // column half: [h·NPH, h·NPH + NPH)
+    const int g = (warp - 2) >> 2;       // column group: [g·NPG, g·NPG + NPG)
     const int row = quarter * 32 + lane;
     const int E = a.E;
+    const int col0 = g * NPG;
     const int col_of_lane =
         ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
-    const uint32_t t_lane = tmem_base + (uint32_t(quarter * 32) << 16) + uint32_t(h * NPH);
+    const uint32_t t_lane = tmem_base + (uint32_t(quarter * 32) << 16) + uint32_t(col0);
     uint32_t seg_count = 0;
     bool ok = true;
     for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
       const int64_t t = tile * kTileM + row;
       const bool valid = t < a.T;
-      float v[NPH];
+      float v[NPG];
 #pragma unroll
-      for (int j = 0; j < NPH; ++j) v[j] = 0.f;
+      for (int j = 0; j < NPG; ++j) v[j] = 0.f;
       for (int sg = 0; sg < nseg; ++sg, ++seg_count) {
         const uint32_t buf = seg_count & 1u;
         if (ok) {
@@ -238,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) {
           tc::fence_after_sync();
 #pragma unroll
-          for (int c0 = 0; c0 < NPH; c0 += CH) {
+          for (int c0 = 0; c0 < NPG; c0 += CH) {
             uint32_t r[CH];
             if constexpr (CH == 32)
               tc::tmem_ld_x32(t_lane + buf * uint32_t(NP) + uint32_t(c0), r);
@@ -252,58 +259,67 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::mbar_arrive(&tempty_bar[buf]);
         }
       }
-      // Logits, this half's max and top-k.
-      float hmax = -INFINITY;
+      // Logits, this group's max and top-k.
+      float gmax = -INFINITY;
       float tv[KMAX];
       int ti[KMAX];
 #pragma unroll
       for (int r = 0; r < KMAX; ++r) tv[r] = -INFINITY, ti[r] = 0x7fffffff;
 #pragma unroll
-      for (int j = 0; j < NPH; ++j) {
-        const int e = h * NPH + j;
+      for (int j = 0; j < NPG; ++j) {
+        const int e = col0 + j;
         v[j] += s_bias[e];
         if (e < E) {
-          hmax = fmaxf(hmax, v[j]);
+          gmax = fmaxf(gmax, v[j]);
           topk_insert<KMAX>(tv, ti, v[j], e);
         }
       }
-      if (valid && ok && a.logits && h * NPH < E) {
-        float* lrow = a.logits + t * E + h * NPH;
-        const int ncol = min(NPH, E - h * NPH);
+      if (valid && ok && a.logits && col0 < E) {
+        float* lrow = a.logits + t * E + col0;
+        const int ncol = min(NPG, E - col0);
         if ((E & 3) == 0) {
 #pragma unroll
-          for (int j = 0; j < NPH; j += 4)
+          for (int j = 0; j < NPG; j += 4)
             if (j < ncol)
               *reinterpret_cast<float4*>(lrow + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
         } else {
 #pragma unroll
-          for (int j = 0; j < NPH; ++j)
+          for (int j = 0; j < NPG; ++j)
             if (j < ncol) lrow[j] = v[j];
         }
       }
-      // Merge the upper half into the lower half's list.
-      if (h == 1) {
-        s_hmax[row] = hmax;
+      // Pairwise merges, lower columns first: at step s, group g with
+      // g % 2s == s hands its max and list to group g - s.
 #pragma unroll
-        for (int r = 0; r < KMAX; ++r) s_htv[r][row] = tv[r], s_hti[r][row] = ti[r];
-      }
-      bar_epi();
-      if (h == 0) {
-        const float M = fmaxf(hmax, s_hmax[row]);
+      for (int st = 1; st < G; st <<= 1) {
+        if (g % (2 * st) == st) {
+          const int slot = g / (2 * st);
+          s_xmax[slot][row] = gmax;
 #pragma unroll
-        for (int r = 0; r < KMAX; ++r) topk_insert<KMAX>(tv, ti, s_htv[r][row], s_hti[r][row]);
-        s_M[row] = M;
+          for (int r = 0; r < KMAX; ++r) s_xtv[slot][r][row] = tv[r], s_xti[slot][r][row] = ti[r];
+        }
+        bar_epi<G>();
+        if (g % (2 * st) == 0) {
+          const int slot = g / (2 * st);
+          gmax = fmaxf(gmax, s_xmax[slot][row]);
+#pragma unroll
+          for (int r = 0; r < KMAX; ++r)
+            topk_insert<KMAX>(tv, ti, s_xtv[slot][r][row], s_xti[slot][r][row]);
+        }
+        bar_epi<G>();
       }
-      bar_epi();
+      if (g == 0) s_M[row] = gmax;
+      bar_epi<G>();
       const float M = s_M[row];
       float z = 0.f;
 #pragma unroll
-      for (int j = 0; j < NPH; ++j)
-        if (h * NPH + j < E) z += expf(v[j] - M);
-      if (h == 1) s_hz[row] = z;
-      bar_epi();
-      if (h == 0) {
-        z += s_hz[row];
+      for (int j = 0; j < NPG; ++j)
+        if (col0 + j < E) z += expf(v[j] - M);
+      if (g > 0) s_gz[g - 1][row] = z;
+      bar_epi<G>();
+      if (g == 0) {
+#pragma unroll
+        for (int j = 0; j < G - 1; ++j) z += s_gz[j][row];
         const float inv_z = 1.f / z;
         s_invz[row] = inv_z;
         if (valid && ok) {
@@ -320,17 +336,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
       }
-      bar_epi();
+      bar_epi<G>();
       // Column sums of p over the tile: per warp a transposing butterfly over
       // 16 columns at a time (lane L, L even, ends with column col_of_lane),
       // then the four lane quarters in order.
       const float inv_z = s_invz[row];
 #pragma unroll
-      for (int c0 = 0; c0 < NPH; c0 += 16) {
+      for (int c0 = 0; c0 < NPG; c0 += 16) {
         float p[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j)
-          p[j] = (valid && ok && h * NPH + c0 + j < E) ? expf(v[c0 + j] - M) * inv_z : 0.f;
+          p[j] = (valid && ok && col0 + c0 + j < E) ? expf(v[c0 + j] - M) * inv_z : 0.f;
 #pragma unroll
         for (int half = 8, o = 16; half >= 1; half >>= 1, o >>= 1) {
           const bool upper = (lane & o) != 0;
@@ -342,9 +358,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         p[0] += __shfl_xor_sync(0xffffffffu, p[0], 1);
-        if ((lane & 1) == 0) s_red[quarter][h * NPH + c0 + col_of_lane] = p[0];
+        if ((lane & 1) == 0) s_red[quarter][col0 + c0 + col_of_lane] = p[0];
       }
-      bar_epi();
+      bar_epi<G>();
       for (int e = threadIdx.x - 64; e < E; e += kEpiThreads)
         a.psum_partial[tile * E + e] = ((s_red[0][e] + s_red[1][e]) + s_red[2][e]) + s_red[3][e];
     }
@@ -388,24 +404,39 @@ bool encode_2d(EncodeTiledFn encode, CUtensorMap* m, const void* base, int64_t i
          CUDA_SUCCESS;
 }
 
-template <int NPH, int KMAX>
-cudaError_t launch_k(const CUtensorMap& tmX, const CUtensorMap& tmW, const RouteTcArgs& a,
-                     size_t smem, unsigned grid, cudaStream_t st) {
-  cudaError_t err = cudaFuncSetAttribute(route_tc_kernel<NPH, KMAX>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+template <int NPG, int G, int KMAX>
+cudaError_t launch_k(const CUtensorMap& tmX, const CUtensorMap& tmW, RouteTcArgs a,
+                     unsigned grid, cudaStream_t st) {
+  auto kernel = route_tc_kernel<NPG, G, KMAX>;
+  int dev = 0, smem_optin = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  cudaFuncAttributes fa{};
+  cudaError_t err = cudaFuncGetAttributes(&fa, kernel);
   if (err != cudaSuccess) return err;
-  route_tc_kernel<NPH, KMAX><<<grid, kThreads, smem, st>>>(tmX, tmW, a);
+  // As many stages as fit beside the kernel's static shared memory.
+  const size_t stage_bytes = size_t(kTileM) * kTileK * 2 + size_t(G * NPG) * kTileK * 2;
+  const size_t budget = size_t(smem_optin) - fa.sharedSizeBytes - 1024;
+  int stages = int(budget / stage_bytes);
+  if (stages > kMaxStages) stages = kMaxStages;
+  if (stages < 2) return cudaErrorInvalidValue;
+  a.stages = stages;
+  size_t smem = 1024 + size_t(stages) * stage_bytes;
+  if (smem < kMinSmem) smem = kMinSmem;
+  err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (err != cudaSuccess) return err;
+  kernel<<<grid, 64 + 128 * G, smem, st>>>(tmX, tmW, a);
   return cudaGetLastError();
 }
 
-template <int NPH>
+template <int NPG, int G>
 cudaError_t launch_np(int k, const CUtensorMap& tmX, const CUtensorMap& tmW,
-                      const RouteTcArgs& a, size_t smem, unsigned grid, cudaStream_t st) {
-  if (k <= 1) return launch_k<NPH, 1>(tmX, tmW, a, smem, grid, st);
-  if (k <= 2) return launch_k<NPH, 2>(tmX, tmW, a, smem, grid, st);
-  if (k <= 4) return launch_k<NPH, 4>(tmX, tmW, a, smem, grid, st);
-  if (k <= 8) return launch_k<NPH, 8>(tmX, tmW, a, smem, grid, st);
-  return launch_k<NPH, 16>(tmX, tmW, a, smem, grid, st);
+                      const RouteTcArgs& a, unsigned grid, cudaStream_t st) {
+  if (k <= 1) return launch_k<NPG, G, 1>(tmX, tmW, a, grid, st);
+  if (k <= 2) return launch_k<NPG, G, 2>(tmX, tmW, a, grid, st);
+  if (k <= 4) return launch_k<NPG, G, 4>(tmX, tmW, a, grid, st);
+  if (k <= 8) return launch_k<NPG, G, 8>(tmX, tmW, a, grid, st);
+  return launch_k<NPG, G, 16>(tmX, tmW, a, grid, st);
 }
 
 }  // namespace
@@ -430,10 +461,6 @@ cudaError_t launch_route_tc(const moe_config_t& c, const void* x, const void* Wr
   a.k = c.k;
   a.renorm = c.renormalize;
   a.tmem_cols = uint32_t(2 * NP);  // two accumulator buffers
-  const size_t stage_bytes = size_t(kTileM) * kTileK * 2 + size_t(NP) * kTileK * 2;
-  int stages = int((192 * 1024) / stage_bytes);
-  if (stages > kMaxStages) stages = kMaxStages;
-  a.stages = stages;
   a.br = br;
   a.logits = logits;
   a.ids = ids;
@@ -444,8 +471,6 @@ cudaError_t launch_route_tc(const moe_config_t& c, const void* x, const void* Wr
   CUtensorMap tmX, tmW;
   if (!encode_2d(encode, &tmX, x, c.d, c.T, kTileK, kTileM)) return cudaErrorInvalidValue;
   if (!encode_2d(encode, &tmW, Wr, c.d, c.E, kTileK, uint32_t(NP))) return cudaErrorInvalidValue;
-  size_t smem = 1024 + size_t(stages) * stage_bytes;
-  if (smem < kMinSmem) smem = kMinSmem;
   const int64_t n_tiles = (c.T + kTileM - 1) / kTileM;
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
@@ -453,10 +478,10 @@ cudaError_t launch_route_tc(const moe_config_t& c, const void* x, const void* Wr
   const unsigned grid = unsigned(n_tiles < sms ? n_tiles : sms);
   cudaError_t err;
   switch (NP) {
-    case 32: err = launch_np<16>(c.k, tmX, tmW, a, smem, grid, st); break;
-    case 64: err = launch_np<32>(c.k, tmX, tmW, a, smem, grid, st); break;
-    case 128: err = launch_np<64>(c.k, tmX, tmW, a, smem, grid, st); break;
-    default: err = launch_np<128>(c.k, tmX, tmW, a, smem, grid, st); break;
+    case 32: err = launch_np<16, 2>(c.k, tmX, tmW, a, grid, st); break;
+    case 64: err = launch_np<16, 4>(c.k, tmX, tmW, a, grid, st); break;
+    case 128: err = launch_np<32, 4>(c.k, tmX, tmW, a, grid, st); break;
+    default: err = launch_np<64, 4>(c.k, tmX, tmW, a, grid, st); break;
   }
   count_launch();
   if (err != cudaSuccess) return err;

@@ -94,3 +94,21 @@ def test_tensor_core_gemm_matches_cuda_core_gemm():
     assert ((a - b).abs() <= 1e-2 + 2e-2 * b.abs()).all()
     ha, hb = out_tc["H"][:n].float(), out_s["H"][:n].float()
     assert ((ha - hb).abs() <= 1e-2 + 2e-2 * hb.abs()).all()
+
+
+def test_two_sm_gemm_matches_one_sm_gemm():
+    # Default: CTA pairs with the 2-SM MMA (M = 256); MOE_GEMM_PAIR=0 runs the
+    # 1-SM kernel (M = 128).  Ragged experts with odd 128-row tile counts
+    # exercise the pair's empty upper half.
+    wl = W["bf16_t8192_d2048_e64_top6"].replace(T=3000)
+    _, inp, out_p, _ = run_gpu(wl, expert_bias=True)
+    os.environ["MOE_GEMM_PAIR"] = "0"
+    try:
+        _, _, out_1, _ = run_gpu(wl, inp=inp)
+    finally:
+        del os.environ["MOE_GEMM_PAIR"]
+    n = int(h(out_p["offsets"])[-1])
+    for name in ["H", "yd"]:
+        a = out_p[name][:n].float()
+        b = out_1[name][:n].float()
+        assert ((a - b).abs() <= 1e-2 + 2e-2 * b.abs()).all(), name
