@@ -5,9 +5,12 @@
 
 One step = one forward pass of the whole layer (route, dispatch, grouped
 expert FFN, combine, aux statistics) over one batch of T synthetic tokens,
-inputs already resident in HBM.  Each step is timed with CUDA events on the
-launching stream, with the L2 cache flushed between steps (a 512 MiB write,
-outside the events).  Rank 0 prints one JSON line.
+inputs already resident in HBM.  The pass (one moe_forward call) is captured
+once into a CUDA graph and each step replays it, timed with CUDA events on
+the stream, with the L2 cache flushed between steps (a 512 MiB write, outside
+the events).  Per-stage times come from one graph per stage, replayed the
+same way; the eager time of moe_forward launched from Python is reported
+beside them.  Rank 0 prints one JSON line.
 
 Multi-GPU: the layer does not shard in this design (replicas only), so under
 torchrun every rank runs an independent replica on its own batch and
@@ -216,6 +219,15 @@ def run_reference(args, wl, rank, world):
 
 # ------------------------------------------------------------- GPU bench ----
 
+def capture(fn):
+    """Capture the launches of fn() into a CUDA graph (on torch's capture
+    stream, which the library calls pick up as the current stream)."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    return g
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -264,28 +276,77 @@ def main():
         moe.forward_stages(cfg, inp, out, ws, args.alpha, stream)
     torch.cuda.synchronize(dev)
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize(dev)
+    # The forward pass is captured once into a CUDA graph (every library call
+    # only enqueues kernels), as a serving loop would run it; each timed step
+    # replays it.  Per-stage times come from one graph per stage.
     launches0 = moe.launch_count()
-    with ClockSampler(local_rank) as clocks:
-        for s in range(args.steps):
-            flush.zero_()  # evict L2 between steps (outside the timed events)
-            moe.forward_stages(cfg, inp, out, ws, args.alpha, stream, events=evs[s])
-        torch.cuda.synchronize(dev)
-    launches = moe.launch_count() - launches0
+    g_full = capture(lambda: moe.forward(cfg, inp, out, ws, args.alpha))
+    per_forward = moe.launch_count() - launches0
+    stage_calls = {
+        "route": lambda: moe.route(cfg, inp["x"], inp["Wr"], inp["br"], out, ws),
+        "dispatch": lambda: moe.dispatch(cfg, inp["x"], out["topk_ids"], out, ws),
+        "ffn_up": lambda: moe.ffn_up(cfg, out["xd"], out["offsets"], inp["W1"], inp["b1"],
+                                     out["H"], ws),
+        "ffn_down": lambda: moe.ffn_down(cfg, out["H"], out["offsets"], inp["W2"], inp["b2"],
+                                         out["yd"], ws),
+        "combine": lambda: moe.combine(cfg, out["yd"], out["slot_row"], out["topk_w"], out["y"]),
+        "aux": lambda: moe.aux_stats(cfg, out["counts"], out["psum"], args.alpha, out["f"],
+                                     out["pbar"], out["l_aux"]),
+    }
+    g_stage = {name: capture(fn) for name, fn in stage_calls.items()}
+    for _ in range(2):
+        g_full.replay()
+        for name in STAGES:
+            g_stage[name].replay()
+    torch.cuda.synchronize(dev)
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+
+    K = args.steps
+    evs = [(ev(), ev()) for _ in range(K)]
+    sevs = [[ev() for _ in range(7)] for _ in range(K)]
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize(dev)
+    with ClockSampler(local_rank) as clocks:
+        for s_ in range(K):
+            flush.zero_()  # evict L2 between steps (outside the timed events)
+            evs[s_][0].record(stream)
+            g_full.replay()
+            evs[s_][1].record(stream)
+        torch.cuda.synchronize(dev)
+    launches = K * per_forward
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    # Stage breakdown: the same steps, one graph per stage.
+    for s_ in range(K):
+        flush.zero_()
+        for i, name in enumerate(STAGES):
+            sevs[s_][i].record(stream)
+            g_stage[name].replay()
+        sevs[s_][6].record(stream)
+    torch.cuda.synchronize(dev)
+    # Eager reference: moe_forward launched from Python each step.
+    eager_ms = 0.0
+    for s_ in range(K):
+        flush.zero_()
+        a, b = ev(), ev()
+        a.record(stream)
+        moe.forward(cfg, inp, out, ws, args.alpha, stream)
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        eager_ms += a.elapsed_time(b)
+    eager_ms /= K
     assert moe.device_status(ws) == moe.MOE_OK
 
     stage_ms = {name: 0.0 for name in STAGES}
     total_ms = 0.0
-    for e in evs:
-        total_ms += e[0].elapsed_time(e[6])
+    for s_ in range(K):
+        total_ms += evs[s_][0].elapsed_time(evs[s_][1])
         for i, name in enumerate(STAGES):
-            stage_ms[name] += e[i].elapsed_time(e[i + 1])
+            stage_ms[name] += sevs[s_][i].elapsed_time(sevs[s_][i + 1])
     t = torch.tensor([total_ms], dtype=torch.float64)
     if dist is not None:
         t = t.to(dev)
@@ -297,7 +358,6 @@ def main():
     slot = out["slot_row"].cpu()
     t_kept = int((slot >= 0).any(dim=1).sum())
     alg = algorithmic(wl, n_kept, t_kept)
-    K = args.steps
     peaks = load_peaks()
     mean = {k: v / K for k, v in stage_ms.items()}
     ffn_ms = mean["ffn_up"] + mean["ffn_down"]
@@ -365,6 +425,9 @@ def main():
                  h2d_bytes_per_step=wl.T * wl.d * b, d2h_bytes_per_step=wl.T * wl.d * b + 4),
         gpu_launches=launches,
         clocks=clocks.summary(),
+        timing="forward captured once as a CUDA graph, replayed per step; stages_ms from "
+               "one graph per stage; eager_ms_per_step = moe_forward launched from Python",
+        eager_ms_per_step=eager_ms,
         stages_ms={k: round(v, 5) for k, v in mean.items()},
         ffn_tflops=alg["ffn_up_flops"] * 2 / (ffn_ms * 1e-3) / 1e12,
         ffn_tc_frac=alg["ffn_up_flops"] * 2 / (ffn_ms * 1e-3) / 1e12 / peaks["bf16"],

@@ -116,12 +116,16 @@ int64_t moe_capacity(const moe_config_t* cfg);
 /* Rows of the dispatch buffer to allocate: min(T·k, E·C).  -1 if invalid. */
 int64_t moe_max_rows(const moe_config_t* cfg);
 
-/* Bytes of scratch workspace the stage calls need (status word, per-chunk
- * histograms, per-tile probability partial sums).  Host only. */
+/* Bytes of scratch workspace the stage calls need (1 KiB header with the
+ * status word and completion counters, per-chunk histograms, per-block
+ * probability partial sums, and for small T the router's per-split partial
+ * logits).  Host only.  A workspace serves one stream at a time. */
 moe_status_t moe_workspace_size(const moe_config_t* cfg, size_t* bytes);
 
-/* Clear the workspace's device status word (enqueued on stream).  Call once
- * after allocating a workspace, and after reading a nonzero status. */
+/* Clear the workspace's 1 KiB header: the device status word and the
+ * counters the kernels use to find the last block of a grid (enqueued on
+ * stream; kernels leave the counters at zero).  Call once after allocating a
+ * workspace, and after reading a nonzero status. */
 moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, void* stream);
 
 /* [MoE 模型原理 §2.1–§2.2] Router: logits s = x W_rᵀ + b_r (fp32 accumulate),

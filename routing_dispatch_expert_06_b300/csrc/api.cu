@@ -2,6 +2,9 @@
 // kernel launches for each stage.  See include/moe.h for the contract.
 #include <atomic>
 #include <cmath>
+#include <map>
+#include <mutex>
+#include <tuple>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -23,6 +26,79 @@ static moe_status_t fail(moe_status_t code, const std::string& msg) {
 }
 
 moe_status_t report_error(moe_status_t code, const char* msg) { return fail(code, msg); }
+
+namespace {
+constexpr int kMaxDev = 64;
+std::mutex g_cache_mu;
+int g_sms[kMaxDev] = {};
+int g_smem_optin[kMaxDev] = {};
+std::map<const void*, size_t> g_static_smem;
+std::map<std::pair<int, const void*>, size_t> g_dyn_smem;
+std::map<std::tuple<int, const void*, size_t, unsigned>, int> g_clusters;
+
+int current_device() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  return dev < 0 || dev >= kMaxDev ? 0 : dev;
+}
+}  // namespace
+
+int device_sms() {
+  const int dev = current_device();
+  std::lock_guard<std::mutex> lock(g_cache_mu);
+  if (!g_sms[dev] && cudaDeviceGetAttribute(&g_sms[dev], cudaDevAttrMultiProcessorCount, dev) !=
+                         cudaSuccess)
+    g_sms[dev] = 0;
+  return g_sms[dev] > 0 ? g_sms[dev] : 148;
+}
+
+int device_smem_optin() {
+  const int dev = current_device();
+  std::lock_guard<std::mutex> lock(g_cache_mu);
+  if (!g_smem_optin[dev] &&
+      cudaDeviceGetAttribute(&g_smem_optin[dev], cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+          cudaSuccess)
+    g_smem_optin[dev] = 0;
+  return g_smem_optin[dev];
+}
+
+size_t kernel_static_smem(const void* kernel) {
+  std::lock_guard<std::mutex> lock(g_cache_mu);
+  auto it = g_static_smem.find(kernel);
+  if (it != g_static_smem.end()) return it->second;
+  cudaFuncAttributes fa{};
+  const size_t v = cudaFuncGetAttributes(&fa, kernel) == cudaSuccess ? fa.sharedSizeBytes : 0;
+  g_static_smem[kernel] = v;
+  return v;
+}
+
+cudaError_t ensure_dynamic_smem(const void* kernel, size_t bytes) {
+  const int dev = current_device();
+  std::lock_guard<std::mutex> lock(g_cache_mu);
+  size_t& have = g_dyn_smem[{dev, kernel}];
+  if (have >= bytes) return cudaSuccess;
+  cudaError_t e =
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes));
+  if (e == cudaSuccess) have = bytes;
+  return e;
+}
+
+cudaError_t max_active_clusters(const void* kernel, const cudaLaunchConfig_t& cfg, int* clusters) {
+  const int dev = current_device();
+  unsigned csize = 1;
+  for (unsigned i = 0; i < cfg.numAttrs; ++i)
+    if (cfg.attrs[i].id == cudaLaunchAttributeClusterDimension) csize = cfg.attrs[i].val.clusterDim.x;
+  std::lock_guard<std::mutex> lock(g_cache_mu);
+  const auto key = std::make_tuple(dev, kernel, cfg.dynamicSmemBytes, csize);
+  auto it = g_clusters.find(key);
+  if (it != g_clusters.end()) {
+    *clusters = it->second;
+    return cudaSuccess;
+  }
+  cudaError_t e = cudaOccupancyMaxActiveClusters(clusters, kernel, &cfg);
+  if (e == cudaSuccess) g_clusters[key] = *clusters;
+  return e;
+}
 
 static moe_status_t cuda_fail(cudaError_t e, const char* where) {
   return fail(MOE_ERR_CUDA, std::string(where) + ": " + cudaGetErrorString(e));
@@ -77,19 +153,28 @@ static WsLayout layout_of(const moe_config_t& c) {
   L.n_route_blocks = rb_simt > rb_tc ? rb_simt : rb_tc;
   size_t off = 0;
   L.status = off;
-  off += 256;
+  L.split_count = off + kWsSplitCounters;
+  off += kWsHeaderBytes;
   L.chunk_counts = off;
   off += align256(size_t(L.n_chunks) * c.E * sizeof(int32_t));
   L.psum_partial = off;
   off += align256(size_t(L.n_route_blocks) * c.E * sizeof(float));
+  L.split_part = off;
+  if (route_tc_supported(c) && route_tc_nsplit(c) > 1)
+    off += align256(size_t(rb_tc) * route_tc_nsplit(c) * route_tc_np(c) * kRouteTileM *
+                    sizeof(float));
   L.total = off;
   return L;
 }
 
 struct Ws {
   int32_t* status;
+  int* route_counter;     // grid-completion counters (inside the status block)
+  int* dispatch_counter;
   int32_t* chunk_counts;
   float* psum_partial;
+  float* split_part;
+  int* split_count;
 };
 
 static moe_status_t get_ws(const moe_config_t& c, void* ws, size_t ws_bytes, Ws* out) {
@@ -101,8 +186,12 @@ static moe_status_t get_ws(const moe_config_t& c, void* ws, size_t ws_bytes, Ws*
     return fail(MOE_ERR_WORKSPACE, "workspace smaller than moe_workspace_size()");
   char* b = static_cast<char*>(ws);
   out->status = reinterpret_cast<int32_t*>(b + L.status);
+  out->route_counter = reinterpret_cast<int*>(b + L.status + kWsRouteCounter);
+  out->dispatch_counter = reinterpret_cast<int*>(b + L.status + kWsDispatchCounter);
   out->chunk_counts = reinterpret_cast<int32_t*>(b + L.chunk_counts);
   out->psum_partial = reinterpret_cast<float*>(b + L.psum_partial);
+  out->split_part = reinterpret_cast<float*>(b + L.split_part);
+  out->split_count = reinterpret_cast<int*>(b + L.split_count);
   return MOE_OK;
 }
 
@@ -116,13 +205,21 @@ static bool use_tc_gemm(const moe_config_t& c) {
   return !(v && std::strcmp(v, "simt") == 0);
 }
 
-// Which router runs: the tcgen05 kernel for bf16 layers with E <= 256, else
-// the CUDA-core kernel; MOE_ROUTE_IMPL=simt selects the CUDA-core kernel
-// (a cross-check in tests).
-static bool use_tc_router(const moe_config_t& c) {
-  if (!route_tc_supported(c)) return false;
+// Which router runs.  bf16 layers: the tcgen05 router for E <= 256, else the
+// generic CUDA-core router; fp32 layers: the generic CUDA-core router (tf32
+// tensor cores would not meet an fp32 tolerance).  MOE_ROUTE_IMPL=simt|warp|tc
+// forces one where it applies (the warp router, bf16 with E <= 32, is a
+// cross-check: it measured slower than the tcgen05 router on these shapes).  Inputs that are not 16-byte aligned take the generic router.
+enum class Router { kSimt, kWarp, kTc };
+static Router pick_router(const moe_config_t& c, bool aligned) {
+  // The warp and tcgen05 routers read x and W_r in 16-byte units.
+  if (!aligned) return Router::kSimt;
   const char* v = std::getenv("MOE_ROUTE_IMPL");
-  return !(v && std::strcmp(v, "simt") == 0);
+  if (v && std::strcmp(v, "simt") == 0) return Router::kSimt;
+  if (v && std::strcmp(v, "tc") == 0 && route_tc_supported(c)) return Router::kTc;
+  if (v && std::strcmp(v, "warp") == 0 && route_warp_supported(c)) return Router::kWarp;
+  if (route_tc_supported(c)) return Router::kTc;
+  return Router::kSimt;
 }
 
 }  // namespace moe
@@ -152,8 +249,8 @@ moe_status_t moe_workspace_size(const moe_config_t* cfg, size_t* bytes) {
 }
 
 moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, void* stream) {
-  if (!ws || ws_bytes < 256) return fail(MOE_ERR_INVALID_ARG, "workspace too small");
-  cudaError_t e = cudaMemsetAsync(ws, 0, 256, static_cast<cudaStream_t>(stream));
+  if (!ws || ws_bytes < kWsHeaderBytes) return fail(MOE_ERR_INVALID_ARG, "workspace too small");
+  cudaError_t e = cudaMemsetAsync(ws, 0, kWsHeaderBytes, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_workspace_init");
 }
 
@@ -170,10 +267,22 @@ moe_status_t moe_route(const moe_config_t* cfg, const void* x, const void* Wr, c
   if ((s = get_ws(*cfg, ws, ws_bytes, &w)) != MOE_OK) return s;
   float* lg = cfg->write_logits ? logits : nullptr;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = use_tc_router(*cfg) ? launch_route_tc(*cfg, x, Wr, br, lg, topk_ids, topk_w,
-                                                        w.psum_partial, psum, w.status, st)
-                                      : launch_route_simt(*cfg, x, Wr, br, lg, topk_ids, topk_w,
-                                                          w.psum_partial, psum, st);
+  int* counter = w.route_counter;
+  cudaError_t e;
+  switch (pick_router(*cfg, aligned16(x) && aligned16(Wr))) {
+    case Router::kWarp:
+      e = launch_route_warp(*cfg, x, Wr, br, lg, topk_ids, topk_w, w.psum_partial, psum, counter,
+                            st);
+      break;
+    case Router::kTc:
+      e = launch_route_tc(*cfg, x, Wr, br, lg, topk_ids, topk_w, w.psum_partial, psum, counter,
+                          w.status, w.split_part, w.split_count, st);
+      break;
+    default:
+      e = launch_route_simt(*cfg, x, Wr, br, lg, topk_ids, topk_w, w.psum_partial, psum, counter,
+                            st);
+      break;
+  }
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_route");
 }
 
@@ -190,7 +299,7 @@ moe_status_t moe_dispatch(const moe_config_t* cfg, const void* x, const int32_t*
   if ((s = get_ws(*cfg, ws, ws_bytes, &w)) != MOE_OK) return s;
   const int64_t C = capacity_of(cfg->T, cfg->k, cfg->E, cfg->capacity_factor);
   cudaError_t e = launch_dispatch(*cfg, C, x, topk_ids, counts, kept, offsets, slot_row,
-                                  row_token, xd, w.chunk_counts, w.status,
+                                  row_token, xd, w.chunk_counts, w.status, w.dispatch_counter,
                                   static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_dispatch");
 }

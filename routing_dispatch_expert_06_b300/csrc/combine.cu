@@ -132,9 +132,7 @@ cudaError_t launch_combine(const moe_config_t& c, int64_t max_rows, const void* 
                            const int32_t* slot_row, const float* w, void* y, cudaStream_t st) {
   const int elem = c.dtype == MOE_DT_BF16 ? 2 : 4;
   const int64_t row_vecs = int64_t(c.d) * elem / 16;
-  int dev = 0, sms = 148;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int sms = device_sms();
   const int64_t want = (c.T + 7) / 8;
   const unsigned grid = unsigned(want < int64_t(sms) * 8 ? want : int64_t(sms) * 8);
   auto run = [&](auto kernel) {

@@ -15,16 +15,60 @@ constexpr int kChunkTokens = 256;
 constexpr int kRouteTokensSimt = 64;
 // Rows per router tile in the tensor-core router.
 constexpr int kRouteTileM = 128;
+// Target count of (tile, split) work units of the tensor-core router.
+constexpr int64_t kRouteSplitUnits = 148;
+// Largest W_r (bytes) the warp router stages in shared memory.
+constexpr size_t kRouteWarpSmemMax = 96 * 1024;
 
 // Workspace layout (byte offsets), all 256-byte aligned.
 struct WsLayout {
   size_t status;        // int32 status word
   size_t chunk_counts;  // int32 [n_chunks, E]: histogram, then chunk bases in place
   size_t psum_partial;  // fp32 [n_route_blocks, E]
+  size_t split_part;    // fp32 [n_tiles, nsplit, NP, 128] (tensor-core router, nsplit > 1)
+  size_t split_count;   // int32 [n_tiles], zeroed
   size_t total;
   int64_t n_chunks;
   int64_t n_route_blocks;
 };
+
+// The workspace starts with a 1 KiB header that moe_workspace_init clears:
+// the status word, grid-completion counters, and the per-tile arrival
+// counters of the split router (every kernel leaves them at zero).
+constexpr size_t kWsHeaderBytes = 1024;
+constexpr size_t kWsRouteCounter = 64;
+constexpr size_t kWsDispatchCounter = 128;
+constexpr size_t kWsSplitCounters = 256;  // int32 [n_tiles] for n_tiles <= 192
+
+// Called by every thread of every block once its results are written.
+// Returns true in exactly one block, the last to arrive, after which that
+// block sees every other block's global writes.  The counter returns to 0,
+// ready for the next launch.
+__device__ __forceinline__ bool last_block_to_finish(int* counter, int* s_flag) {
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int prev = atomicAdd(counter, 1);
+    const bool last = prev == int(gridDim.x) - 1;
+    if (last) atomicExch(counter, 0);
+    *s_flag = last;
+  }
+  __syncthreads();
+  const bool last = *s_flag != 0;
+  if (last) __threadfence();
+  return last;
+}
+
+// psum[i] = Σ_b part[b][i] for b = 0, 1, ..., nblk-1 in that order (fixed,
+// deterministic); threads of one block stride over i.
+__device__ __forceinline__ void sum_partials_rows(int64_t nblk, int E, const float* part,
+                                                  float* psum) {
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    float s = 0.f;
+    for (int64_t b = 0; b < nblk; ++b) s += __ldcg(part + b * E + e);
+    psum[e] = s;
+  }
+}
 
 // Record the first asynchronous error in the status word.
 __device__ __forceinline__ void set_status(int32_t* status, int32_t code) {

@@ -11,10 +11,12 @@
 // Position of slot (t, r) routed to expert e = number of earlier tokens t' < t
 // that also routed to e (a token selects each expert at most once, so the
 // (token, rank) order within an expert is plain token order).  It is built in
-// three integer passes and never materialises a T×E one-hot mask:
+// integer passes and never materialises a T×E one-hot mask:
 //   1. histogram per chunk of 256 tokens         chunk_counts[chunk][e]
 //   2. per-expert exclusive scan over chunks     chunk_counts -> chunk bases,
-//      counts[e], kept[e] = min(counts[e], C)
+//      counts[e], kept[e] = min(counts[e], C) — done by the last histogram
+//      block to finish when a completion counter is given, else by a
+//      separate kernel
 //   3. per chunk: expert offsets (scan of kept), per-warp bases, then each
 //      warp walks its 32 tokens in order: slot_row, row_token
 // and a fourth, bandwidth-bound pass copies each token row once from x and
@@ -27,10 +29,43 @@ namespace moe {
 constexpr int kDispatchThreads = 256;  // 8 warps × 32 tokens = one chunk
 static_assert(kDispatchThreads == kChunkTokens, "one token per thread in a chunk");
 
+// Per-expert exclusive scan over the chunk histograms (in place), the total
+// count and kept = min(count, C); threads of one block stride over experts.
+// Each expert's chunks are read eight at a time so the loads overlap.
+__device__ void scan_chunks_by_expert(int64_t n_chunks, int E, int64_t C,
+                                      int32_t* __restrict__ chunk_counts,
+                                      int32_t* __restrict__ counts, int32_t* __restrict__ kept) {
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int32_t run = 0;
+    int64_t ch = 0;
+    for (; ch + 8 <= n_chunks; ch += 8) {
+      int32_t v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = __ldcg(chunk_counts + (ch + u) * E + e);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        chunk_counts[(ch + u) * E + e] = run;
+        run += v[u];
+      }
+    }
+    for (; ch < n_chunks; ++ch) {
+      const int32_t v = __ldcg(chunk_counts + ch * E + e);
+      chunk_counts[ch * E + e] = run;
+      run += v;
+    }
+    counts[e] = run;
+    kept[e] = int32_t(run < C ? run : C);
+  }
+}
+
+// Histogram of one chunk; with a completion counter, the last block to
+// finish also runs the per-expert scan.
 __global__ void __launch_bounds__(kDispatchThreads)
     histogram_kernel(int64_t T, int E, int k, const int32_t* __restrict__ ids,
-                     int32_t* __restrict__ chunk_counts, int32_t* status) {
+                     int32_t* __restrict__ chunk_counts, int32_t* status, int* counter,
+                     int64_t C, int32_t* __restrict__ counts, int32_t* __restrict__ kept) {
   extern __shared__ int32_t hist[];
+  __shared__ int s_last;
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
   const int64_t t = int64_t(blockIdx.x) * kChunkTokens + threadIdx.x;
@@ -46,6 +81,8 @@ __global__ void __launch_bounds__(kDispatchThreads)
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x)
     chunk_counts[int64_t(blockIdx.x) * E + e] = hist[e];
+  if (counter && last_block_to_finish(counter, &s_last))
+    scan_chunks_by_expert(gridDim.x, E, C, chunk_counts, counts, kept);
 }
 
 // One CTA per expert: exclusive scan of that expert's chunk counts (in place),
@@ -84,17 +121,25 @@ __global__ void __launch_bounds__(256)
 }
 
 // One CTA per chunk of 256 tokens; warp w owns tokens [32w, 32w+32) of it.
-// Dynamic shared memory: off[E+1] | wbase[8][E].
+// Dynamic shared memory: off[E+1] | wbase[8][E] | the chunk's ids [256·k].
 __global__ void __launch_bounds__(kDispatchThreads)
     assign_kernel(int64_t T, int E, int k, int64_t C, const int32_t* __restrict__ ids,
                   const int32_t* __restrict__ chunk_base, const int32_t* __restrict__ kept,
                   int32_t* __restrict__ offsets, int32_t* __restrict__ slot_row,
                   int32_t* __restrict__ row_token) {
   extern __shared__ int32_t sm[];
-  int32_t* off = sm;              // [E+1]
-  int32_t* wbase = sm + E + 1;    // [8][E]
+  int32_t* off = sm;                       // [E+1]
+  int32_t* wbase = sm + E + 1;             // [8][E]
+  int32_t* s_ids = wbase + 8 * E;          // [256·k]
   __shared__ int32_t part[kDispatchThreads];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t chunk0 = int64_t(blockIdx.x) * kChunkTokens;
+  {
+    // The chunk's ids, coalesced, once.
+    const int64_t n_ids = (T - chunk0 < kChunkTokens ? T - chunk0 : kChunkTokens) * k;
+    const int32_t* src = ids + chunk0 * k;
+    for (int i = tid; i < n_ids; i += kDispatchThreads) s_ids[i] = src[i];
+  }
 
   // Expert offsets: exclusive scan of kept[0..E).  Thread i sums a run of
   // consecutive experts, then a scan over the 256 run totals.
@@ -127,11 +172,10 @@ __global__ void __launch_bounds__(kDispatchThreads)
     for (int e = tid; e <= E; e += kDispatchThreads) offsets[e] = off[e];
 
   // Per-warp histograms of this chunk.
-  const int64_t chunk0 = int64_t(blockIdx.x) * kChunkTokens;
   const int64_t t_own = chunk0 + tid;
   if (t_own < T)
     for (int r = 0; r < k; ++r) {
-      const int e = ids[t_own * k + r];
+      const int e = s_ids[tid * k + r];
       if (e >= 0 && e < E) atomicAdd(&wbase[warp * E + e], 1);
     }
   __syncthreads();
@@ -151,7 +195,7 @@ __global__ void __launch_bounds__(kDispatchThreads)
     const int64_t t = chunk0 + warp * 32 + j;
     if (t >= T) break;
     if (lane < k) {
-      const int e = ids[t * k + lane];
+      const int e = s_ids[(warp * 32 + j) * k + lane];
       int32_t row = -1;
       if (e >= 0 && e < E) {
         const int32_t pos = my[e]++;
@@ -205,19 +249,22 @@ __global__ void __launch_bounds__(256)
 cudaError_t launch_dispatch(const moe_config_t& c, int64_t C, const void* x,
                             const int32_t* ids, int32_t* counts, int32_t* kept,
                             int32_t* offsets, int32_t* slot_row, int32_t* row_token, void* xd,
-                            int32_t* chunk_counts, int32_t* status, cudaStream_t st) {
+                            int32_t* chunk_counts, int32_t* status, int* counter,
+                            cudaStream_t st) {
   const int64_t n_chunks = (c.T + kChunkTokens - 1) / kChunkTokens;
   cudaError_t err;
   histogram_kernel<<<unsigned(n_chunks), kDispatchThreads, size_t(c.E) * 4, st>>>(
-      c.T, c.E, c.k, ids, chunk_counts, status);
+      c.T, c.E, c.k, ids, chunk_counts, status, counter, C, counts, kept);
   count_launch();
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  expert_scan_kernel<<<unsigned(c.E), 256, 0, st>>>(n_chunks, c.E, C, chunk_counts, counts, kept);
-  count_launch();
-  if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  const size_t smem = size_t(c.E + 1 + 8 * c.E) * 4;
-  err = cudaFuncSetAttribute(assign_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(smem));
+  if (!counter) {
+    expert_scan_kernel<<<unsigned(c.E), 256, 0, st>>>(n_chunks, c.E, C, chunk_counts, counts,
+                                                       kept);
+    count_launch();
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  }
+  const size_t smem = size_t(c.E + 1 + 8 * c.E + kChunkTokens * c.k) * 4;
+  err = ensure_dynamic_smem(reinterpret_cast<const void*>(assign_kernel), smem);
   if (err != cudaSuccess) return err;
   assign_kernel<<<unsigned(n_chunks), kDispatchThreads, smem, st>>>(
       c.T, c.E, c.k, C, ids, chunk_counts, kept, offsets, slot_row, row_token);
@@ -225,9 +272,7 @@ cudaError_t launch_dispatch(const moe_config_t& c, int64_t C, const void* x,
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   const int elem = c.dtype == MOE_DT_BF16 ? 2 : 4;
   const int64_t row_vecs = int64_t(c.d) * elem / 16;
-  int dev = 0, sms = 148;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int sms = device_sms();
   const int64_t want = (c.T + 7) / 8;
   const unsigned grid = unsigned(want < int64_t(sms) * 8 ? want : int64_t(sms) * 8);
   scatter_rows_kernel<<<grid, 256, 0, st>>>(c.T, c.k, row_vecs, static_cast<const uint4*>(x),

@@ -439,26 +439,21 @@ template <bool PAIR>
 cudaError_t launch_variant(int act, const CUtensorMap& tmA, const CUtensorMap& tmB, int E, int N,
                            int K, int BN, const int32_t* offsets, const float* bias, void* out,
                            int64_t max_rows, int32_t* status, cudaStream_t st) {
-  int dev = 0, sms = 148, smem_optin = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-  cudaFuncAttributes fa{};
-  cudaError_t err = cudaFuncGetAttributes(&fa, gemm_tc_kernel<kActNone, PAIR>);
-  if (err != cudaSuccess) return err;
+  const int sms = device_sms();
+  const size_t static_smem =
+      kernel_static_smem(reinterpret_cast<const void*>(gemm_tc_kernel<kActNone, PAIR>));
   // As many pipeline stages as fit beside the epilogue buffers and the
   // kernel's static shared memory.
   const int bn_cta = PAIR ? BN / 2 : BN;
   const size_t stage_bytes = size_t(kTileM) * kTileK * 2 + size_t(bn_cta) * kTileK * 2;
   const size_t fixed = 1024 + size_t(kEpiWarps) * kEpiBufBytes;
-  const size_t budget = size_t(smem_optin) - fa.sharedSizeBytes;
+  const size_t budget = size_t(device_smem_optin()) - static_smem;
   int stages = budget > fixed ? int((budget - fixed) / stage_bytes) : 0;
   if (stages > kMaxStages) stages = kMaxStages;
   if (stages < 2) return cudaErrorInvalidValue;
   const size_t smem = fixed + size_t(stages) * stage_bytes;
   auto run = [&](auto kernel) {
-    cudaError_t e =
-        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kernel), smem);
     if (e != cudaSuccess) return e;
     unsigned grid = unsigned(sms);
     cudaLaunchConfig_t cfg{};
@@ -476,7 +471,7 @@ cudaError_t launch_variant(int act, const CUtensorMap& tmA, const CUtensorMap& t
       cfg.numAttrs = 1;
       cfg.gridDim = dim3(2);
       int clusters = 0;
-      e = cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg);
+      e = max_active_clusters(reinterpret_cast<const void*>(kernel), cfg, &clusters);
       if (e != cudaSuccess) return e;
       if (clusters < 1) return cudaErrorInvalidConfiguration;
       grid = unsigned(2 * clusters);

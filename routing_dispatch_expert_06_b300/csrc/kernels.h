@@ -14,27 +14,54 @@ void count_launch();
 // Records msg as the calling thread's moe_last_error() text; returns code.
 moe_status_t report_error(moe_status_t code, const char* msg);
 
-// Router on CUDA cores (fp32 or bf16): logits, softmax, top-k, weights, psum.
+// Host-side launch helpers that query the driver once per device (or per
+// kernel) and then answer from a cache, so a stage call costs little more
+// than its launches.
+int device_sms();                      // SMs of the current device
+int device_smem_optin();               // opt-in shared memory per block
+size_t kernel_static_smem(const void* kernel);
+// Raise the kernel's dynamic shared-memory limit to at least `bytes` on the
+// current device (once per device and size).
+cudaError_t ensure_dynamic_smem(const void* kernel, size_t bytes);
+// Resident clusters of the kernel for this launch shape (cached).
+cudaError_t max_active_clusters(const void* kernel, const cudaLaunchConfig_t& cfg, int* clusters);
+
+// Router on CUDA cores (fp32 or bf16, any E): logits, softmax, top-k,
+// weights; per-block column sums of p in psum_partial, summed into psum by the
+// last block to finish (counter: a zeroed int in the workspace).
 cudaError_t launch_route_simt(const moe_config_t& c, const void* x, const void* Wr,
                               const float* br, float* logits, int32_t* ids, float* w,
-                              float* psum_partial, float* psum, cudaStream_t st);
+                              float* psum_partial, float* psum, int* counter, cudaStream_t st);
 
-// psum[i] = Σ_b psum_partial[b][i] over nblk router blocks, b ascending.
-cudaError_t launch_psum_reduce(int64_t nblk, int E, const float* psum_partial, float* psum,
-                               cudaStream_t st);
+// Router on CUDA cores for bf16 layers with E <= 32 and W_r small enough for
+// shared memory: one warp per token, 16-byte loads, same outputs.
+bool route_warp_supported(const moe_config_t& c);
+cudaError_t launch_route_warp(const moe_config_t& c, const void* x, const void* Wr,
+                              const float* br, float* logits, int32_t* ids, float* w,
+                              float* psum_partial, float* psum, int* counter, cudaStream_t st);
 
-// Router on the tcgen05 tensor cores (bf16, E <= 256): same outputs as the
-// CUDA-core router; psum_partial holds one row per 128-token tile.
+// Router on the tcgen05 tensor cores (bf16, E <= 256): same outputs;
+// psum_partial holds one row per 128-token tile.
+// When T is small, nsplit CTAs share a tile's reduction over d through
+// split_part [n_tiles, nsplit, NP, 128] fp32 and split_count [n_tiles] (zeroed
+// ints, left zeroed).
 bool route_tc_supported(const moe_config_t& c);
+int route_tc_nsplit(const moe_config_t& c);
+int route_tc_np(const moe_config_t& c);
 cudaError_t launch_route_tc(const moe_config_t& c, const void* x, const void* Wr,
                             const float* br, float* logits, int32_t* ids, float* w,
-                            float* psum_partial, float* psum, int32_t* status, cudaStream_t st);
+                            float* psum_partial, float* psum, int* counter, int32_t* status,
+                            float* split_part, int* split_count, cudaStream_t st);
 
-// Dispatch: histogram per chunk, per-expert scan + capacity, positions, row copy.
+// Dispatch: histogram per chunk, per-expert scan + capacity, positions, row
+// copy.  counter: a zeroed int for the histogram's grid-completion count (the
+// last histogram block then runs the scan), or NULL for a separate scan
+// kernel.
 cudaError_t launch_dispatch(const moe_config_t& c, int64_t C, const void* x,
                             const int32_t* ids, int32_t* counts, int32_t* kept,
                             int32_t* offsets, int32_t* slot_row, int32_t* row_token, void* xd,
-                            int32_t* chunk_counts, int32_t* status, cudaStream_t st);
+                            int32_t* chunk_counts, int32_t* status, int* counter,
+                            cudaStream_t st);
 
 // Grouped GEMM on CUDA cores over ragged expert row ranges (fp32 or bf16):
 //   out[rows of e] = epi(A[rows of e] · B[e]ᵀ + bias[e]),  A [R,K], B [E,N,K].

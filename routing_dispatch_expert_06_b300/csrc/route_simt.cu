@@ -14,6 +14,18 @@
 
 namespace moe {
 
+struct Bf16x8 {
+  __device__ static void unpack(const uint4& v, float* f) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 p = __bfloat1622float2(h[i]);
+      f[2 * i] = p.x;
+      f[2 * i + 1] = p.y;
+    }
+  }
+};
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -83,7 +95,9 @@ template <typename TIn>
 __global__ void __launch_bounds__(256)
     route_simt_kernel(int64_t T, int d, int E, int k, int renorm, const TIn* __restrict__ x,
                       const TIn* __restrict__ Wr, const float* __restrict__ br, float* logits,
-                      int32_t* topk_ids, float* topk_w, float* psum_partial) {
+                      int32_t* topk_ids, float* topk_w, float* psum_partial, float* psum,
+                      int* counter) {
+  __shared__ int s_flag;
   extern __shared__ float smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float* s_log = smem + warp * E;
@@ -124,59 +138,143 @@ __global__ void __launch_bounds__(256)
     for (int w = 0; w < 8; ++w) s += smem[8 * E + w * E + e];
     psum_partial[int64_t(blockIdx.x) * E + e] = s;
   }
+  if (last_block_to_finish(counter, &s_flag)) sum_partials_rows(gridDim.x, E, psum_partial, psum);
 }
 
-// psum[i] = Σ_b partial[b][i], b ascending (fixed order, deterministic).
-__global__ void psum_reduce_kernel(int64_t nblk, int E, const float* __restrict__ part,
-                                   float* __restrict__ psum) {
-  const int e = blockIdx.x * blockDim.x + threadIdx.x;
-  if (e >= E) return;
-  float s = 0.f;
-  int64_t b = 0;
-  for (; b + 4 <= nblk; b += 4) {
-    float a0 = part[(b + 0) * E + e], a1 = part[(b + 1) * E + e];
-    float a2 = part[(b + 2) * E + e], a3 = part[(b + 3) * E + e];
-    s += a0;
-    s += a1;
-    s += a2;
-    s += a3;
+// Router on CUDA cores for small expert counts (bf16, E <= 32, W_r small
+// enough for shared memory): at E <= 32 the contraction has at most 32 flop
+// per byte of x, so it is bound by reading x and needs no tensor cores.  One
+// warp per token: lanes take 16-byte chunks of x (8 bf16), multiply them by
+// the same chunk of every W_r row (staged once per CTA in shared memory) and
+// keep EB running fp32 dot products.  A transposing butterfly leaves lane L
+// with the full sum for expert L >> (5 - log2 EB); softmax, top-k and weights
+// follow as in the other routers.  The block's column sums of p go to
+// psum_partial, and the last block to finish adds the rows in order.
+template <int EB>
+__global__ void __launch_bounds__(256)
+    route_warp_kernel(int64_t T, int d, int E, int k, int renorm,
+                      const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ Wr,
+                      const float* __restrict__ br, float* logits, int32_t* topk_ids,
+                      float* topk_w, float* psum_partial, float* psum, int* counter) {
+  extern __shared__ uint4 s_w[];  // [E][d/8] 16-byte chunks of W_r
+  __shared__ float s_log[8][32];
+  __shared__ float s_ps[8][32];
+  __shared__ int s_flag;
+  constexpr int kSteps = EB == 8 ? 3 : EB == 16 ? 4 : 5;  // halving steps
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nch = d / 8;
+  const uint4* wg = reinterpret_cast<const uint4*>(Wr);
+  for (int i = threadIdx.x; i < E * nch; i += blockDim.x) s_w[i] = wg[i];
+  s_ps[warp][lane] = 0.f;
+  __syncthreads();
+  const int col = lane >> (5 - kSteps);
+  const bool holder = (lane & ((1 << (5 - kSteps)) - 1)) == 0;
+  const int64_t nwarps = int64_t(gridDim.x) * 8;
+  for (int64_t t = int64_t(blockIdx.x) * 8 + warp; t < T; t += nwarps) {
+    float acc[EB];
+#pragma unroll
+    for (int e = 0; e < EB; ++e) acc[e] = 0.f;
+    const uint4* xr = reinterpret_cast<const uint4*>(x + t * d);
+    for (int c = lane; c < nch; c += 32) {
+      float xf[8];
+      Bf16x8::unpack(__ldcs(xr + c), xf);
+#pragma unroll
+      for (int e = 0; e < EB; ++e) {
+        if (e < E) {
+          float wf[8];
+          Bf16x8::unpack(s_w[e * nch + c], wf);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) acc[e] = fmaf(xf[j], wf[j], acc[e]);
+        }
+      }
+    }
+    int n = EB;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+      if (n > 1) {
+        const int half = n >> 1;
+        const bool upper = (lane & o) != 0;
+#pragma unroll
+        for (int j = 0; j < EB / 2; ++j) {
+          if (j < half) {
+            const float send = upper ? acc[j] : acc[j + half];
+            const float keep = upper ? acc[j + half] : acc[j];
+            acc[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+          }
+        }
+        n = half;
+      } else {
+        acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], o);
+      }
+    }
+    if (holder && col < E) s_log[warp][col] = acc[0] + br[col];
+    __syncwarp();
+    if (logits && lane < E) logits[t * E + lane] = s_log[warp][lane];
+    __syncwarp();
+    softmax_topk_warp(s_log[warp], s_ps[warp], E, k, renorm, t, topk_ids, topk_w);
+    __syncwarp();
   }
-  for (; b < nblk; ++b) s += part[b * E + e];
-  psum[e] = s;
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    float s = 0.f;
+    for (int w2 = 0; w2 < 8; ++w2) s += s_ps[w2][e];
+    psum_partial[int64_t(blockIdx.x) * E + e] = s;
+  }
+  if (last_block_to_finish(counter, &s_flag)) sum_partials_rows(gridDim.x, E, psum_partial, psum);
 }
 
 cudaError_t launch_route_simt(const moe_config_t& c, const void* x, const void* Wr,
                               const float* br, float* logits, int32_t* ids, float* w,
-                              float* psum_partial, float* psum, cudaStream_t st) {
+                              float* psum_partial, float* psum, int* counter, cudaStream_t st) {
   const int64_t nblk = (c.T + kRouteTokensSimt - 1) / kRouteTokensSimt;
   const size_t smem = size_t(16) * c.E * sizeof(float);
   cudaError_t err;
   if (c.dtype == MOE_DT_F32) {
-    err = cudaFuncSetAttribute(route_simt_kernel<float>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    err = ensure_dynamic_smem(reinterpret_cast<const void*>(route_simt_kernel<float>), smem);
     if (err != cudaSuccess) return err;
     route_simt_kernel<float><<<unsigned(nblk), 256, smem, st>>>(
         c.T, c.d, c.E, c.k, c.renormalize, static_cast<const float*>(x),
-        static_cast<const float*>(Wr), br, logits, ids, w, psum_partial);
+        static_cast<const float*>(Wr), br, logits, ids, w, psum_partial, psum, counter);
   } else {
-    err = cudaFuncSetAttribute(route_simt_kernel<__nv_bfloat16>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    err = ensure_dynamic_smem(reinterpret_cast<const void*>(route_simt_kernel<__nv_bfloat16>),
+                              smem);
     if (err != cudaSuccess) return err;
     route_simt_kernel<__nv_bfloat16><<<unsigned(nblk), 256, smem, st>>>(
         c.T, c.d, c.E, c.k, c.renormalize, static_cast<const __nv_bfloat16*>(x),
-        static_cast<const __nv_bfloat16*>(Wr), br, logits, ids, w, psum_partial);
+        static_cast<const __nv_bfloat16*>(Wr), br, logits, ids, w, psum_partial, psum, counter);
   }
   count_launch();
-  err = cudaGetLastError();
-  if (err != cudaSuccess) return err;
-  return launch_psum_reduce(nblk, c.E, psum_partial, psum, st);
+  return cudaGetLastError();
 }
 
-cudaError_t launch_psum_reduce(int64_t nblk, int E, const float* psum_partial, float* psum,
-                               cudaStream_t st) {
-  psum_reduce_kernel<<<unsigned((E + 255) / 256), 256, 0, st>>>(nblk, E, psum_partial, psum);
+bool route_warp_supported(const moe_config_t& c) {
+  return c.dtype == MOE_DT_BF16 && c.E <= 32 && size_t(c.E) * c.d * 2 <= kRouteWarpSmemMax;
+}
+
+cudaError_t launch_route_warp(const moe_config_t& c, const void* x, const void* Wr,
+                              const float* br, float* logits, int32_t* ids, float* w,
+                              float* psum_partial, float* psum, int* counter, cudaStream_t st) {
+  if (!route_warp_supported(c)) return cudaErrorInvalidValue;
+  const int sms = device_sms();
+  // Blocks of 8 warps, about 8 tokens per warp, at most 4 blocks per SM; one
+  // psum_partial row per block (at most ceil(T / 64) rows).
+  const int64_t want = (c.T + kRouteTokensSimt - 1) / kRouteTokensSimt;
+  const unsigned grid = unsigned(want < int64_t(4) * sms ? want : int64_t(4) * sms);
+  const size_t smem = size_t(c.E) * c.d * 2;
+  auto run = [&](auto kernel) {
+    cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kernel), smem);
+    if (e != cudaSuccess) return e;
+    kernel<<<grid, 256, smem, st>>>(c.T, c.d, c.E, c.k, c.renormalize,
+                                    static_cast<const __nv_bfloat16*>(x),
+                                    static_cast<const __nv_bfloat16*>(Wr), br, logits, ids, w,
+                                    psum_partial, psum, counter);
+    return cudaGetLastError();
+  };
+  cudaError_t err = c.E <= 8 ? run(route_warp_kernel<8>)
+                    : c.E <= 16 ? run(route_warp_kernel<16>)
+                                : run(route_warp_kernel<32>);
   count_launch();
-  return cudaGetLastError();
+  return err;
 }
 
 }  // namespace moe

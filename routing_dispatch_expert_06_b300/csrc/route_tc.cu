@@ -6,7 +6,12 @@
 // [MoE 模型原理 §2.2] S_t = TopK(p_t, k), p̃ = p/Σ_{S_t} p (or raw p);
 // [MoE 模型原理 §3.2] the column sums Σ_t p_{t,i} feed p̄_i.
 //
-// Tiles of 128 tokens; a CTA walks tiles b, b + grid, ...  Warps:
+// Tiles of 128 tokens.  When there are few tiles (small T), nsplit CTAs
+// share one tile's reduction over d: each takes a contiguous run of its
+// segments, writes its fp32 partial logits to a workspace buffer, and the
+// last split of the tile to arrive adds the splits in split order (so the
+// result does not depend on which CTA arrives last) and finishes the tile.
+// A CTA walks units (tile, split) b, b + grid, ...  Warps:
 //   warp 0     TMA producer: x tile [128 × 64] and W_r tile [NP × 64] per
 //              stage (NP = E rounded up to a power of two >= 32; rows past E
 //              and columns past d arrive as zeros from the copy engine's
@@ -29,7 +34,8 @@
 // expert index: insertion into a sorted list that only a strictly larger
 // value passes, and higher indices are always inserted later), then
 // Σ exp, weights, and the tile's column sums of p by a transposing warp
-// butterfly.  Every wait is bounded (4 s); on a timeout the kernel records
+// butterfly; the last CTA to finish adds the tiles' column sums in tile
+// order (deterministic).  Every wait is bounded (4 s); on a timeout the kernel records
 // MOE_ERR_TIMEOUT, drains its copies and MMAs, frees its tensor memory and
 // returns.
 #include "common.cuh"
@@ -60,7 +66,12 @@ struct RouteTcArgs {
   int32_t* ids;
   float* w;
   float* psum_partial;
+  float* psum;
+  int* counter;
   int32_t* status;
+  int nsplit;             // CTAs sharing one tile's reduction over d
+  float* split_part;      // [n_tiles][nsplit][NP][128] partial logits (nsplit > 1)
+  int* split_count;       // [n_tiles] zeroed arrival counters (nsplit > 1)
 };
 
 template <int G>
@@ -105,6 +116,8 @@ __global__ void __launch_bounds__(64 + 128 * G, 1)
   __shared__ float s_xmax[G / 2][kTileM];
   __shared__ float s_xtv[G / 2][KMAX][kTileM];
   __shared__ int s_xti[G / 2][KMAX][kTileM];
+  __shared__ int s_last;
+  __shared__ int s_last_cta;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -116,6 +129,13 @@ __global__ void __launch_bounds__(64 + 128 * G, 1)
   const int nk = (a.d + kTileK - 1) / kTileK;
   const int nseg = (nk + kSegBlocks - 1) / kSegBlocks;
   const int64_t n_tiles = (a.T + kTileM - 1) / kTileM;
+  // Work unit u: tile u / nsplit, segments [seg_lo, seg_hi) of split u % nsplit.
+  const int64_t n_units = n_tiles * a.nsplit;
+  auto seg_range = [&](int64_t u, int& lo, int& hi) {
+    const int sp = int(u % a.nsplit);
+    lo = int(int64_t(sp) * nseg / a.nsplit);
+    hi = int(int64_t(sp + 1) * nseg / a.nsplit);
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < a.stages; ++s) {
@@ -153,9 +173,12 @@ __global__ void __launch_bounds__(64 + 128 * G, 1)
     uint32_t phase = 0;
     int64_t issued = 0;
     bool ok = true;
-    for (int64_t tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-      const int32_t m0 = int32_t(tile * kTileM);
-      for (int kb = 0; kb < nk; ++kb) {
+    for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+      const int32_t m0 = int32_t((u / a.nsplit) * kTileM);
+      int seg_lo, seg_hi;
+      seg_range(u, seg_lo, seg_hi);
+      const int kb_hi = min(nk, seg_hi * kSegBlocks);
+      for (int kb = seg_lo * kSegBlocks; kb < kb_hi; ++kb) {
         if (!tc::mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, kWaitLimitNs)) {
           give_up();
           ok = false;
@@ -180,8 +203,10 @@ __global__ void __launch_bounds__(64 + 128 * G, 1)
     uint32_t phase = 0;
     uint32_t seg_count = 0;  // segments issued by this CTA (all tiles)
     bool ok = true;
-    for (int64_t tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-      for (int sg = 0; sg < nseg && ok; ++sg, ++seg_count) {
+    for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+      int seg_lo, seg_hi;
+      seg_range(u, seg_lo, seg_hi);
+      for (int sg = seg_lo; sg < seg_hi && ok; ++sg, ++seg_count) {
         const uint32_t buf = seg_count & 1u;
         if (!tc::mbar_wait(&tempty_bar[buf], ((seg_count >> 1) & 1u) ^ 1u, abort_flag,
                            kWaitLimitNs)) {
@@ -227,13 +252,16 @@ __global__ void __launch_bounds__(64 + 128 * G, 1)
     const uint32_t t_lane = tmem_base + (uint32_t(quarter * 32) << 16) + uint32_t(col0);
     uint32_t seg_count = 0;
     bool ok = true;
-    for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+    for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
+      const int64_t tile = u / a.nsplit;
       const int64_t t = tile * kTileM + row;
       const bool valid = t < a.T;
+      int seg_lo, seg_hi;
+      seg_range(u, seg_lo, seg_hi);
       float v[NPG];
 #pragma unroll
       for (int j = 0; j < NPG; ++j) v[j] = 0.f;
-      for (int sg = 0; sg < nseg; ++sg, ++seg_count) {
+      for (int sg = seg_lo; sg < seg_hi; ++sg, ++seg_count) {
         const uint32_t buf = seg_count & 1u;
         if (ok) {
           // The tensor-memory loads are warp-collective: the whole warp takes
@@ -258,6 +286,32 @@ __global__ void __launch_bounds__(64 + 128 * G, 1)
           tc::fence_before_sync();
           tc::mbar_arrive(&tempty_bar[buf]);
         }
+      }
+      if (a.nsplit > 1) {
+        // Hand this split's partial logits over; the last split of the tile to
+        // arrive adds all splits in split order and goes on, the others move
+        // to their next unit.
+        const int sp = int(u % a.nsplit);
+        float* mine = a.split_part + ((tile * a.nsplit + sp) * NP + col0) * kTileM + row;
+#pragma unroll
+        for (int j = 0; j < NPG; ++j) __stcg(mine + j * kTileM, v[j]);
+        __threadfence();
+        bar_epi<G>();
+        if (threadIdx.x == 64) {
+          const int prev = atomicAdd(a.split_count + tile, 1);
+          const bool last = prev == a.nsplit - 1;
+          if (last) atomicExch(a.split_count + tile, 0);
+          s_last = last;
+        }
+        bar_epi<G>();
+        if (!s_last) continue;
+        __threadfence();
+        const float* base = a.split_part + (tile * a.nsplit * NP + col0) * kTileM + row;
+#pragma unroll
+        for (int j = 0; j < NPG; ++j) v[j] = __ldcg(base + j * kTileM);
+        for (int s2 = 1; s2 < a.nsplit; ++s2)
+#pragma unroll
+          for (int j = 0; j < NPG; ++j) v[j] += __ldcg(base + (int64_t(s2) * NP + j) * kTileM);
       }
       // Logits, this group's max and top-k.
       float gmax = -INFINITY;
@@ -372,6 +426,9 @@ __global__ void __launch_bounds__(64 + 128 * G, 1)
     __syncwarp();
     tc::tmem_dealloc(tmem_base, a.tmem_cols);
   }
+  // The last CTA to finish adds the per-tile column sums, in tile order.
+  if (last_block_to_finish(a.counter, &s_last_cta))
+    sum_partials_rows(n_tiles, a.E, a.psum_partial, a.psum);
 }
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -408,22 +465,17 @@ template <int NPG, int G, int KMAX>
 cudaError_t launch_k(const CUtensorMap& tmX, const CUtensorMap& tmW, RouteTcArgs a,
                      unsigned grid, cudaStream_t st) {
   auto kernel = route_tc_kernel<NPG, G, KMAX>;
-  int dev = 0, smem_optin = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-  cudaFuncAttributes fa{};
-  cudaError_t err = cudaFuncGetAttributes(&fa, kernel);
-  if (err != cudaSuccess) return err;
+  const void* kp = reinterpret_cast<const void*>(kernel);
   // As many stages as fit beside the kernel's static shared memory.
   const size_t stage_bytes = size_t(kTileM) * kTileK * 2 + size_t(G * NPG) * kTileK * 2;
-  const size_t budget = size_t(smem_optin) - fa.sharedSizeBytes - 1024;
+  const size_t budget = size_t(device_smem_optin()) - kernel_static_smem(kp) - 1024;
   int stages = int(budget / stage_bytes);
   if (stages > kMaxStages) stages = kMaxStages;
   if (stages < 2) return cudaErrorInvalidValue;
   a.stages = stages;
   size_t smem = 1024 + size_t(stages) * stage_bytes;
   if (smem < kMinSmem) smem = kMinSmem;
-  err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  cudaError_t err = ensure_dynamic_smem(kp, smem);
   if (err != cudaSuccess) return err;
   kernel<<<grid, 64 + 128 * G, smem, st>>>(tmX, tmW, a);
   return cudaGetLastError();
@@ -441,13 +493,32 @@ cudaError_t launch_np(int k, const CUtensorMap& tmX, const CUtensorMap& tmW,
 
 }  // namespace
 
+// Splits per tile: enough (tile, split) units to give every SM of a
+// 148-SM part about one unit, at most one split per segment.  Depends on the
+// configuration only, so results do not depend on the device.
+int route_tc_nsplit(const moe_config_t& c) {
+  const int64_t n_tiles = (c.T + kTileM - 1) / kTileM;
+  const int nseg = int(((c.d + kTileK - 1) / kTileK + kSegBlocks - 1) / kSegBlocks);
+  int64_t ns = kRouteSplitUnits / n_tiles;
+  if (ns > nseg) ns = nseg;
+  if (ns < 1) ns = 1;
+  return int(ns);
+}
+
+int route_tc_np(const moe_config_t& c) {
+  int NP = 32;
+  while (NP < c.E) NP <<= 1;
+  return NP;
+}
+
 bool route_tc_supported(const moe_config_t& c) {
   return c.dtype == MOE_DT_BF16 && c.E <= kMaxNP && c.k <= 16;
 }
 
 cudaError_t launch_route_tc(const moe_config_t& c, const void* x, const void* Wr,
                             const float* br, float* logits, int32_t* ids, float* w,
-                            float* psum_partial, float* psum, int32_t* status, cudaStream_t st) {
+                            float* psum_partial, float* psum, int* counter, int32_t* status,
+                            float* split_part, int* split_count, cudaStream_t st) {
   if (!route_tc_supported(c)) return cudaErrorInvalidValue;
   EncodeTiledFn encode = get_encode();
   if (!encode) return cudaErrorNotSupported;
@@ -466,16 +537,19 @@ cudaError_t launch_route_tc(const moe_config_t& c, const void* x, const void* Wr
   a.ids = ids;
   a.w = w;
   a.psum_partial = psum_partial;
+  a.psum = psum;
+  a.counter = counter;
   a.status = status;
+  a.nsplit = route_tc_nsplit(c);
+  a.split_part = split_part;
+  a.split_count = split_count;
 
   CUtensorMap tmX, tmW;
   if (!encode_2d(encode, &tmX, x, c.d, c.T, kTileK, kTileM)) return cudaErrorInvalidValue;
   if (!encode_2d(encode, &tmW, Wr, c.d, c.E, kTileK, uint32_t(NP))) return cudaErrorInvalidValue;
-  const int64_t n_tiles = (c.T + kTileM - 1) / kTileM;
-  int dev = 0, sms = 148;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const unsigned grid = unsigned(n_tiles < sms ? n_tiles : sms);
+  const int64_t n_units = ((c.T + kTileM - 1) / kTileM) * a.nsplit;
+  const int sms = device_sms();
+  const unsigned grid = unsigned(n_units < sms ? n_units : sms);
   cudaError_t err;
   switch (NP) {
     case 32: err = launch_np<16, 2>(c.k, tmX, tmW, a, grid, st); break;
@@ -484,8 +558,7 @@ cudaError_t launch_route_tc(const moe_config_t& c, const void* x, const void* Wr
     default: err = launch_np<64, 4>(c.k, tmX, tmW, a, grid, st); break;
   }
   count_launch();
-  if (err != cudaSuccess) return err;
-  return launch_psum_reduce(n_tiles, c.E, psum_partial, psum, st);
+  return err;
 }
 
 }  // namespace moe

@@ -1,8 +1,9 @@
 """Router parity on ragged shapes, through the C ABI (moe_route).
 
-Both routers are checked: the tensor-core router (bf16, E <= 256, the default
-for bf16 layers) and the CUDA-core router (MOE_ROUTE_IMPL=simt).  Against
-the oracle ("MoE 模型原理" §2.1–§2.2):
+Three routers are checked: the warp router (bf16, E <= 32, the default there),
+the tensor-core router (bf16, E <= 256) and the generic CUDA-core router
+(MOE_ROUTE_IMPL=warp|tc|simt forces one where it applies).  Against the
+oracle ("MoE 模型原理" §2.1–§2.2):
 
 * logits within 1e-5 · max(|ref|, rms(row)) of the double-precision router;
 * top-k ids bit-exact with the oracle's selection on the device's own fp32
@@ -54,8 +55,7 @@ def _route(wl, inp, impl):
     cfg = moe.config_from_workload(wl, write_logits=True)
     ws = moe.workspace(cfg)
     out = moe.allocate(cfg)
-    if impl == "simt":
-        os.environ["MOE_ROUTE_IMPL"] = "simt"
+    os.environ["MOE_ROUTE_IMPL"] = impl
     try:
         moe.route(cfg, inp["x"], inp["Wr"], inp["br"], out, ws)
         torch.cuda.synchronize()
@@ -75,7 +75,7 @@ def _check(wl, inp, out):
     assert_rel_rms(h(out["psum"]), psum, 1e-4, "psum")
 
 
-@pytest.mark.parametrize("impl", ["tc", "simt"])
+@pytest.mark.parametrize("impl", ["warp", "tc", "simt"])
 @pytest.mark.parametrize("case", CASES, ids=lambda c: f"t{c[0]}_d{c[1]}_e{c[2]}_k{c[3]}")
 def test_router_matches_oracle(case, impl):
     wl = _workload(*case)
@@ -83,7 +83,7 @@ def test_router_matches_oracle(case, impl):
     _check(wl, inp, _route(wl, inp, impl))
 
 
-@pytest.mark.parametrize("impl", ["tc", "simt"])
+@pytest.mark.parametrize("impl", ["warp", "tc", "simt"])
 def test_router_ties_go_to_lower_index(impl):
     # W_r = 0 makes every logit equal to its bias; the bias repeats values, so
     # the ranking must break ties by the lower expert index.
@@ -110,3 +110,26 @@ def test_tensor_core_router_agrees_with_cuda_core_router():
     # the two routers round differently, so a near-tie may rank differently;
     # with these seeded inputs nearly every token must agree
     assert same.mean() > 0.99
+
+
+def test_warp_router_agrees_with_tensor_core_router():
+    wl = _workload(5000, 1024, 8, 2, True, "normal:0.5", seed=9)
+    inp = inputs.make_inputs(wl, "cuda")
+    a = _route(wl, inp, "warp")
+    b = _route(wl, inp, "tc")
+    assert_rel_rms(h(a["logits"]), h(b["logits"]).astype(np.float64), 2e-5, "warp vs tc logits")
+    same = (h(a["topk_ids"]) == h(b["topk_ids"])).all(axis=1)
+    assert same.mean() > 0.99
+
+
+def test_unaligned_inputs_take_the_generic_router():
+    # x starting 2 bytes past a 16-byte boundary: the 16-byte routers must not
+    # be used; the result still matches the oracle.
+    wl = _workload(300, 200, 20, 3, True, "normal:1.0")
+    inp = inputs.make_inputs(wl, "cuda")
+    buf = torch.empty(wl.T * wl.d + 1, dtype=torch.bfloat16, device="cuda")
+    x = buf[1:].view(wl.T, wl.d)
+    x.copy_(inp["x"])
+    assert x.data_ptr() % 16 != 0
+    inp = dict(inp, x=x)
+    _check(wl, inp, _route(wl, inp, "warp"))
