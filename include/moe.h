@@ -191,7 +191,9 @@ moe_status_t moe_combine(const moe_config_t* cfg, const void* yd, const int32_t*
 moe_status_t moe_aux_stats(const moe_config_t* cfg, const int32_t* counts, const float* psum,
                            float alpha, float* f, float* pbar, float* l_aux, void* stream);
 
-/* The whole layer: route, dispatch, expert FFN, combine, aux. */
+/* The whole layer: route, dispatch, expert FFN, combine, aux (the aux
+ * statistics are computed inside the dispatch launches here, with the same
+ * arithmetic and results as moe_aux_stats). */
 moe_status_t moe_forward(const moe_config_t* cfg, const moe_tensors_t* t, float alpha, void* ws,
                          size_t ws_bytes, void* stream);
 

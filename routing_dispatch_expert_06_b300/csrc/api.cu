@@ -286,9 +286,16 @@ moe_status_t moe_route(const moe_config_t* cfg, const void* x, const void* Wr, c
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_route");
 }
 
-moe_status_t moe_dispatch(const moe_config_t* cfg, const void* x, const int32_t* topk_ids,
-                          int32_t* counts, int32_t* kept, int32_t* offsets, int32_t* slot_row,
-                          int32_t* row_token, void* xd, void* ws, size_t ws_bytes, void* stream) {
+}  // extern "C"
+
+namespace moe {
+// moe_dispatch, optionally with the f / p̄ / L_aux statistics computed by the
+// histogram's last block (aux != NULL, as in moe_forward).
+static moe_status_t dispatch_impl(const moe_config_t* cfg, const void* x,
+                                  const int32_t* topk_ids, int32_t* counts, int32_t* kept,
+                                  int32_t* offsets, int32_t* slot_row, int32_t* row_token,
+                                  void* xd, void* ws, size_t ws_bytes, const AuxArgs* aux,
+                                  void* stream) {
   moe_status_t s = check_cfg(cfg);
   if (s != MOE_OK) return s;
   if (!x || !topk_ids || !counts || !kept || !offsets || !slot_row || !row_token || !xd)
@@ -300,8 +307,18 @@ moe_status_t moe_dispatch(const moe_config_t* cfg, const void* x, const int32_t*
   const int64_t C = capacity_of(cfg->T, cfg->k, cfg->E, cfg->capacity_factor);
   cudaError_t e = launch_dispatch(*cfg, C, x, topk_ids, counts, kept, offsets, slot_row,
                                   row_token, xd, w.chunk_counts, w.status, w.dispatch_counter,
-                                  static_cast<cudaStream_t>(stream));
+                                  aux, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_dispatch");
+}
+}  // namespace moe
+
+extern "C" {
+
+moe_status_t moe_dispatch(const moe_config_t* cfg, const void* x, const int32_t* topk_ids,
+                          int32_t* counts, int32_t* kept, int32_t* offsets, int32_t* slot_row,
+                          int32_t* row_token, void* xd, void* ws, size_t ws_bytes, void* stream) {
+  return dispatch_impl(cfg, x, topk_ids, counts, kept, offsets, slot_row, row_token, xd, ws,
+                       ws_bytes, nullptr, stream);
 }
 
 moe_status_t moe_ffn_up(const moe_config_t* cfg, const void* xd, const int32_t* offsets,
@@ -381,18 +398,22 @@ moe_status_t moe_aux_stats(const moe_config_t* cfg, const int32_t* counts, const
 moe_status_t moe_forward(const moe_config_t* cfg, const moe_tensors_t* t, float alpha, void* ws,
                          size_t ws_bytes, void* stream) {
   if (!t) return fail(MOE_ERR_INVALID_ARG, "moe_forward: tensors is NULL");
+  if (!t->f || !t->pbar || !t->l_aux)
+    return fail(MOE_ERR_INVALID_ARG, "moe_aux_stats: NULL tensor");
   moe_status_t s;
   if ((s = moe_route(cfg, t->x, t->Wr, t->br, t->logits, t->topk_ids, t->topk_w, t->psum, ws,
                      ws_bytes, stream)) != MOE_OK)
     return s;
-  if ((s = moe_dispatch(cfg, t->x, t->topk_ids, t->counts, t->kept, t->offsets, t->slot_row,
-                        t->row_token, t->xd, ws, ws_bytes, stream)) != MOE_OK)
+  // The statistics need only counts and psum: the dispatch's last histogram
+  // block computes them (same arithmetic as moe_aux_stats), saving a launch.
+  const AuxArgs aux{alpha, t->psum, t->f, t->pbar, t->l_aux};
+  if ((s = dispatch_impl(cfg, t->x, t->topk_ids, t->counts, t->kept, t->offsets, t->slot_row,
+                         t->row_token, t->xd, ws, ws_bytes, &aux, stream)) != MOE_OK)
     return s;
   if ((s = moe_expert_ffn(cfg, t->xd, t->offsets, t->W1, t->b1, t->W2, t->b2, t->H, t->yd, ws,
                           ws_bytes, stream)) != MOE_OK)
     return s;
-  if ((s = moe_combine(cfg, t->yd, t->slot_row, t->topk_w, t->y, stream)) != MOE_OK) return s;
-  return moe_aux_stats(cfg, t->counts, t->psum, alpha, t->f, t->pbar, t->l_aux, stream);
+  return moe_combine(cfg, t->yd, t->slot_row, t->topk_w, t->y, stream);
 }
 
 moe_status_t moe_get_device_status(const void* ws, int32_t* status) {

@@ -105,27 +105,12 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-// One CTA; thread i handles expert i (E <= 1024), then a fixed-shape tree sum.
-__global__ void __launch_bounds__(1024)
+// One block computes f, p̄ and L_aux (see aux_stats_block).
+__global__ void __launch_bounds__(kAuxThreads)
     aux_kernel(int E, int64_t T, float alpha, const int32_t* __restrict__ counts,
                const float* __restrict__ psum, float* f, float* pbar, float* l_aux) {
-  __shared__ float red[1024];
-  const int i = threadIdx.x;
-  float prod = 0.f;
-  if (i < E) {
-    const float fi = float(counts[i]) / float(T);
-    const float pi = psum[i] / float(T);
-    f[i] = fi;
-    pbar[i] = pi;
-    prod = fi * pi;
-  }
-  red[i] = prod;
-  __syncthreads();
-  for (int s = 512; s > 0; s >>= 1) {
-    if (i < s) red[i] += red[i + s];
-    __syncthreads();
-  }
-  if (i == 0) *l_aux = alpha * float(E) * red[0];
+  __shared__ float red[kAuxThreads];
+  aux_stats_block(E, T, alpha, counts, psum, f, pbar, l_aux, red);
 }
 
 cudaError_t launch_combine(const moe_config_t& c, int64_t max_rows, const void* yd,
@@ -156,7 +141,7 @@ cudaError_t launch_combine(const moe_config_t& c, int64_t max_rows, const void* 
 
 cudaError_t launch_aux(const moe_config_t& c, const int32_t* counts, const float* psum,
                        float alpha, float* f, float* pbar, float* l_aux, cudaStream_t st) {
-  aux_kernel<<<1, 1024, 0, st>>>(c.E, c.T, alpha, counts, psum, f, pbar, l_aux);
+  aux_kernel<<<1, kAuxThreads, 0, st>>>(c.E, c.T, alpha, counts, psum, f, pbar, l_aux);
   count_launch();
   return cudaGetLastError();
 }

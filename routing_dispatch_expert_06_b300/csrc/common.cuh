@@ -70,6 +70,44 @@ __device__ __forceinline__ void sum_partials_rows(int64_t nblk, int E, const flo
   }
 }
 
+// [MoE 模型原理 §3.2] f_i = counts_i/T, p̄_i = psum_i/T, L_aux = α·E·Σ_i f_i p̄_i,
+// computed by one block of kAuxThreads threads: thread j takes experts j,
+// j + kAuxThreads, ... in order, then a fixed-shape tree adds the threads'
+// sums.  Explicitly rounded products and sums keep the result identical
+// wherever the routine runs (the stand-alone statistics kernel, or the last
+// histogram block of a forward pass).  red: kAuxThreads floats of shared memory.
+constexpr int kAuxThreads = 256;
+__device__ __forceinline__ void aux_stats_block(int E, int64_t T, float alpha,
+                                                const int32_t* counts, const float* psum,
+                                                float* f, float* pbar, float* l_aux, float* red) {
+  const int j = threadIdx.x;
+  float prod = 0.f;
+  for (int e = j; e < E; e += kAuxThreads) {
+    const float fi = float(__ldcg(counts + e)) / float(T);
+    const float pi = __ldcg(psum + e) / float(T);
+    f[e] = fi;
+    pbar[e] = pi;
+    prod = __fadd_rn(prod, __fmul_rn(fi, pi));
+  }
+  red[j] = prod;
+  __syncthreads();
+  for (int s = kAuxThreads / 2; s > 0; s >>= 1) {
+    if (j < s) red[j] = __fadd_rn(red[j], red[j + s]);
+    __syncthreads();
+  }
+  if (j == 0) *l_aux = __fmul_rn(__fmul_rn(alpha, float(E)), red[0]);
+}
+
+// Aux-statistics outputs for the dispatch's last histogram block (forward
+// pass only).
+struct AuxArgs {
+  float alpha;
+  const float* psum;
+  float* f;
+  float* pbar;
+  float* l_aux;
+};
+
 // Record the first asynchronous error in the status word.
 __device__ __forceinline__ void set_status(int32_t* status, int32_t code) {
   if (status) atomicCAS(status, 0, code);

@@ -28,6 +28,7 @@ namespace moe {
 
 constexpr int kDispatchThreads = 256;  // 8 warps × 32 tokens = one chunk
 static_assert(kDispatchThreads == kChunkTokens, "one token per thread in a chunk");
+static_assert(kDispatchThreads == kAuxThreads, "the last histogram block runs the statistics");
 
 // Per-expert exclusive scan over the chunk histograms (in place), the total
 // count and kept = min(count, C); threads of one block stride over experts.
@@ -63,9 +64,11 @@ __device__ void scan_chunks_by_expert(int64_t n_chunks, int E, int64_t C,
 __global__ void __launch_bounds__(kDispatchThreads)
     histogram_kernel(int64_t T, int E, int k, const int32_t* __restrict__ ids,
                      int32_t* __restrict__ chunk_counts, int32_t* status, int* counter,
-                     int64_t C, int32_t* __restrict__ counts, int32_t* __restrict__ kept) {
+                     int64_t C, int32_t* __restrict__ counts, int32_t* __restrict__ kept,
+                     AuxArgs aux) {
   extern __shared__ int32_t hist[];
   __shared__ int s_last;
+  __shared__ float s_red[kAuxThreads];
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
   const int64_t t = int64_t(blockIdx.x) * kChunkTokens + threadIdx.x;
@@ -81,8 +84,13 @@ __global__ void __launch_bounds__(kDispatchThreads)
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x)
     chunk_counts[int64_t(blockIdx.x) * E + e] = hist[e];
-  if (counter && last_block_to_finish(counter, &s_last))
+  if (counter && last_block_to_finish(counter, &s_last)) {
     scan_chunks_by_expert(gridDim.x, E, C, chunk_counts, counts, kept);
+    if (aux.f) {
+      __syncthreads();
+      aux_stats_block(E, T, aux.alpha, counts, aux.psum, aux.f, aux.pbar, aux.l_aux, s_red);
+    }
+  }
 }
 
 // One CTA per expert: exclusive scan of that expert's chunk counts (in place),
@@ -250,11 +258,12 @@ cudaError_t launch_dispatch(const moe_config_t& c, int64_t C, const void* x,
                             const int32_t* ids, int32_t* counts, int32_t* kept,
                             int32_t* offsets, int32_t* slot_row, int32_t* row_token, void* xd,
                             int32_t* chunk_counts, int32_t* status, int* counter,
-                            cudaStream_t st) {
+                            const AuxArgs* aux, cudaStream_t st) {
   const int64_t n_chunks = (c.T + kChunkTokens - 1) / kChunkTokens;
+  const AuxArgs aux_v = (aux && counter) ? *aux : AuxArgs{0.f, nullptr, nullptr, nullptr, nullptr};
   cudaError_t err;
   histogram_kernel<<<unsigned(n_chunks), kDispatchThreads, size_t(c.E) * 4, st>>>(
-      c.T, c.E, c.k, ids, chunk_counts, status, counter, C, counts, kept);
+      c.T, c.E, c.k, ids, chunk_counts, status, counter, C, counts, kept, aux_v);
   count_launch();
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   if (!counter) {

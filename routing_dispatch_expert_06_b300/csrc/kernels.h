@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "common.cuh"
 #include "moe.h"
 
 namespace moe {
@@ -55,13 +56,13 @@ cudaError_t launch_route_tc(const moe_config_t& c, const void* x, const void* Wr
 
 // Dispatch: histogram per chunk, per-expert scan + capacity, positions, row
 // copy.  counter: a zeroed int for the histogram's grid-completion count (the
-// last histogram block then runs the scan), or NULL for a separate scan
-// kernel.
+// last histogram block then runs the scan, and with aux != NULL also the
+// f / p̄ / L_aux statistics), or NULL for a separate scan kernel.
 cudaError_t launch_dispatch(const moe_config_t& c, int64_t C, const void* x,
                             const int32_t* ids, int32_t* counts, int32_t* kept,
                             int32_t* offsets, int32_t* slot_row, int32_t* row_token, void* xd,
                             int32_t* chunk_counts, int32_t* status, int* counter,
-                            cudaStream_t st);
+                            const AuxArgs* aux, cudaStream_t st);
 
 // Grouped GEMM on CUDA cores over ragged expert row ranges (fp32 or bf16):
 //   out[rows of e] = epi(A[rows of e] · B[e]ᵀ + bias[e]),  A [R,K], B [E,N,K].

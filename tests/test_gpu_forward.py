@@ -112,3 +112,33 @@ def test_two_sm_gemm_matches_one_sm_gemm():
         a = out_p[name][:n].float()
         b = out_1[name][:n].float()
         assert ((a - b).abs() <= 1e-2 + 2e-2 * b.abs()).all(), name
+
+
+def test_forward_replays_from_a_cuda_graph():
+    # moe_forward only enqueues kernels (no allocation, no synchronisation),
+    # so it can be captured once and replayed; the replay must reproduce the
+    # eager outputs bit for bit (the benchmark times such replays).
+    wl = W["bf16_t8192_d2048_e64_top6"].replace(T=3000)
+    cfg, inp, out_e, _ = run_gpu(wl)
+    ws = moe.workspace(cfg)
+    out_g = moe.allocate(cfg)
+    moe.forward(cfg, inp, out_g, ws, 1.0)  # first call per shape: host-side setup
+    torch.cuda.synchronize()
+    for t in out_g.values():
+        if t is not None:
+            t.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        moe.forward(cfg, inp, out_g, ws, 1.0)
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    assert moe.device_status(ws) == moe.MOE_OK
+    n = int(h(out_e["offsets"])[-1])
+    for name in ["logits", "topk_ids", "topk_w", "psum", "counts", "kept", "offsets", "slot_row",
+                 "f", "pbar", "l_aux", "y"]:
+        if out_e[name] is None:
+            continue
+        assert torch.equal(out_e[name], out_g[name]), name
+    for name in ["row_token", "xd", "H", "yd"]:
+        assert torch.equal(out_e[name][:n], out_g[name][:n]), name
