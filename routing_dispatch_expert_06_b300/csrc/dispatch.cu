@@ -31,31 +31,50 @@ static_assert(kDispatchThreads == kChunkTokens, "one token per thread in a chunk
 static_assert(kDispatchThreads == kAuxThreads, "the last histogram block runs the statistics");
 
 // Per-expert exclusive scan over the chunk histograms (in place), the total
-// count and kept = min(count, C); threads of one block stride over experts.
-// Each expert's chunks are read eight at a time so the loads overlap.
+// count and kept = min(count, C), by one block.  A group of tpe lanes (a power
+// of two, as many as the block holds for E experts, at most 32) scans one
+// expert; each lane loads 8 consecutive chunk counts at once, so an expert's
+// n_chunks take ceil(n_chunks / (8·tpe)) rounds of overlapping loads.
 __device__ void scan_chunks_by_expert(int64_t n_chunks, int E, int64_t C,
                                       int32_t* __restrict__ chunk_counts,
                                       int32_t* __restrict__ counts, int32_t* __restrict__ kept) {
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int32_t run = 0;
-    int64_t ch = 0;
-    for (; ch + 8 <= n_chunks; ch += 8) {
-      int32_t v[8];
+  constexpr int U = 8;
+  int tpe = 32;
+  while (tpe > 1 && tpe * E > int(blockDim.x)) tpe >>= 1;
+  const int lane = threadIdx.x & 31;
+  const int sub = lane & (tpe - 1);
+  const int group = threadIdx.x / tpe;
+  const int ngroups = blockDim.x / tpe;
+  const unsigned gmask =
+      tpe == 32 ? 0xffffffffu : (((1u << tpe) - 1u) << (lane & ~(tpe - 1)));
+  for (int e = group; e < E; e += ngroups) {
+    int32_t carry = 0;
+    for (int64_t base = 0; base < n_chunks; base += int64_t(tpe) * U) {
+      const int64_t c0 = base + int64_t(sub) * U;
+      int32_t v[U];
+      int32_t tot = 0;
 #pragma unroll
-      for (int u = 0; u < 8; ++u) v[u] = __ldcg(chunk_counts + (ch + u) * E + e);
+      for (int u = 0; u < U; ++u) {
+        v[u] = c0 + u < n_chunks ? __ldcg(chunk_counts + (c0 + u) * E + e) : 0;
+        tot += v[u];
+      }
+      int32_t incl = tot;
+      for (int o = 1; o < tpe; o <<= 1) {
+        const int32_t up = __shfl_up_sync(gmask, incl, o, tpe);
+        if (sub >= o) incl += up;
+      }
+      int32_t run = carry + incl - tot;
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        chunk_counts[(ch + u) * E + e] = run;
+      for (int u = 0; u < U; ++u) {
+        if (c0 + u < n_chunks) chunk_counts[(c0 + u) * E + e] = run;
         run += v[u];
       }
+      carry += __shfl_sync(gmask, incl, tpe - 1, tpe);
     }
-    for (; ch < n_chunks; ++ch) {
-      const int32_t v = __ldcg(chunk_counts + ch * E + e);
-      chunk_counts[ch * E + e] = run;
-      run += v;
+    if (sub == 0) {
+      counts[e] = carry;
+      kept[e] = int32_t(carry < C ? carry : C);
     }
-    counts[e] = run;
-    kept[e] = int32_t(run < C ? run : C);
   }
 }
 
@@ -150,25 +169,25 @@ __global__ void __launch_bounds__(kDispatchThreads)
   }
 
   // Expert offsets: exclusive scan of kept[0..E).  Thread i sums a run of
-  // consecutive experts, then a scan over the 256 run totals.
+  // consecutive experts; a block scan (warp shuffles, then the 8 warp
+  // totals) gives each run's start.
   const int per = (E + kDispatchThreads - 1) / kDispatchThreads;
   const int lo = tid * per, hi = min(E, lo + per);
   int32_t run = 0;
   for (int e = lo; e < hi; ++e) run += kept[e];
-  part[tid] = run;
-  __syncthreads();
-  if (tid == 0) {
-    int32_t acc = 0;
-    for (int i = 0; i < kDispatchThreads; ++i) {
-      int32_t v = part[i];
-      part[i] = acc;
-      acc += v;
-    }
-    off[E] = acc;
+  int32_t incl = run;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t u = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += u;
   }
+  if (lane == 31) part[warp] = incl;
   __syncthreads();
+  int32_t before = 0;
+  for (int w = 0; w < warp; ++w) before += part[w];
+  if (tid == kDispatchThreads - 1) off[E] = before + incl;
   {
-    int32_t acc = part[tid];
+    int32_t acc = before + incl - run;
     for (int e = lo; e < hi; ++e) {
       off[e] = acc;
       acc += kept[e];
