@@ -52,10 +52,12 @@ struct Vec<float> {
 };
 
 // One warp per token.  Lane r < k fetches slot r's row and weight; every
-// lane then holds all k (row, weight) pairs.  For each 16-byte column vector
-// the k row loads are issued together before any arithmetic, so a lane keeps
-// up to KMAX independent loads in flight; the weighted sum then runs in rank
-// order (a dropped slot adds 0·0, which leaves the fp32 sum unchanged).
+// lane then holds all k (row, weight) pairs.  Each lane takes two 16-byte
+// column vectors per step and issues the 2·k row loads together before any
+// arithmetic, so it keeps up to 2·KMAX independent loads in flight (one
+// vector per step measured 20-25% slower on the larger layers); the weighted
+// sum then runs in rank order (a dropped slot adds 0·0, which leaves the fp32
+// sum unchanged).
 template <typename T, int KMAX>
 __global__ void __launch_bounds__(256)
     combine_kernel(int64_t n_tok, int k, int64_t row_vecs, int64_t max_rows,
@@ -80,27 +82,34 @@ __global__ void __launch_bounds__(256)
       wts[r] = kept[r] ? __shfl_sync(0xffffffffu, my_w, r) : 0.f;
       src[r] = yd + (kept[r] ? int64_t(row) * row_vecs : 0);
     }
-    for (int64_t v = lane; v < row_vecs; v += 32) {
-      uint4 buf[KMAX];
+    for (int64_t v0 = lane; v0 < row_vecs; v0 += 64) {
+      uint4 buf[2][KMAX];
 #pragma unroll
-      for (int r = 0; r < KMAX; ++r)
-        if (kept[r]) buf[r] = __ldcs(src[r] + v);
-      float acc[NV];
+      for (int u = 0; u < 2; ++u)
 #pragma unroll
-      for (int i = 0; i < NV; ++i) acc[i] = 0.f;
+        for (int r = 0; r < KMAX; ++r)
+          if (kept[r] && v0 + 32 * u < row_vecs) buf[u][r] = __ldcs(src[r] + v0 + 32 * u);
 #pragma unroll
-      for (int r = 0; r < KMAX; ++r) {
-        float f[NV];
-        if (kept[r]) {
-          Vec<T>::unpack(buf[r], f);
-        } else {
+      for (int u = 0; u < 2; ++u) {
+        const int64_t v = v0 + 32 * u;
+        if (v >= row_vecs) break;
+        float acc[NV];
 #pragma unroll
-          for (int i = 0; i < NV; ++i) f[i] = 0.f;
+        for (int i = 0; i < NV; ++i) acc[i] = 0.f;
+#pragma unroll
+        for (int r = 0; r < KMAX; ++r) {
+          float f[NV];
+          if (kept[r]) {
+            Vec<T>::unpack(buf[u][r], f);
+          } else {
+#pragma unroll
+            for (int i = 0; i < NV; ++i) f[i] = 0.f;
+          }
+#pragma unroll
+          for (int i = 0; i < NV; ++i) acc[i] = fmaf(wts[r], f[i], acc[i]);
         }
-#pragma unroll
-        for (int i = 0; i < NV; ++i) acc[i] = fmaf(wts[r], f[i], acc[i]);
+        __stcs(y + t * row_vecs + v, Vec<T>::pack(acc));
       }
-      __stcs(y + t * row_vecs + v, Vec<T>::pack(acc));
     }
   }
 }
