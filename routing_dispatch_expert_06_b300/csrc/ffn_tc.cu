@@ -22,6 +22,16 @@
 //     than shared memory delivers) and leaves room for 6 stages at BN = 256.
 //   PAIR = false: one CTA per tile, tcgen05.mma.cta_group::1, M = 128.
 //
+// With many experts (E >= kTailSplitMinExperts) a GEMM is two launches: CTA
+// pairs take each expert's whole 256-row tiles (and a last one holding more
+// than 128 rows), and one-CTA tiles take the 1..128 rows left at the end of
+// an expert.  A pair tile whose upper half lies past the expert's end spends
+// half of its MMA work on rows that are not stored (1.31x the kept rows on the
+// E = 256 layer, against 1.15x for 128-row tiles).  The tail launch uses
+// programmatic dependent launch: it may start as soon as the pair launch is
+// running, its CTAs take the SMs that pair CTAs leave, and it waits for the
+// pair launch before it completes.
+//
 //   warp 0     TMA producer: 128×64 A tile + (BN or BN/2)×64 B tile per stage,
 //              128-byte swizzle, a ring of as many stages as fit
 //   warp 1     TMEM allocator and (in the even CTA of a pair) MMA issuer:
@@ -62,17 +72,39 @@ constexpr uint32_t kTmemCols = 512;
 constexpr int kAccCols = 256;           // each of the two accumulators owns 256 columns
 constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s
 constexpr int kMaxExperts = 1024;
+// Experts from which a GEMM splits each expert's 1..128-row tail off to
+// one-CTA tiles.  Measured: with E = 256 the split saves 9% of the GEMM time;
+// with E = 8 or 64 the few long-K tail tiles land on the critical path and
+// it cost 3-15%.
+constexpr int kTailSplitMinExperts = 128;
 enum { kActNone = -1 };
 
 struct TileCoord {
   int e, m0, m_end, n0;
 };
 
+// Which of an expert's row tiles a launch covers.
+enum TileSet {
+  kAllTiles = 0,    // every 128-row tile (one CTA) or 256-row tile (a pair)
+  kPairBody = 1,    // pairs: whole 256-row tiles, and a last one with > 128 rows
+  kTail = 2,        // one CTA: the expert's last rows when 1..128 remain after
+                    // its whole 256-row tiles
+};
+
+// Row tiles of an expert with `rows` rows in the given set (rows_per_tile:
+// 128 for one CTA, 256 for a pair).
+__device__ __forceinline__ int tiles_in_set(int rows, int set, int rows_per_tile) {
+  if (rows <= 0) return 0;
+  if (set == kPairBody) return rows / 256 + (rows % 256 > 128 ? 1 : 0);
+  if (set == kTail) return (rows % 256 != 0 && rows % 256 <= 128) ? 1 : 0;
+  return (rows + rows_per_tile - 1) / rows_per_tile;
+}
+
 // Tile i of the expert-major order.  rows_per_tile = 128 (one CTA) or 256
 // (a CTA pair; `rank` selects the pair's lower or upper 128 rows).
 __device__ __forceinline__ TileCoord tile_coord(int64_t i, const int* mt_prefix, int E, int n_tn,
                                                 const int32_t* offsets_s, int BN,
-                                                int rows_per_tile, int rank) {
+                                                int rows_per_tile, int rank, int set) {
   // Find e with mt_prefix[e]*n_tn <= i < mt_prefix[e+1]*n_tn.
   int lo = 0, hi = E;  // invariant: prefix[lo]*n_tn <= i < prefix[hi]*n_tn
   while (hi - lo > 1) {
@@ -88,7 +120,9 @@ __device__ __forceinline__ TileCoord tile_coord(int64_t i, const int* mt_prefix,
   const int nt = int(local / mts), mt = int(local % mts);
   TileCoord c;
   c.e = e;
-  c.m0 = offsets_s[e] + mt * rows_per_tile + rank * kTileM;
+  // A tail tile starts after the expert's whole 256-row tiles.
+  const int tail0 = set == kTail ? ((offsets_s[e + 1] - offsets_s[e]) / 256) * 256 : 0;
+  c.m0 = offsets_s[e] + tail0 + mt * rows_per_tile + rank * kTileM;
   c.m_end = offsets_s[e + 1] > offsets_s[e] ? offsets_s[e + 1] : offsets_s[e];
   c.n0 = nt * BN;
   return c;
@@ -107,7 +141,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    int E, int N, int K, int BN, const int32_t* __restrict__ offsets,
                    const float* __restrict__ bias, __nv_bfloat16* __restrict__ out,
-                   int64_t max_rows, int32_t* status, int stages) {
+                   int64_t max_rows, int32_t* status, int stages, int set) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages];
   __shared__ uint64_t tfull_bar[2], tempty_bar[2], drain_bar;
@@ -171,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int e = lo; e < hi; ++e) {
       const int32_t a = clamp_row(e), b = clamp_row(e + 1);
       s_off[e] = a;
-      run += b > a ? (b - a + rows_per_tile - 1) / rows_per_tile : 0;
+      run += tiles_in_set(b - a, set, rows_per_tile);
     }
     if (lane == 31) s_off[E] = clamp_row(E);
     int incl = run;
@@ -184,7 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int e = lo; e < hi; ++e) {
       s_mt[e] = acc;
       const int32_t a = clamp_row(e), b = clamp_row(e + 1);
-      acc += b > a ? (b - a + rows_per_tile - 1) / rows_per_tile : 0;
+      acc += tiles_in_set(b - a, set, rows_per_tile);
     }
     if (lane == 31) s_mt[E] = incl;
   }
@@ -192,6 +226,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem_base = s_tmem;
+  // The pair launch lets the tail launch start early: its CTAs take SMs as
+  // pair CTAs finish (the tiles are independent).
+  if (set == kPairBody && threadIdx.x == 0) tc::grid_launch_dependents();
 
   const int n_tn = (N + BN - 1) / BN;
   const int64_t total = int64_t(s_mt[E]) * n_tn;
@@ -212,7 +249,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     int64_t issued = 0;
     bool ok = true;
     for (int64_t i = first_tile; i < total && ok; i += tile_step) {
-      const TileCoord c = tile_coord(i, s_mt, E, n_tn, s_off, BN, rows_per_tile, int(rank));
+      const TileCoord c =
+          tile_coord(i, s_mt, E, n_tn, s_off, BN, rows_per_tile, int(rank), set);
       for (int kb = 0; kb < nk; ++kb) {
         if (!tc::mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, kWaitLimitNs)) {
           give_up();
@@ -311,7 +349,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int64_t i = first_tile; i < total; i += tile_step) {
-      const TileCoord c = tile_coord(i, s_mt, E, n_tn, s_off, BN, rows_per_tile, int(rank));
+      const TileCoord c =
+          tile_coord(i, s_mt, E, n_tn, s_off, BN, rows_per_tile, int(rank), set);
       // The tensor-memory loads below are warp-collective: the whole warp
       // takes the same branch.
       if (!__all_sync(0xffffffffu, tc::mbar_wait(&tfull_bar[acc], acc_phase, abort_flag,
@@ -401,6 +440,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     else
       tc::tmem_dealloc(tmem_base, kTmemCols);
   }
+  // A tail launch that started early does not finish before the pair launch
+  // it overlapped: work after it in the stream sees every tile.
+  if (set == kTail) tc::grid_dependency_wait();
 }
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -443,7 +485,7 @@ bool use_pair() {
 template <bool PAIR>
 cudaError_t launch_variant(int act, const CUtensorMap& tmA, const CUtensorMap& tmB, int E, int N,
                            int K, int BN, const int32_t* offsets, const float* bias, void* out,
-                           int64_t max_rows, int32_t* status, cudaStream_t st) {
+                           int64_t max_rows, int32_t* status, int set, cudaStream_t st) {
   const int sms = device_sms();
   const size_t static_smem =
       kernel_static_smem(reinterpret_cast<const void*>(gemm_tc_kernel<kActNone, PAIR>));
@@ -466,6 +508,12 @@ cudaError_t launch_variant(int act, const CUtensorMap& tmA, const CUtensorMap& t
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
+    if (set == kTail) {
+      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[0].val.programmaticStreamSerializationAllowed = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+    }
     if constexpr (PAIR) {
       // Persistent grid: as many CTA pairs as can be resident at once.
       attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -483,7 +531,7 @@ cudaError_t launch_variant(int act, const CUtensorMap& tmA, const CUtensorMap& t
     }
     cfg.gridDim = dim3(grid);
     e = cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, E, N, K, BN, offsets, bias,
-                           static_cast<__nv_bfloat16*>(out), max_rows, status, stages);
+                           static_cast<__nv_bfloat16*>(out), max_rows, status, stages, set);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
   };
@@ -502,7 +550,7 @@ cudaError_t launch_gemm_tc(int E, int N, int K, int64_t max_rows, const int32_t*
   if (!encode) return cudaErrorNotSupported;
   const int BN = pick_bn(N);
   const bool pair = use_pair();
-  CUtensorMap tmA, tmB;
+  CUtensorMap tmA;
   {
     const cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(max_rows)};
     const cuuint64_t strides[1] = {cuuint64_t(K) * 2};
@@ -514,21 +562,41 @@ cudaError_t launch_gemm_tc(int E, int N, int K, int64_t max_rows, const int32_t*
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  {
+  // B tiles of BN rows (one CTA) or BN/2 rows (each CTA of a pair).
+  auto encode_b = [&](CUtensorMap* m, int box_rows) {
     const cuuint64_t dims[3] = {cuuint64_t(K), cuuint64_t(N), cuuint64_t(E)};
     const cuuint64_t strides[2] = {cuuint64_t(K) * 2, cuuint64_t(N) * K * 2};
-    const cuuint32_t box[3] = {kTileK, cuuint32_t(pair ? BN / 2 : BN), 1};
+    const cuuint32_t box[3] = {kTileK, cuuint32_t(box_rows), 1};
     const cuuint32_t es[3] = {1, 1, 1};
-    if (encode(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(B), dims, strides, box,
-               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
+    return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(B), dims, strides,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  };
+  CUtensorMap tmB_cta;
+  if (!encode_b(&tmB_cta, BN)) return cudaErrorInvalidValue;
+  cudaError_t err;
+  if (pair && E >= kTailSplitMinExperts) {
+    // CTA pairs take every expert's whole 256-row tiles (and a last one with
+    // more than 128 rows); one-CTA tiles take the remaining 1..128 rows, so
+    // no pair computes a 128-row half that lies past its expert's end.
+    CUtensorMap tmB_pair;
+    if (!encode_b(&tmB_pair, BN / 2)) return cudaErrorInvalidValue;
+    err = launch_variant<true>(act, tmA, tmB_pair, E, N, K, BN, offsets, bias, out, max_rows,
+                               status, kPairBody, st);
+    if (err != cudaSuccess) return err;
+    count_launch();
+    err = launch_variant<false>(act, tmA, tmB_cta, E, N, K, BN, offsets, bias, out, max_rows,
+                                status, kTail, st);
+  } else if (pair) {
+    CUtensorMap tmB_pair;
+    if (!encode_b(&tmB_pair, BN / 2)) return cudaErrorInvalidValue;
+    err = launch_variant<true>(act, tmA, tmB_pair, E, N, K, BN, offsets, bias, out, max_rows,
+                               status, kAllTiles, st);
+  } else {
+    err = launch_variant<false>(act, tmA, tmB_cta, E, N, K, BN, offsets, bias, out, max_rows,
+                                status, kAllTiles, st);
   }
-  cudaError_t err = pair ? launch_variant<true>(act, tmA, tmB, E, N, K, BN, offsets, bias, out,
-                                                max_rows, status, st)
-                         : launch_variant<false>(act, tmA, tmB, E, N, K, BN, offsets, bias, out,
-                                                 max_rows, status, st);
   if (err != cudaSuccess) return err;
   count_launch();
   return cudaSuccess;

@@ -105,6 +105,18 @@ __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* m, int32_t x,
                : "memory");
 }
 
+// ---- programmatic dependent launch ---------------------------------------------
+// Let the next kernel in the stream (launched with programmatic stream
+// serialisation) start once every CTA of this grid has signalled or exited.
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Wait until the preceding grid in the stream has completed and its memory
+// operations are visible.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---- clusters and CTA pairs ---------------------------------------------------
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;

@@ -142,3 +142,25 @@ def test_forward_replays_from_a_cuda_graph():
         assert torch.equal(out_e[name], out_g[name]), name
     for name in ["row_token", "xd", "H", "yd"]:
         assert torch.equal(out_e[name][:n], out_g[name][:n]), name
+
+
+def test_pair_body_and_tail_tiles_match_one_sm_gemm():
+    # With E >= 128 each GEMM runs CTA pairs on whole 256-row tiles and a
+    # second, overlapped one-CTA launch on every expert's last 1..128 rows.
+    # Small ragged experts cover every case: no rows, < 128, 128 exactly,
+    # 129..255, whole pairs plus a tail of each size.
+    wl = W["bf16_t32768_d7168_e256_top8"].replace(T=12000, d=256, d_ff=512, capacity_factor=2.0)
+    _, inp, out_p, _ = run_gpu(wl, expert_bias=True)
+    rows = np.diff(h(out_p["offsets"]))
+    assert (rows % 256 > 128).any() and ((rows % 256 > 0) & (rows % 256 <= 128)).any()
+    os.environ["MOE_GEMM_PAIR"] = "0"
+    try:
+        _, _, out_1, _ = run_gpu(wl, inp=inp)
+    finally:
+        del os.environ["MOE_GEMM_PAIR"]
+    n = int(h(out_p["offsets"])[-1])
+    for name in ["H", "yd", "y"]:
+        m = n if name != "y" else wl.T
+        a = out_p[name][:m].float()
+        b = out_1[name][:m].float()
+        assert ((a - b).abs() <= 1e-2 + 2e-2 * b.abs()).all(), name
