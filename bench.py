@@ -364,6 +364,7 @@ def main():
 
     offsets = out["offsets"].cpu()
     n_kept = int(offsets[-1])
+    touched = int((out["kept"].cpu() > 0).sum())
     slot = out["slot_row"].cpu()
     t_kept = int((slot >= 0).any(dim=1).sum())
     alg = algorithmic(wl, n_kept, t_kept)
@@ -445,6 +446,10 @@ def main():
         route_gbs=alg["route_bytes"] / (mean["route"] * 1e-3) / 1e9,
         hbm_peak_gbs=peaks["hbm"],
         kept_rows=n_kept,
+        experts_touched=touched,
+        # With few rows per expert the grouped FFN is bound by reading the
+        # touched experts' W1 and W2: their bytes over the FFN time.
+        ffn_weight_gbs=touched * 2 * wl.d * wl.d_ff * b / (ffn_ms * 1e-3) / 1e9,
     )
     print(json.dumps(line), flush=True)
     if dist is not None:

@@ -56,6 +56,16 @@ WORKLOADS = {
                  "bf16", 3, "zipf:0.8"),
         Workload("bf16_t32768_d7168_e256_top8", 32768, 7168, 2048, 256, 8, 1.25, False,
                  "gelu_tanh", "bf16", 4, "normal:1.0"),
+        # Decode regime: a few tokens per call on the two many-expert layers;
+        # the expert FFN is then bound by reading the touched experts' weights.
+        Workload("decode_bf16_t8_d7168_e256_top8", 8, 7168, 2048, 256, 8, 1.25, False,
+                 "gelu_tanh", "bf16", 6, "normal:1.0"),
+        Workload("decode_bf16_t64_d2048_e64_top6", 64, 2048, 1408, 64, 6, 1.0, True,
+                 "gelu_tanh", "bf16", 7, "zipf:0.8"),
+        # Dropless: c = E/k makes C = ceil(c·T·k/E) = T, so no expert can
+        # overflow (every slot is kept).
+        Workload("dropless_bf16_t8192_d2048_e64_top6", 8192, 2048, 1408, 64, 6, 64 / 6, True,
+                 "gelu_tanh", "bf16", 8, "zipf:0.8"),
     ]
 }
 

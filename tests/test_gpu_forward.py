@@ -164,3 +164,23 @@ def test_pair_body_and_tail_tiles_match_one_sm_gemm():
         a = out_p[name][:m].float()
         b = out_1[name][:m].float()
         assert ((a - b).abs() <= 1e-2 + 2e-2 * b.abs()).all(), name
+
+
+@pytest.mark.parametrize("name", ["decode_bf16_t8_d7168_e256_top8",
+                                  "decode_bf16_t64_d2048_e64_top6"])
+def test_decode_regime(name):
+    # A few tokens per call on the many-expert layers: every output is checked.
+    wl = W[name]
+    _, inp, out, _ = run_gpu(wl)
+    check_forward(wl, inp, out, full=True)
+
+
+def test_dropless_capacity_keeps_every_slot():
+    # c = E/k gives C = T: no expert can overflow, so every slot is kept and
+    # the buffer holds all T·k rows.
+    wl = W["dropless_bf16_t8192_d2048_e64_top6"]
+    _, inp, out, _ = run_gpu(wl)
+    assert (h(out["slot_row"]) >= 0).all()
+    np.testing.assert_array_equal(h(out["counts"]), h(out["kept"]))
+    assert int(h(out["offsets"])[-1]) == wl.T * wl.k
+    check_forward(wl, inp, out, e2e_tokens=64)
