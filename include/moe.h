@@ -116,22 +116,25 @@ int64_t moe_capacity(const moe_config_t* cfg);
 /* Rows of the dispatch buffer to allocate: min(T·k, E·C).  -1 if invalid. */
 int64_t moe_max_rows(const moe_config_t* cfg);
 
-/* Bytes of scratch workspace the stage calls need (1 KiB header with the
- * status word and completion counters, per-chunk histograms, per-block
- * probability partial sums, and for small T the router's per-split partial
- * logits).  Host only.  A workspace serves one stream at a time. */
+/* Bytes of scratch workspace the stage calls need (80 KiB header with the
+ * status word, completion counters and the router's fixed-point column-sum
+ * accumulators; per-chunk histograms; per-block probability partial sums; the
+ * tensor-core router's fp32 partial logits, nsplit·T·E floats, nsplit > 1 only
+ * for small T).  Host only.  A workspace serves one stream at a time. */
 moe_status_t moe_workspace_size(const moe_config_t* cfg, size_t* bytes);
 
-/* Clear the workspace's 1 KiB header: the device status word and the
- * counters the kernels use to find the last block of a grid (enqueued on
- * stream; kernels leave the counters at zero).  Call once after allocating a
+/* Clear the workspace's 80 KiB header: the device status word, the counters
+ * the kernels use to find the last block of a grid and the column-sum
+ * accumulators (enqueued on stream; kernels leave them at zero).  Call once after allocating a
  * workspace, and after reading a nonzero status. */
 moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, void* stream);
 
 /* [MoE 模型原理 §2.1–§2.2] Router: logits s = x W_rᵀ + b_r (fp32 accumulate),
  * softmax, top-k with ties to the lower expert index, combine weights
  * (renormalised over the selected set iff cfg->renormalize), and the column
- * sums psum[i] = Σ_t p_{t,i} in a fixed reduction order.  logits may be NULL
+ * sums psum[i] = Σ_t p_{t,i}, deterministic: a fixed reduction order, or (the
+ * tensor-core router) per-token p (T < 1024) or sums over fixed groups of 32
+ * tokens rounded to 26 fraction bits and added exactly as 64-bit integers.  logits may be NULL
  * unless cfg->write_logits. */
 moe_status_t moe_route(const moe_config_t* cfg, const void* x, const void* Wr, const float* br,
                        float* logits, int32_t* topk_ids, float* topk_w, float* psum, void* ws,
@@ -193,7 +196,10 @@ moe_status_t moe_aux_stats(const moe_config_t* cfg, const int32_t* counts, const
 
 /* The whole layer: route, dispatch, expert FFN, combine, aux (the aux
  * statistics are computed inside the dispatch launches here, with the same
- * arithmetic and results as moe_aux_stats). */
+ * arithmetic and results as moe_aux_stats; psum is also formed there from the
+ * router's fixed-point column sums).  If it returns an error after the router
+ * was enqueued, call moe_workspace_init before the next call on that
+ * workspace. */
 moe_status_t moe_forward(const moe_config_t* cfg, const moe_tensors_t* t, float alpha, void* ws,
                          size_t ws_bytes, void* stream);
 

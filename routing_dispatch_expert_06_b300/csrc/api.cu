@@ -153,16 +153,14 @@ static WsLayout layout_of(const moe_config_t& c) {
   L.n_route_blocks = rb_simt > rb_tc ? rb_simt : rb_tc;
   size_t off = 0;
   L.status = off;
-  L.split_count = off + kWsSplitCounters;
   off += kWsHeaderBytes;
   L.chunk_counts = off;
   off += align256(size_t(L.n_chunks) * c.E * sizeof(int32_t));
   L.psum_partial = off;
   off += align256(size_t(L.n_route_blocks) * c.E * sizeof(float));
-  L.split_part = off;
-  if (route_tc_supported(c) && route_tc_nsplit(c) > 1)
-    off += align256(size_t(rb_tc) * route_tc_nsplit(c) * route_tc_np(c) * kRouteTileM *
-                    sizeof(float));
+  L.route_part = off;
+  if (route_tc_supported(c))
+    off += align256(size_t(route_tc_nsplit(c)) * size_t(c.T) * c.E * sizeof(float));
   L.total = off;
   return L;
 }
@@ -173,8 +171,8 @@ struct Ws {
   int* dispatch_counter;
   int32_t* chunk_counts;
   float* psum_partial;
-  float* split_part;
-  int* split_count;
+  float* route_part;
+  unsigned long long* psum_fixed;
 };
 
 static moe_status_t get_ws(const moe_config_t& c, void* ws, size_t ws_bytes, Ws* out) {
@@ -190,8 +188,8 @@ static moe_status_t get_ws(const moe_config_t& c, void* ws, size_t ws_bytes, Ws*
   out->dispatch_counter = reinterpret_cast<int*>(b + L.status + kWsDispatchCounter);
   out->chunk_counts = reinterpret_cast<int32_t*>(b + L.chunk_counts);
   out->psum_partial = reinterpret_cast<float*>(b + L.psum_partial);
-  out->split_part = reinterpret_cast<float*>(b + L.split_part);
-  out->split_count = reinterpret_cast<int*>(b + L.split_count);
+  out->route_part = reinterpret_cast<float*>(b + L.route_part);
+  out->psum_fixed = reinterpret_cast<unsigned long long*>(b + L.status + kWsPsumFixed);
   return MOE_OK;
 }
 
@@ -222,6 +220,51 @@ static Router pick_router(const moe_config_t& c, bool aligned) {
   return Router::kSimt;
 }
 
+}  // namespace moe
+
+namespace moe {
+// moe_route.  psum_fixed_out == NULL: psum is written before return (every
+// router).  Otherwise the tensor-core router leaves Σ_t p in the workspace's
+// fixed-point accumulators and sets *psum_fixed_out to them, for the
+// dispatch's histogram to convert (psum_from_fixed); the other routers write
+// psum and set it to NULL.
+static moe_status_t route_impl(const moe_config_t* cfg, const void* x, const void* Wr,
+                               const float* br, float* logits, int32_t* topk_ids, float* topk_w,
+                               float* psum, void* ws, size_t ws_bytes,
+                               unsigned long long** psum_fixed_out, void* stream) {
+  moe_status_t s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  if (!x || !Wr || !br || !topk_ids || !topk_w || !psum)
+    return fail(MOE_ERR_INVALID_ARG, "moe_route: NULL tensor");
+  if (cfg->write_logits && !logits)
+    return fail(MOE_ERR_INVALID_ARG, "moe_route: write_logits set but logits is NULL");
+  Ws w;
+  if ((s = get_ws(*cfg, ws, ws_bytes, &w)) != MOE_OK) return s;
+  float* lg = cfg->write_logits ? logits : nullptr;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int* counter = w.route_counter;
+  if (psum_fixed_out) *psum_fixed_out = nullptr;
+  cudaError_t e;
+  switch (pick_router(*cfg, aligned16(x) && aligned16(Wr))) {
+    case Router::kWarp:
+      e = launch_route_warp(*cfg, x, Wr, br, lg, topk_ids, topk_w, w.psum_partial, psum, counter,
+                            st);
+      break;
+    case Router::kTc:
+      e = launch_route_tc(*cfg, x, Wr, w.route_part, w.status, st);
+      if (e == cudaSuccess)
+        e = launch_route_select(*cfg, w.route_part, route_tc_nsplit(*cfg), br, lg, topk_ids,
+                                topk_w, w.psum_fixed, psum, counter, psum_fixed_out == nullptr,
+                                st);
+      if (e == cudaSuccess && psum_fixed_out) *psum_fixed_out = w.psum_fixed;
+      break;
+    default:
+      e = launch_route_simt(*cfg, x, Wr, br, lg, topk_ids, topk_w, w.psum_partial, psum, counter,
+                            st);
+      break;
+  }
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_route");
+}
 }  // namespace moe
 
 using namespace moe;
@@ -257,33 +300,7 @@ moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, void* stream) {
 moe_status_t moe_route(const moe_config_t* cfg, const void* x, const void* Wr, const float* br,
                        float* logits, int32_t* topk_ids, float* topk_w, float* psum, void* ws,
                        size_t ws_bytes, void* stream) {
-  moe_status_t s = check_cfg(cfg);
-  if (s != MOE_OK) return s;
-  if (!x || !Wr || !br || !topk_ids || !topk_w || !psum)
-    return fail(MOE_ERR_INVALID_ARG, "moe_route: NULL tensor");
-  if (cfg->write_logits && !logits)
-    return fail(MOE_ERR_INVALID_ARG, "moe_route: write_logits set but logits is NULL");
-  Ws w;
-  if ((s = get_ws(*cfg, ws, ws_bytes, &w)) != MOE_OK) return s;
-  float* lg = cfg->write_logits ? logits : nullptr;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  int* counter = w.route_counter;
-  cudaError_t e;
-  switch (pick_router(*cfg, aligned16(x) && aligned16(Wr))) {
-    case Router::kWarp:
-      e = launch_route_warp(*cfg, x, Wr, br, lg, topk_ids, topk_w, w.psum_partial, psum, counter,
-                            st);
-      break;
-    case Router::kTc:
-      e = launch_route_tc(*cfg, x, Wr, br, lg, topk_ids, topk_w, w.psum_partial, psum, counter,
-                          w.status, w.split_part, w.split_count, st);
-      break;
-    default:
-      e = launch_route_simt(*cfg, x, Wr, br, lg, topk_ids, topk_w, w.psum_partial, psum, counter,
-                            st);
-      break;
-  }
-  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_route");
+  return route_impl(cfg, x, Wr, br, logits, topk_ids, topk_w, psum, ws, ws_bytes, nullptr, stream);
 }
 
 }  // extern "C"
@@ -401,12 +418,14 @@ moe_status_t moe_forward(const moe_config_t* cfg, const moe_tensors_t* t, float 
   if (!t->f || !t->pbar || !t->l_aux)
     return fail(MOE_ERR_INVALID_ARG, "moe_aux_stats: NULL tensor");
   moe_status_t s;
-  if ((s = moe_route(cfg, t->x, t->Wr, t->br, t->logits, t->topk_ids, t->topk_w, t->psum, ws,
-                     ws_bytes, stream)) != MOE_OK)
+  unsigned long long* psum_fixed = nullptr;
+  if ((s = route_impl(cfg, t->x, t->Wr, t->br, t->logits, t->topk_ids, t->topk_w, t->psum, ws,
+                      ws_bytes, &psum_fixed, stream)) != MOE_OK)
     return s;
   // The statistics need only counts and psum: the dispatch's last histogram
-  // block computes them (same arithmetic as moe_aux_stats), saving a launch.
-  const AuxArgs aux{alpha, t->psum, t->f, t->pbar, t->l_aux};
+  // block computes them (same arithmetic as moe_aux_stats), saving a launch;
+  // with the tensor-core router it first forms psum from the fixed-point sums.
+  const AuxArgs aux{alpha, t->psum, t->f, t->pbar, t->l_aux, psum_fixed};
   if ((s = dispatch_impl(cfg, t->x, t->topk_ids, t->counts, t->kept, t->offsets, t->slot_row,
                          t->row_token, t->xd, ws, ws_bytes, &aux, stream)) != MOE_OK)
     return s;

@@ -25,20 +25,25 @@ struct WsLayout {
   size_t status;        // int32 status word
   size_t chunk_counts;  // int32 [n_chunks, E]: histogram, then chunk bases in place
   size_t psum_partial;  // fp32 [n_route_blocks, E]
-  size_t split_part;    // fp32 [n_tiles, nsplit, NP, 128] (tensor-core router, nsplit > 1)
-  size_t split_count;   // int32 [n_tiles], zeroed
+  size_t route_part;    // fp32 [nsplit, T, E] partial logits (tensor-core router)
   size_t total;
   int64_t n_chunks;
   int64_t n_route_blocks;
 };
 
-// The workspace starts with a 1 KiB header that moe_workspace_init clears:
-// the status word, grid-completion counters, and the per-tile arrival
-// counters of the split router (every kernel leaves them at zero).
-constexpr size_t kWsHeaderBytes = 1024;
+// The workspace starts with an 80 KiB header that moe_workspace_init clears:
+// the status word, grid-completion counters, and the router's fixed-point
+// column-sum accumulators (every kernel leaves them at zero).
+constexpr int kPsumReplicas = 32;       // copies of the accumulator, spread over L2
+constexpr int kPsumFixedMaxE = 256;
 constexpr size_t kWsRouteCounter = 64;
 constexpr size_t kWsDispatchCounter = 128;
-constexpr size_t kWsSplitCounters = 256;  // int32 [n_tiles] for n_tiles <= 192
+constexpr size_t kWsPsumFixed = 16384;  // uint64 [kPsumReplicas][kPsumFixedMaxE]
+constexpr size_t kWsHeaderBytes =
+    kWsPsumFixed + size_t(kPsumReplicas) * kPsumFixedMaxE * sizeof(unsigned long long);
+// Column sums Σ_t p are kept as integers: p rounded to 31 fraction bits.
+constexpr float kPsumFixScale = 2147483648.0f;  // 2^31: p <= 1 fits in 32 bits
+constexpr double kPsumFixInv = 1.0 / 2147483648.0;
 
 // Called by every thread of every block once its results are written.
 // Returns true in exactly one block, the last to arrive, after which that
@@ -98,14 +103,30 @@ __device__ __forceinline__ void aux_stats_block(int E, int64_t T, float alpha,
   if (j == 0) *l_aux = __fmul_rn(__fmul_rn(alpha, float(E)), red[0]);
 }
 
+// psum[c] = (Σ over the kPsumReplicas copies of fixed[c]) / 2^31 for c < E,
+// and the copies return to zero; threads of one block stride over c.  Called
+// by one block after every block that added into the copies has finished.
+__device__ __forceinline__ void psum_from_fixed(int E, unsigned long long* fixed, float* psum) {
+  for (int c = threadIdx.x; c < E; c += blockDim.x) {
+    unsigned long long fx = 0;
+#pragma unroll 8
+    for (int r = 0; r < kPsumReplicas; ++r) fx += __ldcg(fixed + r * kPsumFixedMaxE + c);
+#pragma unroll 8
+    for (int r = 0; r < kPsumReplicas; ++r) __stcg(fixed + r * kPsumFixedMaxE + c, 0ull);
+    psum[c] = float(double(fx) * kPsumFixInv);
+  }
+}
+
 // Aux-statistics outputs for the dispatch's last histogram block (forward
-// pass only).
+// pass only).  psum_fixed: when set, psum is first formed from the router's
+// fixed-point column sums (psum_from_fixed).
 struct AuxArgs {
   float alpha;
-  const float* psum;
+  float* psum;
   float* f;
   float* pbar;
   float* l_aux;
+  unsigned long long* psum_fixed;
 };
 
 // Record the first asynchronous error in the status word.

@@ -106,6 +106,7 @@ __global__ void __launch_bounds__(kDispatchThreads)
   if (counter && last_block_to_finish(counter, &s_last)) {
     scan_chunks_by_expert(gridDim.x, E, C, chunk_counts, counts, kept);
     if (aux.f) {
+      if (aux.psum_fixed) psum_from_fixed(E, aux.psum_fixed, aux.psum);
       __syncthreads();
       aux_stats_block(E, T, aux.alpha, counts, aux.psum, aux.f, aux.pbar, aux.l_aux, s_red);
     }
@@ -279,7 +280,8 @@ cudaError_t launch_dispatch(const moe_config_t& c, int64_t C, const void* x,
                             int32_t* chunk_counts, int32_t* status, int* counter,
                             const AuxArgs* aux, cudaStream_t st) {
   const int64_t n_chunks = (c.T + kChunkTokens - 1) / kChunkTokens;
-  const AuxArgs aux_v = (aux && counter) ? *aux : AuxArgs{0.f, nullptr, nullptr, nullptr, nullptr};
+  const AuxArgs aux_v =
+      (aux && counter) ? *aux : AuxArgs{0.f, nullptr, nullptr, nullptr, nullptr, nullptr};
   cudaError_t err;
   histogram_kernel<<<unsigned(n_chunks), kDispatchThreads, size_t(c.E) * 4, st>>>(
       c.T, c.E, c.k, ids, chunk_counts, status, counter, C, counts, kept, aux_v);

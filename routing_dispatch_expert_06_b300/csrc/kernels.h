@@ -49,10 +49,18 @@ cudaError_t launch_route_warp(const moe_config_t& c, const void* x, const void* 
 bool route_tc_supported(const moe_config_t& c);
 int route_tc_nsplit(const moe_config_t& c);
 int route_tc_np(const moe_config_t& c);
-cudaError_t launch_route_tc(const moe_config_t& c, const void* x, const void* Wr,
-                            const float* br, float* logits, int32_t* ids, float* w,
-                            float* psum_partial, float* psum, int* counter, int32_t* status,
-                            float* split_part, int* split_count, cudaStream_t st);
+// Partial router logits part[split][t][e] = Σ_{d in split} x[t,d]·W_r[e,d]
+// (fp32, no bias), nsplit = route_tc_nsplit(c) splits.
+cudaError_t launch_route_tc(const moe_config_t& c, const void* x, const void* Wr, float* part,
+                            int32_t* status, cudaStream_t st);
+// Softmax, top-k, weights, optional logits and Σ_t p from the partial logits
+// (E <= 256); programmatic dependent launch after launch_route_tc.  finish:
+// the last block writes psum from the fixed-point sums (else psum_from_fixed
+// must run later, before psum_fixed is used again).
+cudaError_t launch_route_select(const moe_config_t& c, const float* part, int nsplit,
+                                const float* br, float* logits, int32_t* ids, float* w,
+                                unsigned long long* psum_fixed, float* psum, int* counter,
+                                bool finish, cudaStream_t st);
 
 // Dispatch: histogram per chunk, per-expert scan + capacity, positions, row
 // copy.  counter: a zeroed int for the histogram's grid-completion count (the

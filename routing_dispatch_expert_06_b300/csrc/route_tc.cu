@@ -1,17 +1,16 @@
-// Router on the sm_103a tensor cores: logits by tcgen05 MMA into tensor
-// memory, then softmax, top-k, combine weights and per-tile probability
-// column sums in the epilogue, all in one persistent kernel.
+// Router logits on the sm_103a tensor cores: s = x W_rᵀ by tcgen05 MMA into
+// tensor memory, reduced over d in fp32 and written as partial logits; the
+// softmax, top-k, weights and column sums run in route_select_kernel
+// (route_select.cu), which reads them.
 //
-// [MoE 模型原理 §2.1] s_t = W_r x_t + b_r, p_t = softmax(s_t);
-// [MoE 模型原理 §2.2] S_t = TopK(p_t, k), p̃ = p/Σ_{S_t} p (or raw p);
-// [MoE 模型原理 §3.2] the column sums Σ_t p_{t,i} feed p̄_i.
+// [MoE 模型原理 §2.1] s_t = W_r x_t + b_r (the bias is added by the select
+// kernel).
 //
-// Tiles of 128 tokens.  When there are few tiles (small T), nsplit CTAs
-// share one tile's reduction over d: each takes a contiguous run of its
-// segments, writes its fp32 partial logits to a workspace buffer, and the
-// last split of the tile to arrive adds the splits in split order (so the
-// result does not depend on which CTA arrives last) and finishes the tile.
-// A CTA walks units (tile, split) b, b + grid, ...  Warps:
+// Tiles of 128 tokens.  When there are few tiles (small T), nsplit CTAs share
+// one tile's reduction over d: each takes a contiguous run of its segments and
+// writes its own fp32 partial logits, part[split][t][e]; the select kernel
+// adds the splits in split order, so the result does not depend on which CTA
+// runs first.  A CTA walks units (tile, split) b, b + grid, ...  Warps:
 //   warp 0     TMA producer: x tile [128 × 64] and W_r tile [NP × 64] per
 //              stage (NP = E rounded up to a power of two >= 32; rows past E
 //              and columns past d arrive as zeros from the copy engine's
@@ -28,16 +27,11 @@
 // into fp32 registers while the MMA fills the other buffer.  Short chains over
 // small partial sums keep the logits close to the exact dot product.
 //
-// After the last segment of a tile the epilogue has the logits in registers:
-// bias, logits out, max and a sorted top-k list per column group, merged
-// pairwise through shared memory, lower columns first (ties go to the lower
-// expert index: insertion into a sorted list that only a strictly larger
-// value passes, and higher indices are always inserted later), then
-// Σ exp, weights, and the tile's column sums of p by a transposing warp
-// butterfly; the last CTA to finish adds the tiles' column sums in tile
-// order (deterministic).  Every wait is bounded (4 s); on a timeout the kernel records
-// MOE_ERR_TIMEOUT, drains its copies and MMAs, frees its tensor memory and
-// returns.
+// After a unit's last segment each epilogue thread stores its row's NP/G sums
+// (16-byte stores; a row's columns are contiguous) while the MMA already runs
+// the next unit into the other buffer.  Every wait is bounded (4 s); on a
+// timeout the kernel records MOE_ERR_TIMEOUT, drains its copies and MMAs,
+// frees its tensor memory and returns.
 #include "common.cuh"
 #include "kernels.h"
 #include "tc.cuh"
@@ -59,65 +53,26 @@ constexpr int epi_threads() { return 128 * G; }
 
 struct RouteTcArgs {
   int64_t T;
-  int d, E, NP, k, renorm, stages;
+  int d, E, NP, stages;
   uint32_t tmem_cols;
-  const float* br;
-  float* logits;
-  int32_t* ids;
-  float* w;
-  float* psum_partial;
-  float* psum;
-  int* counter;
+  int nsplit;        // CTAs sharing one tile's reduction over d
+  float* part;       // [nsplit][T][E] fp32 partial logits (no bias)
   int32_t* status;
-  int nsplit;             // CTAs sharing one tile's reduction over d
-  float* split_part;      // [n_tiles][nsplit][NP][128] partial logits (nsplit > 1)
-  int* split_count;       // [n_tiles] zeroed arrival counters (nsplit > 1)
 };
 
-template <int G>
-__device__ __forceinline__ void bar_epi() {
-  asm volatile("bar.sync 1, %0;" ::"n"(epi_threads<G>()) : "memory");
-}
-
-// Insert (v, i) into a list sorted by descending value; only a strictly
-// larger value moves past an entry, so among equal values the one inserted
-// first (the lower expert index) stays ahead.
-template <int KMAX>
-__device__ __forceinline__ void topk_insert(float* tv, int* ti, float v, int i) {
-#pragma unroll
-  for (int r = 0; r < KMAX; ++r) {
-    const bool gt = v > tv[r];
-    const float ov = tv[r];
-    const int oi = ti[r];
-    tv[r] = gt ? v : ov;
-    ti[r] = gt ? i : oi;
-    v = gt ? ov : v;
-    i = gt ? oi : i;
-  }
-}
-
 // NPG = NP / G columns per epilogue thread.
-template <int NPG, int G, int KMAX>
+template <int NPG, int G>
 __global__ void __launch_bounds__(64 + 128 * G, 1)
     route_tc_kernel(const __grid_constant__ CUtensorMap tmX,
                     const __grid_constant__ CUtensorMap tmW, const RouteTcArgs a) {
   constexpr int NP = G * NPG;
-  constexpr int CH = NPG < 32 ? 16 : 32;  // columns per tensor-memory load
+  constexpr int CH = 16;  // columns per tensor-memory load
   constexpr int kEpiThreads = epi_threads<G>();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages];
   __shared__ uint64_t tfull_bar[2], tempty_bar[2], drain_bar;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
-  __shared__ float s_bias[NP];
-  __shared__ float s_red[4][NP];
-  __shared__ float s_M[kTileM], s_invz[kTileM];
-  __shared__ float s_gz[G - 1][kTileM];
-  __shared__ float s_xmax[G / 2][kTileM];
-  __shared__ float s_xtv[G / 2][KMAX][kTileM];
-  __shared__ int s_xti[G / 2][KMAX][kTileM];
-  __shared__ int s_last;
-  __shared__ int s_last_cta;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -152,7 +107,6 @@ __global__ void __launch_bounds__(64 + 128 * G, 1)
     tc::prefetch_tmap(&tmX);
     tc::prefetch_tmap(&tmW);
   }
-  for (int e = threadIdx.x; e < NP; e += blockDim.x) s_bias[e] = e < a.E ? a.br[e] : 0.f;
   if (warp == 1) {
     tc::tmem_alloc(&s_tmem, a.tmem_cols);
     tc::tmem_relinquish();
@@ -247,15 +201,12 @@ __global__ void __launch_bounds__(64 + 128 * G, 1)
     const int row = quarter * 32 + lane;
     const int E = a.E;
     const int col0 = g * NPG;
-    const int col_of_lane =
-        ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
+    const int ncol = min(NPG, E - col0);
     const uint32_t t_lane = tmem_base + (uint32_t(quarter * 32) << 16) + uint32_t(col0);
     uint32_t seg_count = 0;
     bool ok = true;
     for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
-      const int64_t tile = u / a.nsplit;
-      const int64_t t = tile * kTileM + row;
-      const bool valid = t < a.T;
+      const int64_t t = (u / a.nsplit) * kTileM + row;
       int seg_lo, seg_hi;
       seg_range(u, seg_lo, seg_hi);
       float v[NPG];
@@ -275,10 +226,7 @@ __global__ void __launch_bounds__(64 + 128 * G, 1)
 #pragma unroll
           for (int c0 = 0; c0 < NPG; c0 += CH) {
             uint32_t r[CH];
-            if constexpr (CH == 32)
-              tc::tmem_ld_x32(t_lane + buf * uint32_t(NP) + uint32_t(c0), r);
-            else
-              tc::tmem_ld_x16(t_lane + buf * uint32_t(NP) + uint32_t(c0), r);
+            tc::tmem_ld_x16(t_lane + buf * uint32_t(NP) + uint32_t(c0), r);
             tc::tmem_ld_wait();
 #pragma unroll
             for (int j = 0; j < CH; ++j) v[c0 + j] += __uint_as_float(r[j]);
@@ -287,136 +235,19 @@ __global__ void __launch_bounds__(64 + 128 * G, 1)
           tc::mbar_arrive(&tempty_bar[buf]);
         }
       }
-      if (a.nsplit > 1) {
-        // Hand this split's partial logits over; the last split of the tile to
-        // arrive adds all splits in split order and goes on, the others move
-        // to their next unit.
-        const int sp = int(u % a.nsplit);
-        float* mine = a.split_part + ((tile * a.nsplit + sp) * NP + col0) * kTileM + row;
-#pragma unroll
-        for (int j = 0; j < NPG; ++j) __stcg(mine + j * kTileM, v[j]);
-        __threadfence();
-        bar_epi<G>();
-        if (threadIdx.x == 64) {
-          const int prev = atomicAdd(a.split_count + tile, 1);
-          const bool last = prev == a.nsplit - 1;
-          if (last) atomicExch(a.split_count + tile, 0);
-          s_last = last;
-        }
-        bar_epi<G>();
-        if (!s_last) continue;
-        __threadfence();
-        const float* base = a.split_part + (tile * a.nsplit * NP + col0) * kTileM + row;
-#pragma unroll
-        for (int j = 0; j < NPG; ++j) v[j] = __ldcg(base + j * kTileM);
-        for (int s2 = 1; s2 < a.nsplit; ++s2)
-#pragma unroll
-          for (int j = 0; j < NPG; ++j) v[j] += __ldcg(base + (int64_t(s2) * NP + j) * kTileM);
-      }
-      // Logits, this group's max and top-k.
-      float gmax = -INFINITY;
-      float tv[KMAX];
-      int ti[KMAX];
-#pragma unroll
-      for (int r = 0; r < KMAX; ++r) tv[r] = -INFINITY, ti[r] = 0x7fffffff;
-#pragma unroll
-      for (int j = 0; j < NPG; ++j) {
-        const int e = col0 + j;
-        v[j] += s_bias[e];
-        if (e < E) {
-          gmax = fmaxf(gmax, v[j]);
-          topk_insert<KMAX>(tv, ti, v[j], e);
-        }
-      }
-      if (valid && ok && a.logits && col0 < E) {
-        float* lrow = a.logits + t * E + col0;
-        const int ncol = min(NPG, E - col0);
+      if (ok && t < a.T && ncol > 0) {
+        float* dst = a.part + (int64_t(u % a.nsplit) * a.T + t) * E + col0;
         if ((E & 3) == 0) {
 #pragma unroll
           for (int j = 0; j < NPG; j += 4)
             if (j < ncol)
-              *reinterpret_cast<float4*>(lrow + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+              __stcg(reinterpret_cast<float4*>(dst + j), make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]));
         } else {
 #pragma unroll
           for (int j = 0; j < NPG; ++j)
-            if (j < ncol) lrow[j] = v[j];
+            if (j < ncol) __stcg(dst + j, v[j]);
         }
       }
-      // Pairwise merges, lower columns first: at step s, group g with
-      // g % 2s == s hands its max and list to group g - s.
-#pragma unroll
-      for (int st = 1; st < G; st <<= 1) {
-        if (g % (2 * st) == st) {
-          const int slot = g / (2 * st);
-          s_xmax[slot][row] = gmax;
-#pragma unroll
-          for (int r = 0; r < KMAX; ++r) s_xtv[slot][r][row] = tv[r], s_xti[slot][r][row] = ti[r];
-        }
-        bar_epi<G>();
-        if (g % (2 * st) == 0) {
-          const int slot = g / (2 * st);
-          gmax = fmaxf(gmax, s_xmax[slot][row]);
-#pragma unroll
-          for (int r = 0; r < KMAX; ++r)
-            topk_insert<KMAX>(tv, ti, s_xtv[slot][r][row], s_xti[slot][r][row]);
-        }
-        bar_epi<G>();
-      }
-      if (g == 0) s_M[row] = gmax;
-      bar_epi<G>();
-      const float M = s_M[row];
-      float z = 0.f;
-#pragma unroll
-      for (int j = 0; j < NPG; ++j)
-        if (col0 + j < E) z += expf(v[j] - M);
-      if (g > 0) s_gz[g - 1][row] = z;
-      bar_epi<G>();
-      if (g == 0) {
-#pragma unroll
-        for (int j = 0; j < G - 1; ++j) z += s_gz[j][row];
-        const float inv_z = 1.f / z;
-        s_invz[row] = inv_z;
-        if (valid && ok) {
-          float sel = 0.f;
-#pragma unroll
-          for (int r = 0; r < KMAX; ++r)
-            if (r < a.k) sel += expf(tv[r] - M);
-          const float inv = a.renorm ? 1.f / sel : inv_z;
-#pragma unroll
-          for (int r = 0; r < KMAX; ++r)
-            if (r < a.k) {
-              a.ids[t * a.k + r] = ti[r];
-              a.w[t * a.k + r] = expf(tv[r] - M) * inv;
-            }
-        }
-      }
-      bar_epi<G>();
-      // Column sums of p over the tile: per warp a transposing butterfly over
-      // 16 columns at a time (lane L, L even, ends with column col_of_lane),
-      // then the four lane quarters in order.
-      const float inv_z = s_invz[row];
-#pragma unroll
-      for (int c0 = 0; c0 < NPG; c0 += 16) {
-        float p[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-          p[j] = (valid && ok && col0 + c0 + j < E) ? expf(v[c0 + j] - M) * inv_z : 0.f;
-#pragma unroll
-        for (int half = 8, o = 16; half >= 1; half >>= 1, o >>= 1) {
-          const bool upper = (lane & o) != 0;
-#pragma unroll
-          for (int j = 0; j < half; ++j) {
-            const float send = upper ? p[j] : p[j + half];
-            const float keep = upper ? p[j + half] : p[j];
-            p[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-          }
-        }
-        p[0] += __shfl_xor_sync(0xffffffffu, p[0], 1);
-        if ((lane & 1) == 0) s_red[quarter][col0 + c0 + col_of_lane] = p[0];
-      }
-      bar_epi<G>();
-      for (int e = threadIdx.x - 64; e < E; e += kEpiThreads)
-        a.psum_partial[tile * E + e] = ((s_red[0][e] + s_red[1][e]) + s_red[2][e]) + s_red[3][e];
     }
   }
   tc::fence_before_sync();
@@ -426,9 +257,9 @@ __global__ void __launch_bounds__(64 + 128 * G, 1)
     __syncwarp();
     tc::tmem_dealloc(tmem_base, a.tmem_cols);
   }
-  // The last CTA to finish adds the per-tile column sums, in tile order.
-  if (last_block_to_finish(a.counter, &s_last_cta))
-    sum_partials_rows(n_tiles, a.E, a.psum_partial, a.psum);
+  // The select kernel may be scheduled now; it waits for this grid to finish
+  // and flush before reading the partial logits.
+  tc::grid_launch_dependents();
 }
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -461,10 +292,10 @@ bool encode_2d(EncodeTiledFn encode, CUtensorMap* m, const void* base, int64_t i
          CUDA_SUCCESS;
 }
 
-template <int NPG, int G, int KMAX>
-cudaError_t launch_k(const CUtensorMap& tmX, const CUtensorMap& tmW, RouteTcArgs a,
+template <int NPG, int G>
+cudaError_t launch_g(const CUtensorMap& tmX, const CUtensorMap& tmW, RouteTcArgs a,
                      unsigned grid, cudaStream_t st) {
-  auto kernel = route_tc_kernel<NPG, G, KMAX>;
+  auto kernel = route_tc_kernel<NPG, G>;
   const void* kp = reinterpret_cast<const void*>(kernel);
   // As many stages as fit beside the kernel's static shared memory.
   const size_t stage_bytes = size_t(kTileM) * kTileK * 2 + size_t(G * NPG) * kTileK * 2;
@@ -479,16 +310,6 @@ cudaError_t launch_k(const CUtensorMap& tmX, const CUtensorMap& tmW, RouteTcArgs
   if (err != cudaSuccess) return err;
   kernel<<<grid, 64 + 128 * G, smem, st>>>(tmX, tmW, a);
   return cudaGetLastError();
-}
-
-template <int NPG, int G>
-cudaError_t launch_np(int k, const CUtensorMap& tmX, const CUtensorMap& tmW,
-                      const RouteTcArgs& a, unsigned grid, cudaStream_t st) {
-  if (k <= 1) return launch_k<NPG, G, 1>(tmX, tmW, a, grid, st);
-  if (k <= 2) return launch_k<NPG, G, 2>(tmX, tmW, a, grid, st);
-  if (k <= 4) return launch_k<NPG, G, 4>(tmX, tmW, a, grid, st);
-  if (k <= 8) return launch_k<NPG, G, 8>(tmX, tmW, a, grid, st);
-  return launch_k<NPG, G, 16>(tmX, tmW, a, grid, st);
 }
 
 }  // namespace
@@ -515,10 +336,8 @@ bool route_tc_supported(const moe_config_t& c) {
   return c.dtype == MOE_DT_BF16 && c.E <= kMaxNP && c.k <= 16;
 }
 
-cudaError_t launch_route_tc(const moe_config_t& c, const void* x, const void* Wr,
-                            const float* br, float* logits, int32_t* ids, float* w,
-                            float* psum_partial, float* psum, int* counter, int32_t* status,
-                            float* split_part, int* split_count, cudaStream_t st) {
+cudaError_t launch_route_tc(const moe_config_t& c, const void* x, const void* Wr, float* part,
+                            int32_t* status, cudaStream_t st) {
   if (!route_tc_supported(c)) return cudaErrorInvalidValue;
   EncodeTiledFn encode = get_encode();
   if (!encode) return cudaErrorNotSupported;
@@ -526,23 +345,12 @@ cudaError_t launch_route_tc(const moe_config_t& c, const void* x, const void* Wr
   a.T = c.T;
   a.d = c.d;
   a.E = c.E;
-  int NP = 32;
-  while (NP < c.E) NP <<= 1;
+  const int NP = route_tc_np(c);
   a.NP = NP;
-  a.k = c.k;
-  a.renorm = c.renormalize;
   a.tmem_cols = uint32_t(2 * NP);  // two accumulator buffers
-  a.br = br;
-  a.logits = logits;
-  a.ids = ids;
-  a.w = w;
-  a.psum_partial = psum_partial;
-  a.psum = psum;
-  a.counter = counter;
-  a.status = status;
   a.nsplit = route_tc_nsplit(c);
-  a.split_part = split_part;
-  a.split_count = split_count;
+  a.part = part;
+  a.status = status;
 
   CUtensorMap tmX, tmW;
   if (!encode_2d(encode, &tmX, x, c.d, c.T, kTileK, kTileM)) return cudaErrorInvalidValue;
@@ -552,10 +360,10 @@ cudaError_t launch_route_tc(const moe_config_t& c, const void* x, const void* Wr
   const unsigned grid = unsigned(n_units < sms ? n_units : sms);
   cudaError_t err;
   switch (NP) {
-    case 32: err = launch_np<16, 2>(c.k, tmX, tmW, a, grid, st); break;
-    case 64: err = launch_np<16, 4>(c.k, tmX, tmW, a, grid, st); break;
-    case 128: err = launch_np<32, 4>(c.k, tmX, tmW, a, grid, st); break;
-    default: err = launch_np<64, 4>(c.k, tmX, tmW, a, grid, st); break;
+    case 32: err = launch_g<16, 2>(tmX, tmW, a, grid, st); break;
+    case 64: err = launch_g<16, 4>(tmX, tmW, a, grid, st); break;
+    case 128: err = launch_g<32, 4>(tmX, tmW, a, grid, st); break;
+    default: err = launch_g<64, 4>(tmX, tmW, a, grid, st); break;
   }
   count_launch();
   return err;
