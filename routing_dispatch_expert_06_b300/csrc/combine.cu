@@ -60,15 +60,18 @@ struct Vec<float> {
 // sum unchanged).
 template <typename T, int KMAX>
 __global__ void __launch_bounds__(256)
-    combine_kernel(int64_t n_tok, int k, int64_t row_vecs, int64_t max_rows,
-                   const uint4* __restrict__ yd,
+    combine_kernel(int64_t n_tok, int k, int64_t row_vecs, int64_t n_parts, int64_t part_vecs,
+                   int64_t max_rows, const uint4* __restrict__ yd,
                    const int32_t* __restrict__ slot_row, const float* __restrict__ w,
                    uint4* __restrict__ y) {
   constexpr int NV = Vec<T>::N;
   const int lane = threadIdx.x & 31;
   const int64_t warps = int64_t(gridDim.x) * (blockDim.x >> 5);
-  for (int64_t t = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); t < n_tok;
-       t += warps) {
+  for (int64_t it = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       it < n_tok * n_parts; it += warps) {
+    const int64_t t = it / n_parts;
+    const int64_t vb = (it % n_parts) * part_vecs;
+    const int64_t ve = vb + part_vecs < row_vecs ? vb + part_vecs : row_vecs;
     int32_t my_row = lane < k ? slot_row[t * k + lane] : -1;
     if (my_row >= max_rows) my_row = -1;
     const float my_w = lane < k ? w[t * k + lane] : 0.f;
@@ -82,17 +85,17 @@ __global__ void __launch_bounds__(256)
       wts[r] = kept[r] ? __shfl_sync(0xffffffffu, my_w, r) : 0.f;
       src[r] = yd + (kept[r] ? int64_t(row) * row_vecs : 0);
     }
-    for (int64_t v0 = lane; v0 < row_vecs; v0 += 64) {
+    for (int64_t v0 = vb + lane; v0 < ve; v0 += 64) {
       uint4 buf[2][KMAX];
 #pragma unroll
       for (int u = 0; u < 2; ++u)
 #pragma unroll
         for (int r = 0; r < KMAX; ++r)
-          if (kept[r] && v0 + 32 * u < row_vecs) buf[u][r] = __ldcs(src[r] + v0 + 32 * u);
+          if (kept[r] && v0 + 32 * u < ve) buf[u][r] = __ldcs(src[r] + v0 + 32 * u);
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const int64_t v = v0 + 32 * u;
-        if (v >= row_vecs) break;
+        if (v >= ve) break;
         float acc[NV];
 #pragma unroll
         for (int i = 0; i < NV; ++i) acc[i] = 0.f;
@@ -126,12 +129,14 @@ cudaError_t launch_combine(const moe_config_t& c, int64_t max_rows, const void* 
                            const int32_t* slot_row, const float* w, void* y, cudaStream_t st) {
   const int elem = c.dtype == MOE_DT_BF16 ? 2 : 4;
   const int64_t row_vecs = int64_t(c.d) * elem / 16;
+  const RowSplit rs = row_split(c.T, row_vecs, 64);
   const int sms = device_sms();
-  const int64_t want = (c.T + 7) / 8;
+  const int64_t want = (c.T * rs.n_parts + 7) / 8;
   const unsigned grid = unsigned(want < int64_t(sms) * 8 ? want : int64_t(sms) * 8);
   auto run = [&](auto kernel) {
-    kernel<<<grid, 256, 0, st>>>(c.T, c.k, row_vecs, max_rows, static_cast<const uint4*>(yd),
-                                 slot_row, w, static_cast<uint4*>(y));
+    kernel<<<grid, 256, 0, st>>>(c.T, c.k, row_vecs, rs.n_parts, rs.part_vecs, max_rows,
+                                 static_cast<const uint4*>(yd), slot_row, w,
+                                 static_cast<uint4*>(y));
   };
   if (c.dtype == MOE_DT_BF16) {
     if (c.k <= 2) run(combine_kernel<__nv_bfloat16, 2>);

@@ -129,6 +129,24 @@ struct AuxArgs {
   unsigned long long* psum_fixed;
 };
 
+// Per-token row work (scatter, combine) is done by one warp per (token, part
+// of the row).  With few tokens the row is cut into parts of at least
+// min_part 16-byte vectors so that about kRowWorkItems warps have work (a
+// handful of warps walking long rows one load round after another is
+// latency-bound); with T >= kRowWorkItems a part is the whole row.
+constexpr int64_t kRowWorkItems = 2048;
+struct RowSplit {
+  int64_t n_parts, part_vecs;
+};
+inline RowSplit row_split(int64_t T, int64_t row_vecs, int64_t min_part) {
+  int64_t parts = (kRowWorkItems + T - 1) / T;
+  const int64_t max_parts = (row_vecs + min_part - 1) / min_part;
+  if (parts > max_parts) parts = max_parts;
+  if (parts < 1) parts = 1;
+  const int64_t pv = (row_vecs + parts - 1) / parts;
+  return {(row_vecs + pv - 1) / pv, pv};
+}
+
 // Record the first asynchronous error in the status word.
 __device__ __forceinline__ void set_status(int32_t* status, int32_t code) {
   if (status) atomicCAS(status, 0, code);

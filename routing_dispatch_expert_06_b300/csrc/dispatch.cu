@@ -241,22 +241,26 @@ __global__ void __launch_bounds__(kDispatchThreads)
 // xd[slot_row[t,r]] = x[t] for every kept slot; one warp per token, the row
 // is read once (16-byte vectors, 4 in flight per lane) and written k times.
 __global__ void __launch_bounds__(256)
-    scatter_rows_kernel(int64_t T, int k, int64_t row_vecs, const uint4* __restrict__ x,
-                        const int32_t* __restrict__ slot_row, uint4* __restrict__ xd) {
+    scatter_rows_kernel(int64_t T, int k, int64_t row_vecs, int64_t n_parts, int64_t part_vecs,
+                        const uint4* __restrict__ x, const int32_t* __restrict__ slot_row,
+                        uint4* __restrict__ xd) {
   const int lane = threadIdx.x & 31;
   const int64_t warps = int64_t(gridDim.x) * (blockDim.x >> 5);
-  for (int64_t t = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T;
-       t += warps) {
+  for (int64_t it = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       it < T * n_parts; it += warps) {
+    const int64_t t = it / n_parts;
+    const int64_t vb = (it % n_parts) * part_vecs;
+    const int64_t ve = vb + part_vecs < row_vecs ? vb + part_vecs : row_vecs;
     const int32_t my_row = lane < k ? slot_row[t * k + lane] : -1;
     const unsigned kept_mask = __ballot_sync(0xffffffffu, my_row >= 0);
     if (kept_mask == 0) continue;
     const uint4* src = x + t * row_vecs;
-    for (int64_t v0 = 0; v0 < row_vecs; v0 += 4 * 32) {
+    for (int64_t v0 = vb; v0 < ve; v0 += 4 * 32) {
       uint4 buf[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int64_t v = v0 + u * 32 + lane;
-        if (v < row_vecs) buf[u] = __ldcs(src + v);
+        if (v < ve) buf[u] = __ldcs(src + v);
       }
       unsigned m = kept_mask;
       while (m) {
@@ -267,7 +271,7 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int64_t v = v0 + u * 32 + lane;
-          if (v < row_vecs) dst[v] = buf[u];
+          if (v < ve) dst[v] = buf[u];
         }
       }
     }
@@ -302,11 +306,13 @@ cudaError_t launch_dispatch(const moe_config_t& c, int64_t C, const void* x,
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   const int elem = c.dtype == MOE_DT_BF16 ? 2 : 4;
   const int64_t row_vecs = int64_t(c.d) * elem / 16;
+  const RowSplit rs = row_split(c.T, row_vecs, 128);
   const int sms = device_sms();
-  const int64_t want = (c.T + 7) / 8;
+  const int64_t want = (c.T * rs.n_parts + 7) / 8;
   const unsigned grid = unsigned(want < int64_t(sms) * 8 ? want : int64_t(sms) * 8);
-  scatter_rows_kernel<<<grid, 256, 0, st>>>(c.T, c.k, row_vecs, static_cast<const uint4*>(x),
-                                            slot_row, static_cast<uint4*>(xd));
+  scatter_rows_kernel<<<grid, 256, 0, st>>>(c.T, c.k, row_vecs, rs.n_parts, rs.part_vecs,
+                                            static_cast<const uint4*>(x), slot_row,
+                                            static_cast<uint4*>(xd));
   count_launch();
   return cudaGetLastError();
 }

@@ -133,3 +133,32 @@ def test_unaligned_inputs_take_the_generic_router():
     assert x.data_ptr() % 16 != 0
     inp = dict(inp, x=x)
     _check(wl, inp, _route(wl, inp, "warp"))
+
+
+@pytest.mark.parametrize("case", [(8, 7168, 256, 8), (3000, 1024, 64, 6), (5000, 256, 8, 2)],
+                         ids=lambda c: f"t{c[0]}_e{c[2]}")
+def test_column_sums_repeat_exactly_and_match_the_whole_layer(case):
+    # The tensor-core router keeps Σ_t p as integer sums in the workspace and
+    # clears them after use: repeated calls give the same bits, and the whole
+    # layer (which converts them in the dispatch) gives the same psum.
+    T, d, E, k = case
+    wl = inputs.Workload(f"psum_t{T}_e{E}", T, d, 64, E, k, 1.0, True, "gelu_tanh", "bf16", 3,
+                         "normal:1.0")
+    inp = inputs.make_inputs(wl, "cuda")
+    cfg = moe.config_from_workload(wl)
+    ws = moe.workspace(cfg)
+    out = moe.allocate(cfg)
+    runs = []
+    for _ in range(3):
+        moe.route(cfg, inp["x"], inp["Wr"], inp["br"], out, ws)
+        torch.cuda.synchronize()
+        runs.append(h(out["psum"]).copy())
+    assert moe.device_status(ws) == moe.MOE_OK
+    for r in runs[1:]:
+        np.testing.assert_array_equal(r.view(np.uint32), runs[0].view(np.uint32))
+    moe.forward(cfg, inp, out, ws, 0.01)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(h(out["psum"]).view(np.uint32), runs[0].view(np.uint32))
+    ref_logits = oracle.router_logits(h(inp["x"]), h(inp["Wr"]), h(inp["br"]))
+    _, _, psum, _ = oracle.select(ref_logits, k, True)
+    assert_rel_rms(runs[0], psum, 1e-4, "psum")
