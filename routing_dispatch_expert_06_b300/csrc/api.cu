@@ -195,6 +195,13 @@ static moe_status_t get_ws(const moe_config_t& c, void* ws, size_t ws_bytes, Ws*
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
+// Most rows any expert can hold: min(C, T·k) (kept = min(count, C)).
+static int64_t rows_per_expert_max(const moe_config_t* c) {
+  const int64_t C = capacity_of(c->T, c->k, c->E, c->capacity_factor);
+  const int64_t tk = c->T * c->k;
+  return C < tk ? C : tk;
+}
+
 // Which expert GEMM runs for bf16 layers: the tcgen05 kernel by default;
 // MOE_FFN_IMPL=simt selects the CUDA-core kernel (a cross-check in tests).
 static bool use_tc_gemm(const moe_config_t& c) {
@@ -350,12 +357,17 @@ moe_status_t moe_ffn_up(const moe_config_t* cfg, const void* xd, const int32_t* 
   Ws w;
   if ((s = get_ws(*cfg, ws, ws_bytes, &w)) != MOE_OK) return s;
   const int64_t R = moe_max_rows(cfg);
+  const int64_t rpe = rows_per_expert_max(cfg);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = use_tc_gemm(*cfg)
-                      ? launch_gemm_tc(cfg->E, cfg->d_ff, cfg->d, R, offsets, xd, W1, b1,
-                                       cfg->act, H, w.status, st)
-                      : launch_gemm_simt(cfg->dtype, cfg->E, cfg->d_ff, cfg->d, R, offsets, xd,
-                                         W1, b1, cfg->act, H, st);
+  cudaError_t e =
+      !use_tc_gemm(*cfg)
+          ? launch_gemm_simt(cfg->dtype, cfg->E, cfg->d_ff, cfg->d, R, offsets, xd, W1, b1,
+                             cfg->act, H, st)
+      : gemm_swap_applies(rpe)
+          ? launch_gemm_swap(cfg->E, cfg->d_ff, cfg->d, R, rpe, offsets, xd, W1, b1, cfg->act, H,
+                             w.status, st)
+          : launch_gemm_tc(cfg->E, cfg->d_ff, cfg->d, R, offsets, xd, W1, b1, cfg->act, H,
+                           w.status, st);
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_ffn_up");
 }
 
@@ -372,11 +384,16 @@ moe_status_t moe_ffn_down(const moe_config_t* cfg, const void* H, const int32_t*
   if ((s = get_ws(*cfg, ws, ws_bytes, &w)) != MOE_OK) return s;
   const int64_t R = moe_max_rows(cfg);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = use_tc_gemm(*cfg)
-                      ? launch_gemm_tc(cfg->E, cfg->d, cfg->d_ff, R, offsets, H, W2, b2, -1, yd,
-                                       w.status, st)
-                      : launch_gemm_simt(cfg->dtype, cfg->E, cfg->d, cfg->d_ff, R, offsets, H,
-                                         W2, b2, -1, yd, st);
+  const int64_t rpe = rows_per_expert_max(cfg);
+  cudaError_t e =
+      !use_tc_gemm(*cfg)
+          ? launch_gemm_simt(cfg->dtype, cfg->E, cfg->d, cfg->d_ff, R, offsets, H, W2, b2, -1,
+                             yd, st)
+      : gemm_swap_applies(rpe)
+          ? launch_gemm_swap(cfg->E, cfg->d, cfg->d_ff, R, rpe, offsets, H, W2, b2, -1, yd,
+                             w.status, st)
+          : launch_gemm_tc(cfg->E, cfg->d, cfg->d_ff, R, offsets, H, W2, b2, -1, yd, w.status,
+                           st);
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_ffn_down");
 }
 

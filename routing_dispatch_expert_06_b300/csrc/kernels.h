@@ -83,6 +83,14 @@ cudaError_t launch_gemm_simt(int dtype, int E, int N, int K, int64_t max_rows,
 cudaError_t launch_gemm_tc(int E, int N, int K, int64_t max_rows, const int32_t* offsets,
                            const void* A, const void* B, const float* bias, int act,
                            void* out, int32_t* status, cudaStream_t st);
+// The same GEMM with the operands' roles swapped (MMA M over weight rows, N
+// over an expert's rows), for layers where no expert holds more than
+// rows_per_expert_max <= 64 rows (gemm_swap_applies).
+bool gemm_swap_applies(int64_t rows_per_expert_max);
+cudaError_t launch_gemm_swap(int E, int N, int K, int64_t max_rows, int64_t rows_per_expert_max,
+                             const int32_t* offsets, const void* A, const void* B,
+                             const float* bias, int act, void* out, int32_t* status,
+                             cudaStream_t st);
 
 // Combine: y[t] = Σ_r w[t,r]·yd[slot_row[t,r]] (kept slots, rank order, fp32).
 // Rows outside [0, max_rows) are treated as dropped.

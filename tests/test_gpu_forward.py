@@ -114,6 +114,29 @@ def test_two_sm_gemm_matches_one_sm_gemm():
         assert ((a - b).abs() <= 1e-2 + 2e-2 * b.abs()).all(), name
 
 
+@pytest.mark.parametrize("name,c", [("decode_bf16_t64_d2048_e64_top6", 1.0),
+                                    ("decode_bf16_t64_d2048_e64_top6", 5.0),
+                                    ("decode_bf16_t8_d7168_e256_top8", 1.25)])
+def test_swapped_gemm_matches_regular_gemm(name, c):
+    # With at most min(C, T·k) <= 64 rows per expert the expert GEMMs swap the
+    # operands' roles (MMA M over weight rows, N over the expert's 16/32/64
+    # rows); MOE_FFN_SWAP=0 runs the regular kernel.  c = 5 gives C = 30
+    # (N = 32) with experts holding up to 30 rows.
+    wl = W[name].replace(capacity_factor=c)
+    _, inp, out_s, _ = run_gpu(wl, expert_bias=True)
+    os.environ["MOE_FFN_SWAP"] = "0"
+    try:
+        _, _, out_r, _ = run_gpu(wl, inp=inp)
+    finally:
+        del os.environ["MOE_FFN_SWAP"]
+    n = int(h(out_s["offsets"])[-1])
+    assert n == int(h(out_r["offsets"])[-1]) > 0
+    for name_ in ["H", "yd"]:
+        a = out_s[name_][:n].float()
+        b = out_r[name_][:n].float()
+        assert ((a - b).abs() <= 1e-2 + 2e-2 * b.abs()).all(), name_
+
+
 def test_forward_replays_from_a_cuda_graph():
     # moe_forward only enqueues kernels (no allocation, no synchronisation),
     # so it can be captured once and replayed; the replay must reproduce the
