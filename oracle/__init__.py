@@ -17,6 +17,10 @@ the steps in the order of the source article,
     §1   expert FFN                 -> ffn_rows
     §3.2 f_i, p̄_i, L_aux            -> aux
 
+and, from "MoE Expert Parallelism 工程" (ai-master.cc), the expert-bias
+selection (select's ``sel_bias``) and the routing-health indicators
+(routing_health).
+
 bf16 tensors are passed as numpy ``uint16`` arrays holding the bit patterns.
 """
 
@@ -63,13 +67,14 @@ def _get():
             lib.oracle_num_threads.restype = ctypes.c_int
             lib.oracle_activation.argtypes = [i64, i32, P, P]
             lib.oracle_router_logits.argtypes = [i64, i32, i32, P, i32, P, i32, P, P]
-            lib.oracle_select.argtypes = [i64, i32, i32, i32, P, P, P, P, P]
+            lib.oracle_select.argtypes = [i64, i32, i32, i32, P, P, P, P, P, P]
             lib.oracle_fill.argtypes = [i64, i32, i32, i64, P, P, P, P, P, P]
             lib.oracle_permute.argtypes = [i64, i64, P, P, P]
             lib.oracle_ffn_rows.argtypes = [i32, i32, i32, P, i64, P, P, i32, P, P, P, P, i32,
                                             i32, i32, P]
             lib.oracle_combine.argtypes = [i64, P, i32, i32, P, P, P, P, P]
             lib.oracle_aux.argtypes = [i32, i64, f64, P, P, P, P, P]
+            lib.oracle_routing_health.argtypes = [i32, i64, i32, P, P, P]
             _lib = lib
     return _lib
 
@@ -117,20 +122,23 @@ def router_logits(x, Wr, br):
     return out
 
 
-def select(logits32, k: int, renormalize: bool, want_probs: bool = False):
+def select(logits32, k: int, renormalize: bool, want_probs: bool = False, sel_bias=None):
     """[§2.1, §2.2] softmax, top-k (ties to the lower index), weights, Σ_t p.
 
     ``logits32`` are fp32 scores (the oracle's own, rounded, or a device's).
+    ``sel_bias`` (fp32 [E] or None): experts are ranked by the fp32 sum
+    score + sel_bias; the weights still come from the unbiased softmax.
     Returns (topk_ids int32 [T,k], topk_w float64 [T,k], psum float64 [E],
     probs float64 [T,E] or None).
     """
     s = _c(logits32, np.float32)
     T, E = s.shape
+    sb = None if sel_bias is None else _c(sel_bias, np.float32)
     ids = np.empty((T, k), np.int32)
     w = np.empty((T, k), np.float64)
     psum = np.empty(E, np.float64)
     probs = np.empty((T, E), np.float64) if want_probs else None
-    _get().oracle_select(T, E, int(k), int(bool(renormalize)), _p(s), _p(ids), _p(w),
+    _get().oracle_select(T, E, int(k), int(bool(renormalize)), _p(s), _p(sb), _p(ids), _p(w),
                          _p(probs), _p(psum))
     return ids, w, psum, probs
 
@@ -220,8 +228,20 @@ def aux(counts, psum, T: int, alpha: float):
     return f, pbar, float(l[0])
 
 
+def routing_health(counts, kept, T: int, k: int):
+    """Routing-health indicators from counts (before capacity) and kept rows:
+    (entropy of counts/(T·k) in nats, variance of counts, variance of kept,
+    fraction of slots dropped)."""
+    counts = _c(counts, np.int32)
+    kept = _c(kept, np.int32)
+    out = np.empty(4, np.float64)
+    _get().oracle_routing_health(counts.shape[0], int(T), int(k), _p(counts), _p(kept), _p(out))
+    return out
+
+
 def forward(x, Wr, br, W1, b1, W2, b2, *, k: int, capacity_factor: float, renormalize: bool,
-            act: int, alpha: float = 1.0, logits32=None, tokens=None, round_h: int = 0):
+            act: int, alpha: float = 1.0, logits32=None, tokens=None, round_h: int = 0,
+            sel_bias=None):
     """The whole layer, step by step in the article's order.
 
     ``logits32``: fp32 scores to route on (a device's own); default: the
@@ -238,7 +258,7 @@ def forward(x, Wr, br, W1, b1, W2, b2, *, k: int, capacity_factor: float, renorm
         out["logits_f64"] = ld
         logits32 = ld.astype(np.float32)
     out["logits"] = np.asarray(logits32, np.float32)
-    ids, w, psum, _ = select(logits32, k, renormalize)
+    ids, w, psum, _ = select(logits32, k, renormalize, sel_bias=sel_bias)
     out.update(topk_ids=ids, topk_w=w, psum=psum)
     C = capacity(T, k, E, capacity_factor)
     out["C"] = C
@@ -246,6 +266,7 @@ def forward(x, Wr, br, W1, b1, W2, b2, *, k: int, capacity_factor: float, renorm
     out.update(fl)
     f, pbar, l_aux = aux(fl["counts"], psum, T, alpha)
     out.update(f=f, pbar=pbar, l_aux=l_aux)
+    out["health"] = routing_health(fl["counts"], fl["kept"], T, k)
     slot_row = fl["slot_row"]
     if tokens is None:
         xd = permute(x, fl["row_token"])

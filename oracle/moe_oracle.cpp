@@ -152,9 +152,15 @@ void oracle_router_logits(int64_t T, int32_t d, int32_t E, const void* x, int32_
 //   weights = p_{t,i} / Σ_{j∈S_t} p_{t,j}  if renormalize, else p_{t,i}
 //             (§2.2 notes that some implementations do not renormalise).
 // psum[i] = Σ_t p_{t,i}, summed over t in ascending order (for p̄, §3.2).
+// sel_bias (nullable, [E]): a per-expert bias that moves only the choice of
+// S_t (the expert-bias routing of [EP 工程 ai-master, 一、负载均衡]: it replaces the
+// auxiliary loss and shifts which experts win, not the combine weights):
+// experts are ranked by key_i = s_{t,i} + sel_bias_i, formed in fp32 (a
+// float addition, the precision the selection is taken in), and the weights
+// above still use the unbiased p.
 void oracle_select(int64_t T, int32_t E, int32_t k, int32_t renormalize, const float* logits,
-                   int32_t* topk_ids, double* topk_w, double* probs /*nullable, [T,E]*/,
-                   double* psum) {
+                   const float* sel_bias, int32_t* topk_ids, double* topk_w,
+                   double* probs /*nullable, [T,E]*/, double* psum) {
   std::vector<double> p_all(static_cast<size_t>(T) * E);
   parallel_for(T, [&](int64_t t) {
     const float* s = logits + t * E;
@@ -165,15 +171,19 @@ void oracle_select(int64_t T, int32_t E, int32_t k, int32_t renormalize, const f
     double* p = &p_all[static_cast<size_t>(t) * E];
     for (int32_t i = 0; i < E; ++i) p[i] = std::exp(static_cast<double>(s[i]) - mx) / z;
 
+    // Ranking keys: the scores, or the scores plus the selection bias.
+    std::vector<float> key(s, s + E);
+    if (sel_bias)
+      for (int32_t i = 0; i < E; ++i) key[i] = s[i] + sel_bias[i];
     // Top-k by repeated selection of the maximum among the not-yet-taken
-    // experts; a strict '>' keeps the lowest index among equal scores.
+    // experts; a strict '>' keeps the lowest index among equal keys.
     std::vector<char> taken(E, 0);
     double sel_sum = 0.0;
     for (int32_t r = 0; r < k; ++r) {
       int32_t best = -1;
       for (int32_t i = 0; i < E; ++i) {
         if (taken[i]) continue;
-        if (best < 0 || s[i] > s[best]) best = i;
+        if (best < 0 || key[i] > key[best]) best = i;
       }
       taken[best] = 1;
       topk_ids[t * k + r] = best;
@@ -314,6 +324,35 @@ void oracle_aux(int32_t E, int64_t T, double alpha, const int32_t* counts, const
     acc += f[i] * pbar[i];
   }
   *l_aux = alpha * static_cast<double>(E) * acc;
+}
+
+// Routing-health indicators ([EP 工程 ai-master, 追问 2]: the entropy of the
+// expert-activation distribution and the variance of the tokens each expert
+// processes; [MoE 模型原理 §10.4]: the overflow share), from the counts
+// before capacity and the kept rows after it:
+//   out[0] = H = -Σ_i q_i ln q_i,  q_i = counts_i / (T·k)  (0·ln 0 = 0; nats)
+//   out[1] = (1/E) Σ_i (counts_i - T·k/E)^2      (variance of routed slots)
+//   out[2] = (1/E) Σ_i (kept_i - mean(kept))^2   (variance of processed rows)
+//   out[3] = 1 - Σ_i kept_i / (T·k)              (fraction of slots dropped)
+void oracle_routing_health(int32_t E, int64_t T, int32_t k, const int32_t* counts,
+                           const int32_t* kept, double* out) {
+  const double n = static_cast<double>(T) * static_cast<double>(k);
+  double h = 0.0, vc = 0.0, vk = 0.0, kept_sum = 0.0;
+  for (int32_t i = 0; i < E; ++i) {
+    const double q = static_cast<double>(counts[i]) / n;
+    if (q > 0.0) h -= q * std::log(q);
+    kept_sum += static_cast<double>(kept[i]);
+  }
+  const double mc = n / static_cast<double>(E);
+  const double mk = kept_sum / static_cast<double>(E);
+  for (int32_t i = 0; i < E; ++i) {
+    vc += (counts[i] - mc) * (counts[i] - mc);
+    vk += (kept[i] - mk) * (kept[i] - mk);
+  }
+  out[0] = h;
+  out[1] = vc / static_cast<double>(E);
+  out[2] = vk / static_cast<double>(E);
+  out[3] = 1.0 - kept_sum / n;
 }
 
 }  // extern "C"

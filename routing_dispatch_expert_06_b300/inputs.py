@@ -56,10 +56,19 @@ WORKLOADS = {
                  "bf16", 3, "zipf:0.8"),
         Workload("bf16_t32768_d7168_e256_top8", 32768, 7168, 2048, 256, 8, 1.25, False,
                  "gelu_tanh", "bf16", 4, "normal:1.0"),
-        # Decode regime: a few tokens per call on the two many-expert layers;
-        # the expert FFN is then bound by reading the touched experts' weights.
+        # Decode regime: T = 1, 8, 64 tokens per call on the two many-expert
+        # layers; the expert FFN is then bound by reading the touched experts'
+        # weights.
+        Workload("decode_bf16_t1_d7168_e256_top8", 1, 7168, 2048, 256, 8, 1.25, False,
+                 "gelu_tanh", "bf16", 9, "normal:1.0"),
         Workload("decode_bf16_t8_d7168_e256_top8", 8, 7168, 2048, 256, 8, 1.25, False,
                  "gelu_tanh", "bf16", 6, "normal:1.0"),
+        Workload("decode_bf16_t64_d7168_e256_top8", 64, 7168, 2048, 256, 8, 1.25, False,
+                 "gelu_tanh", "bf16", 10, "normal:1.0"),
+        Workload("decode_bf16_t1_d2048_e64_top6", 1, 2048, 1408, 64, 6, 1.0, True,
+                 "gelu_tanh", "bf16", 11, "zipf:0.8"),
+        Workload("decode_bf16_t8_d2048_e64_top6", 8, 2048, 1408, 64, 6, 1.0, True,
+                 "gelu_tanh", "bf16", 12, "zipf:0.8"),
         Workload("decode_bf16_t64_d2048_e64_top6", 64, 2048, 1408, 64, 6, 1.0, True,
                  "gelu_tanh", "bf16", 7, "zipf:0.8"),
         # Dropless: c = E/k makes C = ceil(c·T·k/E) = T, so no expert can

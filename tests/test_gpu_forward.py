@@ -189,8 +189,7 @@ def test_pair_body_and_tail_tiles_match_one_sm_gemm():
         assert ((a - b).abs() <= 1e-2 + 2e-2 * b.abs()).all(), name
 
 
-@pytest.mark.parametrize("name", ["decode_bf16_t8_d7168_e256_top8",
-                                  "decode_bf16_t64_d2048_e64_top6"])
+@pytest.mark.parametrize("name", [n for n in W if n.startswith("decode_")])
 def test_decode_regime(name):
     # A few tokens per call on the many-expert layers: every output is checked.
     wl = W[name]
