@@ -107,6 +107,9 @@ typedef struct moe_tensors {
   float* f;             /* [E]     f_i                                */
   float* pbar;          /* [E]     p̄_i                                */
   float* l_aux;         /* [1]     L_aux                              */
+  /* optional inputs/outputs (NULL: not used) */
+  const float* sel_bias; /* [E] expert bias for the top-k choice only (moe_route_sel) */
+  float* health;         /* [4] routing-health indicators (moe_routing_health) */
 } moe_tensors_t;
 
 /* [MoE 模型原理 §4.1] Capacity C = ceil(c·T·k/E), exact for the binary value
@@ -190,6 +193,27 @@ moe_status_t moe_expert_ffn(const moe_config_t* cfg, const void* xd, const int32
 moe_status_t moe_combine(const moe_config_t* cfg, const void* yd, const int32_t* slot_row,
                          const float* topk_w, void* y, void* stream);
 
+/* moe_route with an expert bias that moves only the choice of S_t (the
+ * expert-bias routing of [EP 工程 ai-master, 一、负载均衡], which replaces the
+ * auxiliary loss): experts are ranked by the fp32 sum s_{t,i} + sel_bias[i]
+ * (ties to the lower index); topk_w, psum and the logits stay those of the
+ * unbiased scores.  sel_bias: [E] fp32 device, or NULL (= moe_route). */
+moe_status_t moe_route_sel(const moe_config_t* cfg, const void* x, const void* Wr,
+                           const float* br, const float* sel_bias, float* logits,
+                           int32_t* topk_ids, float* topk_w, float* psum, void* ws,
+                           size_t ws_bytes, void* stream);
+
+/* [EP 工程 ai-master, 追问 2; MoE 模型原理 §10.4] Routing-health indicators
+ * from counts (before capacity) and kept (after), into health[4] (fp32,
+ * device):
+ *   health[0] = -Σ_i q_i ln q_i, q_i = counts_i/(T·k)  (activation entropy, nats)
+ *   health[1] = (1/E) Σ_i (counts_i - T·k/E)^2       (variance of routed slots)
+ *   health[2] = (1/E) Σ_i (kept_i - mean kept)^2     (variance of processed rows)
+ *   health[3] = 1 - Σ_i kept_i/(T·k)                 (fraction of slots dropped)
+ * One block, fixed reduction order (deterministic). */
+moe_status_t moe_routing_health(const moe_config_t* cfg, const int32_t* counts,
+                                const int32_t* kept, float* health, void* stream);
+
 /* [MoE 模型原理 §3.2] f = counts/T, p̄ = psum/T, L_aux = α·E·Σ f·p̄. */
 moe_status_t moe_aux_stats(const moe_config_t* cfg, const int32_t* counts, const float* psum,
                            float alpha, float* f, float* pbar, float* l_aux, void* stream);
@@ -197,7 +221,9 @@ moe_status_t moe_aux_stats(const moe_config_t* cfg, const int32_t* counts, const
 /* The whole layer: route, dispatch, expert FFN, combine, aux (the aux
  * statistics are computed inside the dispatch launches here, with the same
  * arithmetic and results as moe_aux_stats; psum is also formed there from the
- * router's fixed-point column sums).  If it returns an error after the router
+ * router's fixed-point column sums).  t->sel_bias (optional) routes as
+ * moe_route_sel; t->health (optional) receives moe_routing_health's
+ * indicators, computed in the same dispatch launch.  If it returns an error after the router
  * was enqueued, call moe_workspace_init before the next call on that
  * workspace. */
 moe_status_t moe_forward(const moe_config_t* cfg, const moe_tensors_t* t, float alpha, void* ws,

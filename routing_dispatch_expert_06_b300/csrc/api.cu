@@ -236,9 +236,10 @@ namespace moe {
 // dispatch's histogram to convert (psum_from_fixed); the other routers write
 // psum and set it to NULL.
 static moe_status_t route_impl(const moe_config_t* cfg, const void* x, const void* Wr,
-                               const float* br, float* logits, int32_t* topk_ids, float* topk_w,
-                               float* psum, void* ws, size_t ws_bytes,
-                               unsigned long long** psum_fixed_out, void* stream) {
+                               const float* br, const float* sel_bias, float* logits,
+                               int32_t* topk_ids, float* topk_w, float* psum, void* ws,
+                               size_t ws_bytes, unsigned long long** psum_fixed_out,
+                               void* stream) {
   moe_status_t s = check_cfg(cfg);
   if (s != MOE_OK) return s;
   if (!x || !Wr || !br || !topk_ids || !topk_w || !psum)
@@ -255,19 +256,19 @@ static moe_status_t route_impl(const moe_config_t* cfg, const void* x, const voi
   switch (pick_router(*cfg, aligned16(x) && aligned16(Wr))) {
     case Router::kWarp:
       e = launch_route_warp(*cfg, x, Wr, br, lg, topk_ids, topk_w, w.psum_partial, psum, counter,
-                            st);
+                            sel_bias, st);
       break;
     case Router::kTc:
       e = launch_route_tc(*cfg, x, Wr, w.route_part, w.status, st);
       if (e == cudaSuccess)
         e = launch_route_select(*cfg, w.route_part, route_tc_nsplit(*cfg), br, lg, topk_ids,
                                 topk_w, w.psum_fixed, psum, counter, psum_fixed_out == nullptr,
-                                st);
+                                sel_bias, st);
       if (e == cudaSuccess && psum_fixed_out) *psum_fixed_out = w.psum_fixed;
       break;
     default:
       e = launch_route_simt(*cfg, x, Wr, br, lg, topk_ids, topk_w, w.psum_partial, psum, counter,
-                            st);
+                            sel_bias, st);
       break;
   }
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_route");
@@ -307,7 +308,26 @@ moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, void* stream) {
 moe_status_t moe_route(const moe_config_t* cfg, const void* x, const void* Wr, const float* br,
                        float* logits, int32_t* topk_ids, float* topk_w, float* psum, void* ws,
                        size_t ws_bytes, void* stream) {
-  return route_impl(cfg, x, Wr, br, logits, topk_ids, topk_w, psum, ws, ws_bytes, nullptr, stream);
+  return route_impl(cfg, x, Wr, br, nullptr, logits, topk_ids, topk_w, psum, ws, ws_bytes,
+                    nullptr, stream);
+}
+
+moe_status_t moe_route_sel(const moe_config_t* cfg, const void* x, const void* Wr,
+                           const float* br, const float* sel_bias, float* logits,
+                           int32_t* topk_ids, float* topk_w, float* psum, void* ws,
+                           size_t ws_bytes, void* stream) {
+  return route_impl(cfg, x, Wr, br, sel_bias, logits, topk_ids, topk_w, psum, ws, ws_bytes,
+                    nullptr, stream);
+}
+
+moe_status_t moe_routing_health(const moe_config_t* cfg, const int32_t* counts,
+                                const int32_t* kept, float* health, void* stream) {
+  moe_status_t s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  if (!counts || !kept || !health)
+    return fail(MOE_ERR_INVALID_ARG, "moe_routing_health: NULL tensor");
+  cudaError_t e = launch_health(*cfg, counts, kept, health, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_routing_health");
 }
 
 }  // extern "C"
@@ -436,13 +456,13 @@ moe_status_t moe_forward(const moe_config_t* cfg, const moe_tensors_t* t, float 
     return fail(MOE_ERR_INVALID_ARG, "moe_aux_stats: NULL tensor");
   moe_status_t s;
   unsigned long long* psum_fixed = nullptr;
-  if ((s = route_impl(cfg, t->x, t->Wr, t->br, t->logits, t->topk_ids, t->topk_w, t->psum, ws,
-                      ws_bytes, &psum_fixed, stream)) != MOE_OK)
+  if ((s = route_impl(cfg, t->x, t->Wr, t->br, t->sel_bias, t->logits, t->topk_ids, t->topk_w,
+                      t->psum, ws, ws_bytes, &psum_fixed, stream)) != MOE_OK)
     return s;
   // The statistics need only counts and psum: the dispatch's last histogram
   // block computes them (same arithmetic as moe_aux_stats), saving a launch;
   // with the tensor-core router it first forms psum from the fixed-point sums.
-  const AuxArgs aux{alpha, t->psum, t->f, t->pbar, t->l_aux, psum_fixed};
+  const AuxArgs aux{alpha, t->psum, t->f, t->pbar, t->l_aux, psum_fixed, t->health};
   if ((s = dispatch_impl(cfg, t->x, t->topk_ids, t->counts, t->kept, t->offsets, t->slot_row,
                          t->row_token, t->xd, ws, ws_bytes, &aux, stream)) != MOE_OK)
     return s;

@@ -125,6 +125,22 @@ __global__ void __launch_bounds__(kAuxThreads)
   aux_stats_block(E, T, alpha, counts, psum, f, pbar, l_aux, red);
 }
 
+// One block computes the routing-health indicators (routing_health_block).
+__global__ void __launch_bounds__(kAuxThreads)
+    health_kernel(int E, int64_t T, int k, const int32_t* __restrict__ counts,
+                  const int32_t* __restrict__ kept, float* health) {
+  __shared__ float red[kAuxThreads];
+  __shared__ unsigned long long s_kept;
+  routing_health_block(E, T, k, counts, kept, health, red, &s_kept);
+}
+
+cudaError_t launch_health(const moe_config_t& c, const int32_t* counts, const int32_t* kept,
+                          float* health, cudaStream_t st) {
+  health_kernel<<<1, kAuxThreads, 0, st>>>(c.E, c.T, c.k, counts, kept, health);
+  count_launch();
+  return cudaGetLastError();
+}
+
 cudaError_t launch_combine(const moe_config_t& c, int64_t max_rows, const void* yd,
                            const int32_t* slot_row, const float* w, void* y, cudaStream_t st) {
   const int elem = c.dtype == MOE_DT_BF16 ? 2 : 4;

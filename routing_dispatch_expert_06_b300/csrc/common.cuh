@@ -117,9 +117,68 @@ __device__ __forceinline__ void psum_from_fixed(int E, unsigned long long* fixed
   }
 }
 
+// Sum of one value per thread over a block of kAuxThreads threads, in a fixed
+// tree order (deterministic); every thread gets the result.
+__device__ __forceinline__ float block_sum_fixed(float v, float* red) {
+  const int j = threadIdx.x;
+  red[j] = v;
+  __syncthreads();
+  for (int s = kAuxThreads / 2; s > 0; s >>= 1) {
+    if (j < s) red[j] = __fadd_rn(red[j], red[j + s]);
+    __syncthreads();
+  }
+  const float r = red[0];
+  __syncthreads();
+  return r;
+}
+
+// Routing-health indicators (one block of kAuxThreads threads), from counts
+// before capacity and kept rows after it:
+//   health[0] = -Σ q ln q, q_i = counts_i/(T·k)   health[1] = var(counts)
+//   health[2] = var(kept)                          health[3] = 1 - Σkept/(T·k)
+// (population variances over the E experts).  Σ kept is an exact integer sum.
+__device__ __forceinline__ void routing_health_block(int E, int64_t T, int k,
+                                                     const int32_t* counts, const int32_t* kept,
+                                                     float* health, float* red,
+                                                     unsigned long long* s_kept) {
+  const int j = threadIdx.x;
+  if (j == 0) *s_kept = 0ull;
+  __syncthreads();
+  const double n = double(T) * double(k);
+  const float mc = float(n / double(E));
+  float h = 0.f, vc = 0.f;
+  unsigned long long ks = 0ull;
+  for (int e = j; e < E; e += kAuxThreads) {
+    const int32_t c = __ldcg(counts + e);
+    const float q = float(double(c) / n);
+    if (q > 0.f) h = __fadd_rn(h, -__fmul_rn(q, logf(q)));
+    const float dc = float(c) - mc;
+    vc = __fadd_rn(vc, __fmul_rn(dc, dc));
+    ks += unsigned(__ldcg(kept + e));
+  }
+  atomicAdd(s_kept, ks);
+  h = block_sum_fixed(h, red);
+  vc = block_sum_fixed(vc, red);
+  const unsigned long long kept_sum = *s_kept;
+  const float mk = float(double(kept_sum) / double(E));
+  float vk = 0.f;
+  for (int e = j; e < E; e += kAuxThreads) {
+    const float dk = float(__ldcg(kept + e)) - mk;
+    vk = __fadd_rn(vk, __fmul_rn(dk, dk));
+  }
+  vk = block_sum_fixed(vk, red);
+  if (j == 0) {
+    health[0] = h;
+    health[1] = vc / float(E);
+    health[2] = vk / float(E);
+    health[3] = float(1.0 - double(kept_sum) / n);
+  }
+}
+
 // Aux-statistics outputs for the dispatch's last histogram block (forward
 // pass only).  psum_fixed: when set, psum is first formed from the router's
-// fixed-point column sums (psum_from_fixed).
+// fixed-point column sums (psum_from_fixed).  health: when set, the
+// routing-health indicators (routing_health_block) from counts and kept.
 struct AuxArgs {
   float alpha;
   float* psum;
@@ -127,6 +186,7 @@ struct AuxArgs {
   float* pbar;
   float* l_aux;
   unsigned long long* psum_fixed;
+  float* health;
 };
 
 // Per-token row work (scatter, combine) is done by one warp per (token, part

@@ -88,6 +88,7 @@ __global__ void __launch_bounds__(kDispatchThreads)
   extern __shared__ int32_t hist[];
   __shared__ int s_last;
   __shared__ float s_red[kAuxThreads];
+  __shared__ unsigned long long s_kept_sum;
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
   const int64_t t = int64_t(blockIdx.x) * kChunkTokens + threadIdx.x;
@@ -109,6 +110,10 @@ __global__ void __launch_bounds__(kDispatchThreads)
       if (aux.psum_fixed) psum_from_fixed(E, aux.psum_fixed, aux.psum);
       __syncthreads();
       aux_stats_block(E, T, aux.alpha, counts, aux.psum, aux.f, aux.pbar, aux.l_aux, s_red);
+    }
+    if (aux.health) {
+      __syncthreads();
+      routing_health_block(E, T, k, counts, kept, aux.health, s_red, &s_kept_sum);
     }
   }
 }
@@ -285,7 +290,8 @@ cudaError_t launch_dispatch(const moe_config_t& c, int64_t C, const void* x,
                             const AuxArgs* aux, cudaStream_t st) {
   const int64_t n_chunks = (c.T + kChunkTokens - 1) / kChunkTokens;
   const AuxArgs aux_v =
-      (aux && counter) ? *aux : AuxArgs{0.f, nullptr, nullptr, nullptr, nullptr, nullptr};
+      (aux && counter) ? *aux
+                       : AuxArgs{0.f, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
   cudaError_t err;
   histogram_kernel<<<unsigned(n_chunks), kDispatchThreads, size_t(c.E) * 4, st>>>(
       c.T, c.E, c.k, ids, chunk_counts, status, counter, C, counts, kept, aux_v);

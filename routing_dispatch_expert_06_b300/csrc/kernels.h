@@ -30,16 +30,20 @@ cudaError_t max_active_clusters(const void* kernel, const cudaLaunchConfig_t& cf
 // Router on CUDA cores (fp32 or bf16, any E): logits, softmax, top-k,
 // weights; per-block column sums of p in psum_partial, summed into psum by the
 // last block to finish (counter: a zeroed int in the workspace).
+// sel_bias (every router, nullable): rank experts by the fp32 sum
+// logit + sel_bias; weights, Σp and logits stay those of the logits.
 cudaError_t launch_route_simt(const moe_config_t& c, const void* x, const void* Wr,
                               const float* br, float* logits, int32_t* ids, float* w,
-                              float* psum_partial, float* psum, int* counter, cudaStream_t st);
+                              float* psum_partial, float* psum, int* counter,
+                              const float* sel_bias, cudaStream_t st);
 
 // Router on CUDA cores for bf16 layers with E <= 32 and W_r small enough for
 // shared memory: one warp per token, 16-byte loads, same outputs.
 bool route_warp_supported(const moe_config_t& c);
 cudaError_t launch_route_warp(const moe_config_t& c, const void* x, const void* Wr,
                               const float* br, float* logits, int32_t* ids, float* w,
-                              float* psum_partial, float* psum, int* counter, cudaStream_t st);
+                              float* psum_partial, float* psum, int* counter,
+                              const float* sel_bias, cudaStream_t st);
 
 // Router on the tcgen05 tensor cores (bf16, E <= 256): same outputs;
 // psum_partial holds one row per 128-token tile.
@@ -60,7 +64,10 @@ cudaError_t launch_route_tc(const moe_config_t& c, const void* x, const void* Wr
 cudaError_t launch_route_select(const moe_config_t& c, const float* part, int nsplit,
                                 const float* br, float* logits, int32_t* ids, float* w,
                                 unsigned long long* psum_fixed, float* psum, int* counter,
-                                bool finish, cudaStream_t st);
+                                bool finish, const float* sel_bias, cudaStream_t st);
+// One block: the routing-health indicators from counts and kept.
+cudaError_t launch_health(const moe_config_t& c, const int32_t* counts, const int32_t* kept,
+                          float* health, cudaStream_t st);
 
 // Dispatch: histogram per chunk, per-expert scan + capacity, positions, row
 // copy.  counter: a zeroed int for the histogram's grid-completion count (the

@@ -25,6 +25,8 @@
 // finish.  With `finish` set the last block to finish adds the copies,
 // converts the sum to fp32 and clears them; otherwise a later kernel does
 // (psum_from_fixed, in the dispatch's histogram when the whole layer runs).
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "tc.cuh"
@@ -42,6 +44,7 @@ struct SelectArgs {
   int finish;                      // 1: the last block converts the column sums
   const float* part;               // [nsplit][T][E]
   const float* br;                 // [E]
+  const float* sel_bias;           // [E] ranking-only bias, or NULL
   float* logits;                   // [T][E] or NULL
   int32_t* ids;                    // [T][k]
   float* w;                        // [T][k]
@@ -119,12 +122,14 @@ __device__ __forceinline__ float ordered_float(int key) {
 }
 
 // LPR lanes per token (8 or 16 for E <= 8 or 16, else 32), EPL columns per
-// lane (LPR < 32 only with EPL = 1).
-template <int EPL, int LPR, bool VEC>
+// lane (LPR < 32 only with EPL = 1).  SELB: experts are ranked by the fp32
+// sum logit + sel_bias (the weights still use the logit).
+template <int EPL, int LPR, bool VEC, bool SELB>
 __global__ void __launch_bounds__(kSelWarps * 32)
     route_select_kernel(const SelectArgs a) {
   constexpr int RPW = 32 / LPR;  // tokens per warp at a time
   __shared__ float s_bias[LPR * EPL];
+  __shared__ float s_sel[SELB ? LPR * EPL : 1];
   __shared__ float s_run[kSelWarps][32 * EPL];
   __shared__ unsigned long long s_acc[kSelWarps][32 * EPL];
   __shared__ unsigned long long s_col[32 * EPL];
@@ -136,7 +141,10 @@ __global__ void __launch_bounds__(kSelWarps * 32)
   const int wpr = a.wpr, slot = warp / wpr, q = warp % wpr;
   const int rows_per_group = (kSelWarps / wpr) * RPW;
   const int64_t n_groups = (a.T + rows_per_group - 1) / rows_per_group;
-  for (int c = threadIdx.x; c < LPR * EPL; c += blockDim.x) s_bias[c] = c < E ? a.br[c] : 0.f;
+  for (int c = threadIdx.x; c < LPR * EPL; c += blockDim.x) {
+    s_bias[c] = c < E ? a.br[c] : 0.f;
+    if constexpr (SELB) s_sel[c] = c < E ? a.sel_bias[c] : 0.f;
+  }
   // Per-column fixed-point sums of p over this lane's tokens.
   unsigned long long acc[EPL];
 #pragma unroll
@@ -204,27 +212,39 @@ __global__ void __launch_bounds__(kSelWarps * 32)
     }
     const float inv_z = __fdividef(1.f, seg_sum<LPR>(z));
 
-    // Top-k by segment argmax rounds; v is the working copy.
+    // Top-k by segment argmax rounds on the ranking keys (the logits, or
+    // logit + sel_bias); `key` is the working copy.  my_v: the winner's logit.
+    float key[EPL];
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) {
+      if constexpr (SELB)
+        key[j] = c0 + j < E ? v[j] + s_sel[c0 + j] : -INFINITY;
+      else
+        key[j] = v[j];
+    }
     float my_v = -INFINITY;
     int my_i = 0;
     for (int r = 0; r < k; ++r) {
-      float lm = v[0];
+      float lm = key[0];
 #pragma unroll
-      for (int j = 1; j < EPL; ++j) lm = fmaxf(lm, v[j]);
+      for (int j = 1; j < EPL; ++j) lm = fmaxf(lm, key[j]);
       if constexpr (LPR == 32) {
-        // Largest remaining value (a warp reduction on an order-preserving
+        // Largest remaining key (a warp reduction on an order-preserving
         // integer image of the float), then the lowest column holding it.
         const int gkey = __reduce_max_sync(0xffffffffu, ordered_key(lm));
         const float gm = ordered_float(gkey);
         int cand = 0x7fffffff;
 #pragma unroll
         for (int j = EPL - 1; j >= 0; --j)
-          if (v[j] == gm) cand = c0 + j;
+          if (key[j] == gm) cand = c0 + j;
         const int idx = __reduce_min_sync(0xffffffffu, cand);
+        float won = -INFINITY;  // the winner's logit, in the lane holding it
 #pragma unroll
         for (int j = 0; j < EPL; ++j)
-          if (c0 + j == idx) v[j] = -INFINITY;
-        if (sub == r) my_v = gm, my_i = idx;
+          if (c0 + j == idx) key[j] = -INFINITY, won = v[j];
+        float wv = gm;
+        if constexpr (SELB) wv = ordered_float(__reduce_max_sync(0xffffffffu, ordered_key(won)));
+        if (sub == r) my_v = wv, my_i = idx;
       } else {
         const float gm = seg_max<LPR>(lm);
         unsigned bits = __ballot_sync(0xffffffffu, lm == gm);
@@ -232,8 +252,9 @@ __global__ void __launch_bounds__(kSelWarps * 32)
         const int L = seg * LPR + __ffs(bits) - 1;
         // EPL == 1 here: lane L's only column.
         const int idx = __shfl_sync(0xffffffffu, c0, L);
-        if (lane == L) v[0] = -INFINITY;
-        if (sub == r) my_v = gm, my_i = idx;
+        const float wv = SELB ? __shfl_sync(0xffffffffu, v[0], L) : gm;
+        if (lane == L) key[0] = -INFINITY;
+        if (sub == r) my_v = wv, my_i = idx;
       }
     }
     const float ev = sub < k ? __expf(my_v - M) : 0.f;
@@ -266,14 +287,15 @@ __global__ void __launch_bounds__(kSelWarps * 32)
   finish_column_sums(a, s_col, &s_last);
 }
 
-template <int EPL, int LPR>
+template <int EPL, int LPR, bool SELB>
 cudaError_t launch_epl(const SelectArgs& a, cudaStream_t st) {
   const bool vec = EPL >= 4 ? (a.E & 3) == 0 : EPL == 2 ? (a.E & 1) == 0 : false;
   cudaLaunchConfig_t cfg{};
   const int rows_per_group = (kSelWarps / a.wpr) * (32 / LPR);
   const int64_t n_groups = (a.T + rows_per_group - 1) / rows_per_group;
   // One wave of resident blocks (the column sums do not depend on the grid).
-  auto kernel = vec ? route_select_kernel<EPL, LPR, true> : route_select_kernel<EPL, LPR, false>;
+  auto kernel = vec ? route_select_kernel<EPL, LPR, true, SELB>
+                    : route_select_kernel<EPL, LPR, false, SELB>;
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kSelWarps * 32, 0) !=
           cudaSuccess ||
@@ -299,7 +321,7 @@ cudaError_t launch_epl(const SelectArgs& a, cudaStream_t st) {
 cudaError_t launch_route_select(const moe_config_t& c, const float* part, int nsplit,
                                 const float* br, float* logits, int32_t* ids, float* w,
                                 unsigned long long* psum_fixed, float* psum, int* counter,
-                                bool finish, cudaStream_t st) {
+                                bool finish, const float* sel_bias, cudaStream_t st) {
   if (c.E > kPsumFixedMaxE) return cudaErrorInvalidValue;
   SelectArgs a{};
   a.T = c.T;
@@ -311,6 +333,7 @@ cudaError_t launch_route_select(const moe_config_t& c, const float* part, int ns
   a.wpr = nsplit <= 4 ? 1 : nsplit <= 8 ? 2 : nsplit <= 16 ? 4 : 8;
   a.part = part;
   a.br = br;
+  a.sel_bias = sel_bias;
   a.logits = logits;
   a.ids = ids;
   a.w = w;
@@ -319,12 +342,16 @@ cudaError_t launch_route_select(const moe_config_t& c, const float* part, int ns
   a.counter = counter;
   a.finish = finish ? 1 : 0;
   cudaError_t err;
-  if (c.E <= 8) err = launch_epl<1, 8>(a, st);
-  else if (c.E <= 16) err = launch_epl<1, 16>(a, st);
-  else if (c.E <= 32) err = launch_epl<1, 32>(a, st);
-  else if (c.E <= 64) err = launch_epl<2, 32>(a, st);
-  else if (c.E <= 128) err = launch_epl<4, 32>(a, st);
-  else err = launch_epl<8, 32>(a, st);
+  auto run = [&](auto selb) {
+    constexpr bool S = decltype(selb)::value;
+    if (c.E <= 8) return launch_epl<1, 8, S>(a, st);
+    if (c.E <= 16) return launch_epl<1, 16, S>(a, st);
+    if (c.E <= 32) return launch_epl<1, 32, S>(a, st);
+    if (c.E <= 64) return launch_epl<2, 32, S>(a, st);
+    if (c.E <= 128) return launch_epl<4, 32, S>(a, st);
+    return launch_epl<8, 32, S>(a, st);
+  };
+  err = sel_bias ? run(std::true_type{}) : run(std::false_type{});
   count_launch();
   return err;
 }

@@ -39,12 +39,14 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 // Softmax, top-k and weights for one token whose E fp32 logits sit in s_log
 // (warp-private shared memory).  Adds p_{t,i} into s_ps[i].  Writes ids and
-// weights for token t.  Ranking is on the fp32 logits; equal logits go to the
-// lower expert index.  Destroys s_log (selected entries become -inf; logits
-// are finite for finite inputs, so a taken entry never wins again).
+// weights for token t.  Ranking is on the fp32 logits, or with sel_bias
+// (nullable) on the fp32 sums logit + sel_bias (the weights still use the
+// logits); equal keys go to the lower expert index.  Destroys s_log (selected
+// entries become -inf; logits are finite for finite inputs, so a taken entry
+// never wins again).
 __device__ __forceinline__ void softmax_topk_warp(float* s_log, float* s_ps, int E, int k,
                                                   int renorm, int64_t t, int32_t* topk_ids,
-                                                  float* topk_w) {
+                                                  float* topk_w, const float* sel_bias) {
   const int lane = lane_id();
   float mx = -INFINITY;
   for (int e = lane; e < E; e += 32) mx = fmaxf(mx, s_log[e]);
@@ -62,6 +64,7 @@ __device__ __forceinline__ void softmax_topk_warp(float* s_log, float* s_ps, int
     int bi = 0x7fffffff;
     for (int e = lane; e < E; e += 32) {
       float v = s_log[e];
+      if (sel_bias) v += sel_bias[e];
       if (v > bv || (v == bv && e < bi)) {
         bv = v;
         bi = e;
@@ -78,7 +81,7 @@ __device__ __forceinline__ void softmax_topk_warp(float* s_log, float* s_ps, int
     }
     if (lane == r) {
       my_id = bi;
-      my_p = expf(bv - mx) * inv_z;
+      my_p = expf(s_log[bi] - mx) * inv_z;
     }
     __syncwarp();
     if (lane == (bi & 31)) s_log[bi] = -INFINITY;
@@ -96,7 +99,7 @@ __global__ void __launch_bounds__(256)
     route_simt_kernel(int64_t T, int d, int E, int k, int renorm, const TIn* __restrict__ x,
                       const TIn* __restrict__ Wr, const float* __restrict__ br, float* logits,
                       int32_t* topk_ids, float* topk_w, float* psum_partial, float* psum,
-                      int* counter) {
+                      int* counter, const float* __restrict__ sel_bias) {
   __shared__ int s_flag;
   extern __shared__ float smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -129,7 +132,7 @@ __global__ void __launch_bounds__(256)
     if (logits)
       for (int e = lane; e < E; e += 32) logits[t * E + e] = s_log[e];
     __syncwarp();
-    softmax_topk_warp(s_log, s_ps, E, k, renorm, t, topk_ids, topk_w);
+    softmax_topk_warp(s_log, s_ps, E, k, renorm, t, topk_ids, topk_w, sel_bias);
     __syncwarp();
   }
   __syncthreads();
@@ -155,7 +158,8 @@ __global__ void __launch_bounds__(256)
     route_warp_kernel(int64_t T, int d, int E, int k, int renorm,
                       const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ Wr,
                       const float* __restrict__ br, float* logits, int32_t* topk_ids,
-                      float* topk_w, float* psum_partial, float* psum, int* counter) {
+                      float* topk_w, float* psum_partial, float* psum, int* counter,
+                      const float* __restrict__ sel_bias) {
   extern __shared__ uint4 s_w[];  // [E][d/8] 16-byte chunks of W_r
   __shared__ float s_log[8][32];
   __shared__ float s_ps[8][32];
@@ -211,7 +215,7 @@ __global__ void __launch_bounds__(256)
     __syncwarp();
     if (logits && lane < E) logits[t * E + lane] = s_log[warp][lane];
     __syncwarp();
-    softmax_topk_warp(s_log[warp], s_ps[warp], E, k, renorm, t, topk_ids, topk_w);
+    softmax_topk_warp(s_log[warp], s_ps[warp], E, k, renorm, t, topk_ids, topk_w, sel_bias);
     __syncwarp();
   }
   __syncthreads();
@@ -225,7 +229,8 @@ __global__ void __launch_bounds__(256)
 
 cudaError_t launch_route_simt(const moe_config_t& c, const void* x, const void* Wr,
                               const float* br, float* logits, int32_t* ids, float* w,
-                              float* psum_partial, float* psum, int* counter, cudaStream_t st) {
+                              float* psum_partial, float* psum, int* counter,
+                              const float* sel_bias, cudaStream_t st) {
   const int64_t nblk = (c.T + kRouteTokensSimt - 1) / kRouteTokensSimt;
   const size_t smem = size_t(16) * c.E * sizeof(float);
   cudaError_t err;
@@ -234,14 +239,15 @@ cudaError_t launch_route_simt(const moe_config_t& c, const void* x, const void* 
     if (err != cudaSuccess) return err;
     route_simt_kernel<float><<<unsigned(nblk), 256, smem, st>>>(
         c.T, c.d, c.E, c.k, c.renormalize, static_cast<const float*>(x),
-        static_cast<const float*>(Wr), br, logits, ids, w, psum_partial, psum, counter);
+        static_cast<const float*>(Wr), br, logits, ids, w, psum_partial, psum, counter, sel_bias);
   } else {
     err = ensure_dynamic_smem(reinterpret_cast<const void*>(route_simt_kernel<__nv_bfloat16>),
                               smem);
     if (err != cudaSuccess) return err;
     route_simt_kernel<__nv_bfloat16><<<unsigned(nblk), 256, smem, st>>>(
         c.T, c.d, c.E, c.k, c.renormalize, static_cast<const __nv_bfloat16*>(x),
-        static_cast<const __nv_bfloat16*>(Wr), br, logits, ids, w, psum_partial, psum, counter);
+        static_cast<const __nv_bfloat16*>(Wr), br, logits, ids, w, psum_partial, psum, counter,
+        sel_bias);
   }
   count_launch();
   return cudaGetLastError();
@@ -253,7 +259,8 @@ bool route_warp_supported(const moe_config_t& c) {
 
 cudaError_t launch_route_warp(const moe_config_t& c, const void* x, const void* Wr,
                               const float* br, float* logits, int32_t* ids, float* w,
-                              float* psum_partial, float* psum, int* counter, cudaStream_t st) {
+                              float* psum_partial, float* psum, int* counter,
+                              const float* sel_bias, cudaStream_t st) {
   if (!route_warp_supported(c)) return cudaErrorInvalidValue;
   const int sms = device_sms();
   // Blocks of 8 warps, about 8 tokens per warp, at most 4 blocks per SM; one
@@ -267,7 +274,7 @@ cudaError_t launch_route_warp(const moe_config_t& c, const void* x, const void* 
     kernel<<<grid, 256, smem, st>>>(c.T, c.d, c.E, c.k, c.renormalize,
                                     static_cast<const __nv_bfloat16*>(x),
                                     static_cast<const __nv_bfloat16*>(Wr), br, logits, ids, w,
-                                    psum_partial, psum, counter);
+                                    psum_partial, psum, counter, sel_bias);
     return cudaGetLastError();
   };
   cudaError_t err = c.E <= 8 ? run(route_warp_kernel<8>)

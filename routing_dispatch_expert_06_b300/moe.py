@@ -42,7 +42,7 @@ class Config(ctypes.Structure):
 
 _TENSOR_FIELDS = ["x", "Wr", "br", "W1", "b1", "W2", "b2", "logits", "topk_ids", "topk_w",
                   "psum", "counts", "kept", "offsets", "slot_row", "row_token", "xd", "H", "yd",
-                  "y", "f", "pbar", "l_aux"]
+                  "y", "f", "pbar", "l_aux", "sel_bias", "health"]
 
 
 class Tensors(ctypes.Structure):
@@ -70,6 +70,8 @@ def load():
         "moe_workspace_size": (st, [cfgp, ctypes.POINTER(sz)]),
         "moe_workspace_init": (st, [_P, sz, _P]),
         "moe_route": (st, [cfgp, _P, _P, _P, _P, _P, _P, _P, _P, sz, _P]),
+        "moe_route_sel": (st, [cfgp, _P, _P, _P, _P, _P, _P, _P, _P, _P, sz, _P]),
+        "moe_routing_health": (st, [cfgp, _P, _P, _P, _P]),
         "moe_dispatch": (st, [cfgp, _P, _P, _P, _P, _P, _P, _P, _P, _P, sz, _P]),
         "moe_dispatch_noalloc": (st, [cfgp, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
         "moe_ffn_up": (st, [cfgp, _P, _P, _P, _P, _P, _P, sz, _P]),
@@ -163,8 +165,10 @@ def workspace(cfg: Config, device="cuda", stream=None) -> torch.Tensor:
     return ws
 
 
-def allocate(cfg: Config, device="cuda") -> dict:
-    """Allocate every output and intermediate tensor of one forward pass."""
+def allocate(cfg: Config, device="cuda", health: bool = False) -> dict:
+    """Allocate every output and intermediate tensor of one forward pass
+    (``health``: also the 4 routing-health indicators, which forward() then
+    computes)."""
     dt = act_dtype(cfg)
     T, d, d_ff, E, k = cfg.T, cfg.d, cfg.d_ff, cfg.E, cfg.k
     R = max(max_rows(cfg), 1)
@@ -186,14 +190,28 @@ def allocate(cfg: Config, device="cuda") -> dict:
         f=torch.empty(E, dtype=torch.float32, **z),
         pbar=torch.empty(E, dtype=torch.float32, **z),
         l_aux=torch.empty(1, dtype=torch.float32, **z),
+        health=torch.empty(4, dtype=torch.float32, **z) if health else None,
     )
 
 
-def route(cfg, x, Wr, br, out, ws, stream=None):
-    _check(load().moe_route(ctypes.byref(cfg), _ptr(x), _ptr(Wr), _ptr(br),
-                            _ptr(out.get("logits")), _ptr(out["topk_ids"]),
-                            _ptr(out["topk_w"]), _ptr(out["psum"]), _ptr(ws), ws.numel(),
-                            _stream(stream)))
+def route(cfg, x, Wr, br, out, ws, stream=None, sel_bias=None):
+    """moe_route, or moe_route_sel when ``sel_bias`` (fp32 [E]) is given."""
+    if sel_bias is None:
+        _check(load().moe_route(ctypes.byref(cfg), _ptr(x), _ptr(Wr), _ptr(br),
+                                _ptr(out.get("logits")), _ptr(out["topk_ids"]),
+                                _ptr(out["topk_w"]), _ptr(out["psum"]), _ptr(ws), ws.numel(),
+                                _stream(stream)))
+    else:
+        _check(load().moe_route_sel(ctypes.byref(cfg), _ptr(x), _ptr(Wr), _ptr(br),
+                                    _ptr(sel_bias), _ptr(out.get("logits")),
+                                    _ptr(out["topk_ids"]), _ptr(out["topk_w"]),
+                                    _ptr(out["psum"]), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def routing_health(cfg, counts, kept, health, stream=None):
+    """moe_routing_health: health[4] from counts and kept."""
+    _check(load().moe_routing_health(ctypes.byref(cfg), _ptr(counts), _ptr(kept), _ptr(health),
+                                     _stream(stream)))
 
 
 def dispatch(cfg, x, topk_ids, out, ws, stream=None):

@@ -66,13 +66,15 @@ def assert_float(got, ref, dtype, what=""):
         assert_rel_rms(got, ref, 1e-4, what)
 
 
-def run_gpu(wl, inp=None, expert_bias=False, alpha=1.0, stages=False):
-    """Run the layer through the C ABI; return (cfg, inputs, outputs, ws)."""
+def run_gpu(wl, inp=None, expert_bias=False, alpha=1.0, stages=False, health=False):
+    """Run the layer through the C ABI; return (cfg, inputs, outputs, ws).
+    An ``inp["sel_bias"]`` routes with the selection-only bias; ``health``
+    also asks for the routing-health indicators."""
     if inp is None:
         inp = inputs.make_inputs(wl, "cuda", expert_bias=expert_bias)
     cfg = moe.config_from_workload(wl, write_logits=True)
     ws = moe.workspace(cfg)
-    out = moe.allocate(cfg)
+    out = moe.allocate(cfg, health=health)
     if stages:
         moe.forward_stages(cfg, inp, out, ws, alpha)
     else:
@@ -121,7 +123,9 @@ def oracle_yd(wl, inp, xd_rows, rows, offsets):
 
 def check_forward(wl, inp, out, alpha=1.0, full=False, max_rows_check=None, n_tokens=None,
                   max_experts=None, e2e_tokens=64, seed=0):
-    """Compare every output of one forward pass with the oracle."""
+    """Compare every output of one forward pass with the oracle (routing with
+    inp["sel_bias"] when present; out["health"] when present)."""
+    sel_bias = h(inp["sel_bias"]) if inp.get("sel_bias") is not None else None
     T, E, k, d = wl.T, wl.E, wl.k, wl.d
     x = h(inp["x"])
     Wr, br = h(inp["Wr"]), h(inp["br"])
@@ -137,7 +141,7 @@ def check_forward(wl, inp, out, alpha=1.0, full=False, max_rows_check=None, n_to
     assert_rel_rms(logits[tok_l], ref_logits, 1e-5, "logits")
 
     # 2. selection on the device's own logits: ids bit-exact, weights, psum
-    ids_ref, w_ref, psum_ref, _ = oracle.select(logits, k, wl.renormalize)
+    ids_ref, w_ref, psum_ref, _ = oracle.select(logits, k, wl.renormalize, sel_bias=sel_bias)
     np.testing.assert_array_equal(h(out["topk_ids"]), ids_ref, "topk_ids")
     assert_rel_rms(h(out["topk_w"]), w_ref, 1e-4, "topk_w")
     assert_rel_rms(h(out["psum"]), psum_ref, 1e-4, "psum")
@@ -205,4 +209,10 @@ def check_forward(wl, inp, out, alpha=1.0, full=False, max_rows_check=None, n_to
     assert_rel_rms(h(out["f"]), f_ref, 1e-6, "f")
     assert_rel_rms(h(out["pbar"]), pbar_ref, 1e-4, "pbar")
     assert abs(float(h(out["l_aux"])[0]) - l_ref) <= 1e-4 * abs(l_ref) + 1e-7
+
+    # 9. routing health
+    if out.get("health") is not None:
+        ref = oracle.routing_health(fl["counts"], fl["kept"], T, k)
+        np.testing.assert_allclose(h(out["health"]), ref, rtol=1e-4, atol=1e-6,
+                                   err_msg="health")
     return dict(n_rows=n, rows_checked=len(rows), tokens_e2e=len(toks))

@@ -206,3 +206,35 @@ def test_dropless_capacity_keeps_every_slot():
     np.testing.assert_array_equal(h(out["counts"]), h(out["kept"]))
     assert int(h(out["offsets"])[-1]) == wl.T * wl.k
     check_forward(wl, inp, out, e2e_tokens=64)
+
+
+@pytest.mark.parametrize("name", ["bf16_t8192_d2048_e64_top6", "fp32_t512_d128_e8_top2",
+                                  "decode_bf16_t64_d7168_e256_top8"])
+def test_forward_with_selection_bias_and_health(name):
+    # The whole layer routed with a selection-only bias, with the routing-
+    # health indicators computed in the dispatch; every output against the
+    # oracle routed with the same bias.
+    wl = W[name]
+    if wl.T > 4096:
+        wl = wl.replace(T=3000)
+    inp = inputs.make_inputs(wl, "cuda", expert_bias=True)
+    inp["sel_bias"] = torch.randn(wl.E, generator=torch.Generator("cuda").manual_seed(3),
+                                  device="cuda")
+    _, inp, out, _ = run_gpu(wl, inp=inp, health=True)
+    check_forward(wl, inp, out, full=wl.T <= 3000)
+
+
+def test_routing_health_call_matches_oracle():
+    import oracle
+    rng = np.random.default_rng(8)
+    for E, T, k in [(8, 4096, 2), (256, 32768, 8), (1, 5, 1), (1024, 300, 16)]:
+        counts = rng.multinomial(T * k, rng.dirichlet(np.full(E, 0.3))).astype(np.int32)
+        kept = np.minimum(counts, int(1.1 * T * k / E) + 1).astype(np.int32)
+        wl = inputs.Workload("h", T, 64, 64, E, k, 1.0, True, "gelu_tanh", "bf16", 0, "zero")
+        cfg = moe.config_from_workload(wl)
+        hdev = torch.empty(4, dtype=torch.float32, device="cuda")
+        moe.routing_health(cfg, torch.as_tensor(counts, device="cuda"),
+                           torch.as_tensor(kept, device="cuda"), hdev)
+        torch.cuda.synchronize()
+        ref = oracle.routing_health(counts, kept, T, k)
+        np.testing.assert_allclose(h(hdev), ref, rtol=1e-4, atol=1e-6)

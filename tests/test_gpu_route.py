@@ -162,3 +162,55 @@ def test_column_sums_repeat_exactly_and_match_the_whole_layer(case):
     ref_logits = oracle.router_logits(h(inp["x"]), h(inp["Wr"]), h(inp["br"]))
     _, _, psum, _ = oracle.select(ref_logits, k, True)
     assert_rel_rms(runs[0], psum, 1e-4, "psum")
+
+
+def _route_sel(wl, inp, impl, sel_bias):
+    cfg = moe.config_from_workload(wl, write_logits=True)
+    ws = moe.workspace(cfg)
+    out = moe.allocate(cfg)
+    os.environ["MOE_ROUTE_IMPL"] = impl
+    try:
+        moe.route(cfg, inp["x"], inp["Wr"], inp["br"], out, ws, sel_bias=sel_bias)
+        torch.cuda.synchronize()
+    finally:
+        os.environ.pop("MOE_ROUTE_IMPL", None)
+    assert moe.device_status(ws) == moe.MOE_OK
+    return out
+
+
+@pytest.mark.parametrize("impl", ["warp", "tc", "simt"])
+@pytest.mark.parametrize("case", [(300, 200, 20, 3, True), (5000, 1024, 8, 2, True),
+                                  (1000, 520, 256, 16, False), (4097, 2048, 64, 6, True),
+                                  (9, 7168, 256, 8, False)],
+                         ids=lambda c: f"t{c[0]}_e{c[2]}_k{c[3]}")
+def test_selection_bias_matches_oracle(case, impl):
+    # Experts are ranked by logit + sel_bias (fp32); the weights, Σp and
+    # logits stay the unbiased ones.  The bias must change many choices.
+    T, d, E, k, renorm = case
+    wl = _workload(T, d, E, k, renorm, "normal:1.0", seed=13)
+    inp = inputs.make_inputs(wl, "cuda")
+    sb = torch.randn(E, generator=torch.Generator("cuda").manual_seed(7), device="cuda") * 1.5
+    out = _route_sel(wl, inp, impl, sb)
+    logits = h(out["logits"])
+    ids, w, psum, _ = oracle.select(logits, k, renorm, sel_bias=h(sb))
+    np.testing.assert_array_equal(h(out["topk_ids"]), ids, "topk_ids")
+    assert_rel_rms(h(out["topk_w"]), w, 1e-4, "topk_w")
+    assert_rel_rms(h(out["psum"]), psum, 1e-4, "psum")
+    plain, *_ = oracle.select(logits, k, renorm)
+    if T > 100:
+        assert (plain != ids).any(axis=1).mean() > 0.1
+
+
+@pytest.mark.parametrize("impl", ["warp", "tc", "simt"])
+def test_selection_bias_ties_go_to_lower_index(impl):
+    # W_r = 0 and b_r = 0: every logit is 0, so the keys are the bias, which
+    # repeats values; equal keys must go to the lower expert index, and the
+    # weights are the unbiased uniform 1/k.
+    T, d, E, k = 200, 128, 24, 5
+    wl = _workload(T, d, E, k, True, "zero")
+    inp = inputs.make_inputs(wl, "cuda")
+    inp["Wr"].zero_()
+    sb = torch.tensor([0.5, 1.0, 1.0, 0.25, 1.0, 0.5] * 4, device="cuda")
+    out = _route_sel(wl, inp, impl, sb)
+    assert (h(out["topk_ids"]) == np.array([1, 2, 4, 7, 8], np.int32)).all()
+    np.testing.assert_allclose(h(out["topk_w"]), 0.2, rtol=1e-6)
