@@ -238,6 +238,10 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--alpha", type=float, default=0.01)
+    ap.add_argument("--sel-bias", action="store_true",
+                    help="route with a seeded selection-only expert bias")
+    ap.add_argument("--health", action="store_true",
+                    help="also compute the routing-health indicators in the forward pass")
     args = ap.parse_args()
     wl = inputs.WORKLOADS[args.workload]
 
@@ -264,12 +268,14 @@ def main():
 
     dev = torch.device("cuda", local_rank)
     inp = inputs.make_inputs(wl, dev)
+    if args.sel_bias:
+        inp["sel_bias"] = inputs.selection_bias(wl, dev)
     if world > 1:  # each replica routes its own batch
         g = torch.Generator(device=dev).manual_seed(wl.seed * 1000 + rank)
         inp["x"] = torch.randn(inp["x"].shape, generator=g, device=dev).to(inp["x"].dtype)
     cfg = moe.config_from_workload(wl, write_logits=False)
     ws = moe.workspace(cfg, dev)
-    out = moe.allocate(cfg, dev)
+    out = moe.allocate(cfg, dev, health=args.health)
     stream = torch.cuda.current_stream(dev)
     flush_w = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     flush_r = torch.ones(512 << 20, dtype=torch.uint8, device=dev)
@@ -292,7 +298,8 @@ def main():
     g_full = capture(lambda: moe.forward(cfg, inp, out, ws, args.alpha))
     per_forward = moe.launch_count() - launches0
     stage_calls = {
-        "route": lambda: moe.route(cfg, inp["x"], inp["Wr"], inp["br"], out, ws),
+        "route": lambda: moe.route(cfg, inp["x"], inp["Wr"], inp["br"], out, ws,
+                                   sel_bias=inp.get("sel_bias")),
         "dispatch": lambda: moe.dispatch(cfg, inp["x"], out["topk_ids"], out, ws),
         "ffn_up": lambda: moe.ffn_up(cfg, out["xd"], out["offsets"], inp["W1"], inp["b1"],
                                      out["H"], ws),
@@ -425,6 +432,7 @@ def main():
         config=dict(workload=wl.name, T=wl.T, d=wl.d, d_ff=wl.d_ff, E=wl.E, k=wl.k,
                     capacity_factor=wl.capacity_factor, renormalize=wl.renormalize,
                     act=wl.act, parallelism=f"replicas{world}" if world > 1 else "single",
+                    sel_bias=bool(args.sel_bias), health=bool(args.health),
                     l2="flushed between steps (512 MiB write, then 512 MiB read)"),
         roofline=dict(bound="tensor", kernel=f"{dom} (tcgen05 grouped GEMM)",
                       achieved=dom_tflops, peak=peaks["bf16"], unit="TFLOP/s",

@@ -129,6 +129,14 @@ def make_inputs(wl: Workload, device="cpu", expert_bias: bool = False, seed: int
     return dict(x=x, Wr=Wr, br=br, W1=W1, b1=b1, W2=W2, b2=b2)
 
 
+def selection_bias(wl: Workload, device="cpu") -> torch.Tensor:
+    """A seeded per-expert selection bias, N(0, 1) fp32 [E] (seed: the
+    workload's + 7919), for routing with a selection-only bias."""
+    gen = torch.Generator(device=torch.device(device))
+    gen.manual_seed(wl.seed + 7919)
+    return torch.randn(wl.E, generator=gen, device=device, dtype=torch.float32)
+
+
 def to_numpy(t: torch.Tensor) -> np.ndarray:
     """Host copy; bf16 becomes a uint16 array of the same bit patterns."""
     t = t.detach().contiguous()

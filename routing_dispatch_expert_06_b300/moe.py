@@ -284,7 +284,8 @@ def forward_stages(cfg, inputs: dict, out: dict, ws, alpha=0.01, stream=None, ev
             events[i].record(s)
 
     mark(0)
-    route(cfg, inputs["x"], inputs["Wr"], inputs["br"], out, ws, s)
+    route(cfg, inputs["x"], inputs["Wr"], inputs["br"], out, ws, s,
+          sel_bias=inputs.get("sel_bias"))
     mark(1)
     dispatch(cfg, inputs["x"], out["topk_ids"], out, ws, s)
     mark(2)
@@ -295,6 +296,8 @@ def forward_stages(cfg, inputs: dict, out: dict, ws, alpha=0.01, stream=None, ev
     combine(cfg, out["yd"], out["slot_row"], out["topk_w"], out["y"], s)
     mark(5)
     aux_stats(cfg, out["counts"], out["psum"], alpha, out["f"], out["pbar"], out["l_aux"], s)
+    if out.get("health") is not None:
+        routing_health(cfg, out["counts"], out["kept"], out["health"], s)
     mark(6)
 
 

@@ -65,14 +65,19 @@ def test_expert_bias_path():
     check_forward(wl, inp, out, full=True)
 
 
-def test_stage_calls_equal_forward_and_are_deterministic():
+@pytest.mark.parametrize("extras", [False, True], ids=["plain", "sel_bias_health"])
+def test_stage_calls_equal_forward_and_are_deterministic(extras):
     wl = W["bf16_t8192_d2048_e64_top6"].replace(T=3000)
-    _, inp, out1, _ = run_gpu(wl)
-    _, _, out2, _ = run_gpu(wl, inp=inp, stages=True)
-    _, _, out3, _ = run_gpu(wl, inp=inp)
+    inp = inputs.make_inputs(wl, "cuda")
+    if extras:
+        inp["sel_bias"] = inputs.selection_bias(wl, "cuda")
+    _, inp, out1, _ = run_gpu(wl, inp=inp, health=extras)
+    _, _, out2, _ = run_gpu(wl, inp=inp, stages=True, health=extras)
+    _, _, out3, _ = run_gpu(wl, inp=inp, health=extras)
     n = int(h(out1["offsets"])[-1])
-    for name in ["logits", "topk_ids", "topk_w", "psum", "counts", "kept", "offsets",
-                 "slot_row", "f", "pbar", "l_aux", "y"]:
+    names = ["logits", "topk_ids", "topk_w", "psum", "counts", "kept", "offsets",
+             "slot_row", "f", "pbar", "l_aux", "y"] + (["health"] if extras else [])
+    for name in names:
         for o in (out2, out3):
             assert torch.equal(out1[name], o[name]), name
     for name in ["row_token", "xd", "H", "yd"]:
