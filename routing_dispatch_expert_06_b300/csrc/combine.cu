@@ -67,6 +67,8 @@ __global__ void __launch_bounds__(256)
   constexpr int NV = Vec<T>::N;
   const int lane = threadIdx.x & 31;
   const int64_t warps = int64_t(gridDim.x) * (blockDim.x >> 5);
+  pdl_wait();
+  pdl_trigger();
   for (int64_t it = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
        it < n_tok * n_parts; it += warps) {
     const int64_t t = it / n_parts;
@@ -149,10 +151,11 @@ cudaError_t launch_combine(const moe_config_t& c, int64_t max_rows, const void* 
   const int sms = device_sms();
   const int64_t want = (c.T * rs.n_parts + 7) / 8;
   const unsigned grid = unsigned(want < int64_t(sms) * 8 ? want : int64_t(sms) * 8);
+  cudaError_t err = cudaSuccess;
   auto run = [&](auto kernel) {
-    kernel<<<grid, 256, 0, st>>>(c.T, c.k, row_vecs, rs.n_parts, rs.part_vecs, max_rows,
-                                 static_cast<const uint4*>(yd), slot_row, w,
-                                 static_cast<uint4*>(y));
+    err = launch_pdl(kernel, dim3(grid), dim3(256), 0, st, c.T, c.k, row_vecs, rs.n_parts,
+                     rs.part_vecs, max_rows, static_cast<const uint4*>(yd), slot_row, w,
+                     static_cast<uint4*>(y));
   };
   if (c.dtype == MOE_DT_BF16) {
     if (c.k <= 2) run(combine_kernel<__nv_bfloat16, 2>);
@@ -166,7 +169,7 @@ cudaError_t launch_combine(const moe_config_t& c, int64_t max_rows, const void* 
     else run(combine_kernel<float, 16>);
   }
   count_launch();
-  return cudaGetLastError();
+  return err != cudaSuccess ? err : cudaGetLastError();
 }
 
 cudaError_t launch_aux(const moe_config_t& c, const int32_t* counts, const float* psum,

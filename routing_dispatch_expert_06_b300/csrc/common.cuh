@@ -1,6 +1,7 @@
 // Shared device helpers for the MoE-layer kernels (sm_103a).
 #pragma once
 
+#include <utility>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -205,6 +206,35 @@ inline RowSplit row_split(int64_t T, int64_t row_vecs, int64_t min_part) {
   if (parts < 1) parts = 1;
   const int64_t pv = (row_vecs + parts - 1) / parts;
   return {(row_vecs + pv - 1) / pv, pv};
+}
+
+// Programmatic dependent launch.  A kernel launched with launch_pdl may be
+// scheduled while the previous kernel in the stream is still running: it
+// calls pdl_wait() before it reads or writes anything that kernel touches
+// (pdl_wait returns once that kernel has completed and its writes are
+// visible), then pdl_trigger(), which lets the next kernel be scheduled.
+// Triggering only after the wait keeps every earlier kernel complete by the
+// time any later one passes its own wait.  Without a programmatic dependency
+// both are no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 // Record the first asynchronous error in the status word.

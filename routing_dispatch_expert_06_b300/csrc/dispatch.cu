@@ -90,6 +90,8 @@ __global__ void __launch_bounds__(kDispatchThreads)
   __shared__ float s_red[kAuxThreads];
   __shared__ unsigned long long s_kept_sum;
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+  pdl_wait();
+  pdl_trigger();
   __syncthreads();
   const int64_t t = int64_t(blockIdx.x) * kChunkTokens + threadIdx.x;
   if (t < T) {
@@ -167,6 +169,8 @@ __global__ void __launch_bounds__(kDispatchThreads)
   __shared__ int32_t part[kDispatchThreads];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t chunk0 = int64_t(blockIdx.x) * kChunkTokens;
+  pdl_wait();
+  pdl_trigger();
   {
     // The chunk's ids, coalesced, once.
     const int64_t n_ids = (T - chunk0 < kChunkTokens ? T - chunk0 : kChunkTokens) * k;
@@ -251,6 +255,8 @@ __global__ void __launch_bounds__(256)
                         uint4* __restrict__ xd) {
   const int lane = threadIdx.x & 31;
   const int64_t warps = int64_t(gridDim.x) * (blockDim.x >> 5);
+  pdl_wait();
+  pdl_trigger();
   for (int64_t it = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
        it < T * n_parts; it += warps) {
     const int64_t t = it / n_parts;
@@ -293,10 +299,11 @@ cudaError_t launch_dispatch(const moe_config_t& c, int64_t C, const void* x,
       (aux && counter) ? *aux
                        : AuxArgs{0.f, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
   cudaError_t err;
-  histogram_kernel<<<unsigned(n_chunks), kDispatchThreads, size_t(c.E) * 4, st>>>(
-      c.T, c.E, c.k, ids, chunk_counts, status, counter, C, counts, kept, aux_v);
+  err = launch_pdl(histogram_kernel, dim3(unsigned(n_chunks)), dim3(kDispatchThreads),
+                   size_t(c.E) * 4, st, c.T, c.E, c.k, ids, chunk_counts, status, counter, C,
+                   counts, kept, aux_v);
   count_launch();
-  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  if (err != cudaSuccess || (err = cudaGetLastError()) != cudaSuccess) return err;
   if (!counter) {
     expert_scan_kernel<<<unsigned(c.E), 256, 0, st>>>(n_chunks, c.E, C, chunk_counts, counts,
                                                        kept);
@@ -306,20 +313,22 @@ cudaError_t launch_dispatch(const moe_config_t& c, int64_t C, const void* x,
   const size_t smem = size_t(c.E + 1 + 8 * c.E + kChunkTokens * c.k) * 4;
   err = ensure_dynamic_smem(reinterpret_cast<const void*>(assign_kernel), smem);
   if (err != cudaSuccess) return err;
-  assign_kernel<<<unsigned(n_chunks), kDispatchThreads, smem, st>>>(
-      c.T, c.E, c.k, C, ids, chunk_counts, kept, offsets, slot_row, row_token);
+  err = launch_pdl(assign_kernel, dim3(unsigned(n_chunks)), dim3(kDispatchThreads), smem, st,
+                   c.T, c.E, c.k, C, ids, static_cast<const int32_t*>(chunk_counts),
+                   static_cast<const int32_t*>(kept), offsets, slot_row, row_token);
   count_launch();
-  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  if (err != cudaSuccess || (err = cudaGetLastError()) != cudaSuccess) return err;
   const int elem = c.dtype == MOE_DT_BF16 ? 2 : 4;
   const int64_t row_vecs = int64_t(c.d) * elem / 16;
   const RowSplit rs = row_split(c.T, row_vecs, 128);
   const int sms = device_sms();
   const int64_t want = (c.T * rs.n_parts + 7) / 8;
   const unsigned grid = unsigned(want < int64_t(sms) * 8 ? want : int64_t(sms) * 8);
-  scatter_rows_kernel<<<grid, 256, 0, st>>>(c.T, c.k, row_vecs, rs.n_parts, rs.part_vecs,
-                                            static_cast<const uint4*>(x), slot_row,
-                                            static_cast<uint4*>(xd));
+  err = launch_pdl(scatter_rows_kernel, dim3(grid), dim3(256), 0, st, c.T, c.k, row_vecs,
+                   rs.n_parts, rs.part_vecs, static_cast<const uint4*>(x), slot_row,
+                   static_cast<uint4*>(xd));
   count_launch();
+  if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
 

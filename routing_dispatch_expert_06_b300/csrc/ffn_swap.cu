@@ -100,6 +100,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::tmem_alloc(&s_tmem, kTmemCols);
     tc::tmem_relinquish();
   }
+  // Launched with programmatic dependent launch: offsets and the A rows come
+  // from the previous kernels.
+  tc::grid_dependency_wait();
+  tc::grid_launch_dependents();
   // Prefix over experts of "has rows": warp 0 scans runs of experts, one run
   // per lane.  Offsets are clamped to [0, max_rows].
   if (warp == 0) {
@@ -301,10 +305,10 @@ cudaError_t launch_nt(const CUtensorMap& tmA, const CUtensorMap& tmB, int E, int
   const size_t smem = 1024 + size_t(stages) * stage_bytes;
   cudaError_t err = ensure_dynamic_smem(kp, smem);
   if (err != cudaSuccess) return err;
-  kernel<<<unsigned(device_sms()), kThreads, smem, st>>>(
-      tmA, tmB, E, N, K, offsets, bias, static_cast<__nv_bfloat16*>(out), max_rows, status,
-      stages);
-  return cudaGetLastError();
+  err = launch_pdl(kernel, dim3(unsigned(device_sms())), dim3(kThreads), smem, st, tmA, tmB, E,
+                   N, K, offsets, bias, static_cast<__nv_bfloat16*>(out), max_rows, status,
+                   stages);
+  return err != cudaSuccess ? err : cudaGetLastError();
 }
 
 template <int NT>

@@ -191,6 +191,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::tmem_relinquish();
     }
   }
+  // Launched with programmatic dependent launch: offsets and the A rows come
+  // from the previous kernels.  The tail launch instead starts while its pair
+  // launch runs (which has waited already) and waits at its end.
+  if (set != kTail) {
+    tc::grid_dependency_wait();
+    tc::grid_launch_dependents();
+  }
   // Per-expert m-tile prefix: warp 0 scans runs of experts, one run per lane.
   // Row offsets are clamped to [0, max_rows] so that no tile can reach
   // outside the buffers, whatever offsets holds.
@@ -226,9 +233,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem_base = s_tmem;
-  // The pair launch lets the tail launch start early: its CTAs take SMs as
-  // pair CTAs finish (the tiles are independent).
-  if (set == kPairBody && threadIdx.x == 0) tc::grid_launch_dependents();
 
   const int n_tn = (N + BN - 1) / BN;
   const int64_t total = int64_t(s_mt[E]) * n_tn;
@@ -504,16 +508,10 @@ cudaError_t launch_variant(int act, const CUtensorMap& tmA, const CUtensorMap& t
     if (e != cudaSuccess) return e;
     unsigned grid = unsigned(sms);
     cudaLaunchConfig_t cfg{};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    if (set == kTail) {
-      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-      attr[0].val.programmaticStreamSerializationAllowed = 1;
-      cfg.attrs = attr;
-      cfg.numAttrs = 1;
-    }
     if constexpr (PAIR) {
       // Persistent grid: as many CTA pairs as can be resident at once.
       attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -530,6 +528,12 @@ cudaError_t launch_variant(int act, const CUtensorMap& tmA, const CUtensorMap& t
       grid = unsigned(2 * clusters);
     }
     cfg.gridDim = dim3(grid);
+    // Programmatic dependent launch on every launch (see the kernel's
+    // prologue): the grid is scheduled while the previous kernel finishes.
+    attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs += 1;
     e = cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, E, N, K, BN, offsets, bias,
                            static_cast<__nv_bfloat16*>(out), max_rows, status, stages, set);
     if (e != cudaSuccess) return e;

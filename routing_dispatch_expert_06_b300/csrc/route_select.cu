@@ -152,6 +152,7 @@ __global__ void __launch_bounds__(kSelWarps * 32)
   __syncthreads();
   // The partial logits come from the preceding router grid.
   tc::grid_dependency_wait();
+  tc::grid_launch_dependents();
 
   // Groups of rows_per_group tokens: group b, b + grid, ...; in a group, slot
   // `slot` takes tokens slot·RPW .. slot·RPW + RPW - 1, one per lane segment.

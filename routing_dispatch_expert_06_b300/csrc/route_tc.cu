@@ -116,6 +116,9 @@ __global__ void __launch_bounds__(64 + 128 * G, 1)
   tc::fence_after_sync();
   const uint32_t tmem_base = s_tmem;
   volatile int* abort_flag = &s_abort;
+  // The select kernel may be scheduled from now on; it waits for this grid to
+  // finish and flush before reading the partial logits.
+  tc::grid_launch_dependents();
   auto give_up = [&]() {
     *abort_flag = 1;
     set_status(a.status, MOE_ERR_TIMEOUT);
@@ -257,9 +260,6 @@ __global__ void __launch_bounds__(64 + 128 * G, 1)
     __syncwarp();
     tc::tmem_dealloc(tmem_base, a.tmem_cols);
   }
-  // The select kernel may be scheduled now; it waits for this grid to finish
-  // and flush before reading the partial logits.
-  tc::grid_launch_dependents();
 }
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
