@@ -67,7 +67,8 @@ def _get():
             lib.oracle_num_threads.restype = ctypes.c_int
             lib.oracle_activation.argtypes = [i64, i32, P, P]
             lib.oracle_router_logits.argtypes = [i64, i32, i32, P, i32, P, i32, P, P]
-            lib.oracle_select.argtypes = [i64, i32, i32, i32, P, P, P, P, P, P]
+            lib.oracle_select.argtypes = [i64, i32, i32, i32, P, P, P, P, P, P, P]
+            lib.oracle_fill_reroute.argtypes = [i64, i32, i32, i64, P, P, P, P, P, P, P, P]
             lib.oracle_fill.argtypes = [i64, i32, i32, i64, P, P, P, P, P, P]
             lib.oracle_permute.argtypes = [i64, i64, P, P, P]
             lib.oracle_ffn_rows.argtypes = [i32, i32, i32, P, i64, P, P, i32, P, P, P, P, i32,
@@ -122,14 +123,16 @@ def router_logits(x, Wr, br):
     return out
 
 
-def select(logits32, k: int, renormalize: bool, want_probs: bool = False, sel_bias=None):
+def select(logits32, k: int, renormalize: bool, want_probs: bool = False, sel_bias=None,
+           want_cand: bool = False):
     """[§2.1, §2.2] softmax, top-k (ties to the lower index), weights, Σ_t p.
 
     ``logits32`` are fp32 scores (the oracle's own, rounded, or a device's).
     ``sel_bias`` (fp32 [E] or None): experts are ranked by the fp32 sum
     score + sel_bias; the weights still come from the unbiased softmax.
     Returns (topk_ids int32 [T,k], topk_w float64 [T,k], psum float64 [E],
-    probs float64 [T,E] or None).
+    probs float64 [T,E] or None), and with ``want_cand`` also cand int32
+    [T,k]: the experts of rank k .. 2k-1 (-1 past E).
     """
     s = _c(logits32, np.float32)
     T, E = s.shape
@@ -138,8 +141,11 @@ def select(logits32, k: int, renormalize: bool, want_probs: bool = False, sel_bi
     w = np.empty((T, k), np.float64)
     psum = np.empty(E, np.float64)
     probs = np.empty((T, E), np.float64) if want_probs else None
+    cand = np.empty((T, k), np.int32) if want_cand else None
     _get().oracle_select(T, E, int(k), int(bool(renormalize)), _p(s), _p(sb), _p(ids), _p(w),
-                         _p(probs), _p(psum))
+                         _p(probs), _p(psum), _p(cand))
+    if want_cand:
+        return ids, w, psum, probs, cand
     return ids, w, psum, probs
 
 
@@ -228,6 +234,27 @@ def aux(counts, psum, T: int, alpha: float):
     return f, pbar, float(l[0])
 
 
+def fill_reroute(topk_ids, cand, E: int, C: int):
+    """[§4.3] first-come fill, then each overflowing slot offered once to its
+    token's next candidate (see oracle_fill_reroute).  Returns fill()'s dict
+    plus slot_expert [T,k] (the expert that processes each slot, -1 dropped).
+    """
+    ids = _c(topk_ids, np.int32)
+    cd = _c(cand, np.int32)
+    T, k = ids.shape
+    counts = np.empty(E, np.int32)
+    kept = np.empty(E, np.int32)
+    offsets = np.empty(E + 1, np.int32)
+    slot_row = np.empty((T, k), np.int32)
+    slot_expert = np.empty((T, k), np.int32)
+    row_token = np.full(max(T * k, 1), -1, np.int32)
+    _get().oracle_fill_reroute(T, int(E), k, int(C), _p(ids), _p(cd), _p(counts), _p(kept),
+                               _p(offsets), _p(slot_row), _p(row_token), _p(slot_expert))
+    n_rows = int(offsets[E])
+    return dict(counts=counts, kept=kept, offsets=offsets, slot_row=slot_row,
+                row_token=row_token[:n_rows].copy(), slot_expert=slot_expert)
+
+
 def routing_health(counts, kept, T: int, k: int):
     """Routing-health indicators from counts (before capacity) and kept rows:
     (entropy of counts/(T·k) in nats, variance of counts, variance of kept,
@@ -241,7 +268,7 @@ def routing_health(counts, kept, T: int, k: int):
 
 def forward(x, Wr, br, W1, b1, W2, b2, *, k: int, capacity_factor: float, renormalize: bool,
             act: int, alpha: float = 1.0, logits32=None, tokens=None, round_h: int = 0,
-            sel_bias=None):
+            sel_bias=None, reroute: bool = False):
     """The whole layer, step by step in the article's order.
 
     ``logits32``: fp32 scores to route on (a device's own); default: the
@@ -258,11 +285,11 @@ def forward(x, Wr, br, W1, b1, W2, b2, *, k: int, capacity_factor: float, renorm
         out["logits_f64"] = ld
         logits32 = ld.astype(np.float32)
     out["logits"] = np.asarray(logits32, np.float32)
-    ids, w, psum, _ = select(logits32, k, renormalize, sel_bias=sel_bias)
-    out.update(topk_ids=ids, topk_w=w, psum=psum)
+    ids, w, psum, _, cand = select(logits32, k, renormalize, sel_bias=sel_bias, want_cand=True)
+    out.update(topk_ids=ids, topk_w=w, psum=psum, cand=cand)
     C = capacity(T, k, E, capacity_factor)
     out["C"] = C
-    fl = fill(ids, E, C)
+    fl = fill_reroute(ids, cand, E, C) if reroute else fill(ids, E, C)
     out.update(fl)
     f, pbar, l_aux = aux(fl["counts"], psum, T, alpha)
     out.update(f=f, pbar=pbar, l_aux=l_aux)

@@ -158,9 +158,11 @@ void oracle_router_logits(int64_t T, int32_t d, int32_t E, const void* x, int32_
 // experts are ranked by key_i = s_{t,i} + sel_bias_i, formed in fp32 (a
 // float addition, the precision the selection is taken in), and the weights
 // above still use the unbiased p.
+// cand (nullable, [T,k]): the experts ranked k .. 2k-1 by the same keys (the
+// next candidates of the ranked list, [MoE 模型原理 §4.3]), -1 past E.
 void oracle_select(int64_t T, int32_t E, int32_t k, int32_t renormalize, const float* logits,
                    const float* sel_bias, int32_t* topk_ids, double* topk_w,
-                   double* probs /*nullable, [T,E]*/, double* psum) {
+                   double* probs /*nullable, [T,E]*/, double* psum, int32_t* cand) {
   std::vector<double> p_all(static_cast<size_t>(T) * E);
   parallel_for(T, [&](int64_t t) {
     const float* s = logits + t * E;
@@ -192,6 +194,18 @@ void oracle_select(int64_t T, int32_t E, int32_t k, int32_t renormalize, const f
     for (int32_t r = 0; r < k; ++r) {
       double pr = p[topk_ids[t * k + r]];
       topk_w[t * k + r] = renormalize ? pr / sel_sum : pr;
+    }
+    if (cand) {
+      // Continue the same selection for ranks k .. 2k-1.
+      for (int32_t r = 0; r < k; ++r) {
+        int32_t best = -1;
+        for (int32_t i = 0; i < E; ++i) {
+          if (taken[i]) continue;
+          if (best < 0 || key[i] > key[best]) best = i;
+        }
+        cand[t * k + r] = best;
+        if (best >= 0) taken[best] = 1;
+      }
     }
   });
   for (int32_t i = 0; i < E; ++i) psum[i] = 0.0;
@@ -238,6 +252,68 @@ void oracle_fill(int64_t T, int32_t E, int32_t k, int64_t C, const int32_t* topk
         slot_row[t * k + r] = -1;
       }
     }
+}
+
+// [MoE 模型原理 §4.3], second policy: an overflowing slot goes to the next
+// expert of the token's candidate list.  The page leaves open whether capacity
+// is cut after the first assignment or assigned candidate by candidate; this
+// takes the first assignment as oracle_fill does, then offers the overflow:
+//   1. first-come fill in (token, rank) order: kept0[e] = min(counts[e], C);
+//   2. the m-th overflowing slot of token t (in rank order) is offered to the
+//      token's next candidate cand[t*k + m] (its expert of rank k + m); no
+//      candidate (-1): the slot stays dropped;
+//   3. offers are served first come in (token, rank) order of the offering
+//      slot, into the room C - kept0[e] left after step 1; the rest drop.
+// Buffer layout: an expert's first-fill rows, then its rerouted rows;
+// kept[e] = kept0[e] + served[e], offsets = exclusive scan of kept.  counts
+// stay those of the first choices (f_i is defined over S_t, §3.2); a
+// rerouted slot keeps its combine weight (the caller's topk_w).
+void oracle_fill_reroute(int64_t T, int32_t E, int32_t k, int64_t C, const int32_t* topk_ids,
+                         const int32_t* cand, int32_t* counts, int32_t* kept, int32_t* offsets,
+                         int32_t* slot_row, int32_t* row_token, int32_t* slot_expert) {
+  const int64_t n = T * k;
+  std::vector<int64_t> pos0(n), pos1(n, -1);
+  std::vector<int32_t> dest(n, -1);
+  std::vector<int64_t> fill(E, 0), served(E, 0), kept0(E);
+  for (int64_t s = 0; s < n; ++s) pos0[s] = fill[topk_ids[s]]++;
+  for (int32_t e = 0; e < E; ++e) {
+    counts[e] = static_cast<int32_t>(fill[e]);
+    kept0[e] = std::min<int64_t>(fill[e], C);
+  }
+  for (int64_t t = 0; t < T; ++t) {
+    int32_t m = 0;
+    for (int32_t r = 0; r < k; ++r) {
+      const int64_t s = t * k + r;
+      if (pos0[s] < C) {
+        dest[s] = topk_ids[s];
+        continue;
+      }
+      const int32_t e2 = m < k ? cand[t * k + m] : -1;
+      ++m;
+      if (e2 < 0) continue;
+      if (served[e2] < C - kept0[e2]) {
+        pos1[s] = served[e2]++;
+        dest[s] = e2;
+      }
+    }
+  }
+  offsets[0] = 0;
+  for (int32_t e = 0; e < E; ++e) {
+    kept[e] = static_cast<int32_t>(kept0[e] + served[e]);
+    offsets[e + 1] = offsets[e] + kept[e];
+  }
+  for (int64_t s = 0; s < n; ++s) {
+    int32_t row = -1;
+    if (dest[s] >= 0) {
+      const int32_t e = dest[s];
+      row = offsets[e] + static_cast<int32_t>(pos0[s] < C && dest[s] == topk_ids[s]
+                                                  ? pos0[s]
+                                                  : kept0[e] + pos1[s]);
+      row_token[row] = static_cast<int32_t>(s / k);
+    }
+    slot_row[s] = row;
+    if (slot_expert) slot_expert[s] = dest[s];
+  }
 }
 
 // [MoE 模型原理 §5]  Dispatch: gather token rows into the per-expert buffer,
