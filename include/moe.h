@@ -75,6 +75,7 @@ typedef struct moe_config {
   int32_t act;              /* MOE_ACT_* : σ of the expert FFN */
   int32_t dtype;            /* MOE_DT_* : x, weights, xd, H, yd, y */
   int32_t write_logits;     /* 1: moe_route also writes fp32 logits[T,E] */
+  int32_t reroute;          /* 1: overflow goes to the next candidate (§4.3) */
 } moe_config_t;
 
 /* Every tensor of one forward pass (all device pointers). */
@@ -136,16 +137,25 @@ moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, void* stream);
  * softmax, top-k with ties to the lower expert index, combine weights
  * (renormalised over the selected set iff cfg->renormalize), and the column
  * sums psum[i] = Σ_t p_{t,i}, deterministic: a fixed reduction order, or (the
- * tensor-core router) per-token p (T < 1024) or sums over fixed groups of 32
- * tokens rounded to 26 fraction bits and added exactly as 64-bit integers.  logits may be NULL
- * unless cfg->write_logits. */
+ * tensor-core router) each p_{t,i} rounded to 31 fraction bits and added
+ * exactly as 64-bit integers.  logits may be NULL unless cfg->write_logits.
+ * With cfg->reroute it also leaves each token's next candidates (the experts
+ * ranked k .. 2k-1) in the workspace for moe_dispatch. */
 moe_status_t moe_route(const moe_config_t* cfg, const void* x, const void* Wr, const float* br,
                        float* logits, int32_t* topk_ids, float* topk_w, float* psum, void* ws,
                        size_t ws_bytes, void* stream);
 
 /* [MoE 模型原理 §4.1–§4.3, §5] Histogram, capacity, first-come positions in
  * (token, rank) order, and the permutation xd[slot_row[t,r]] = x[t] for
- * every kept slot.  Writes counts, kept, offsets, slot_row, row_token, xd. */
+ * every kept slot.  Writes counts, kept, offsets, slot_row, row_token, xd.
+ * With cfg->reroute (§4.3, second policy) an overflowing slot is then offered
+ * to its token's next candidate (the m-th overflowing slot of a token, in
+ * rank order, to the expert ranked k + m, read from the candidates the last
+ * moe_route call left in this workspace); offers are served first come in
+ * (token, rank) order into the room each expert has left, and an expert's
+ * rerouted rows follow its own.  counts stay the first choices' (f_i is over
+ * S_t); kept, offsets, slot_row and row_token are final; a rerouted slot keeps
+ * its combine weight. */
 moe_status_t moe_dispatch(const moe_config_t* cfg, const void* x, const int32_t* topk_ids,
                           int32_t* counts, int32_t* kept, int32_t* offsets, int32_t* slot_row,
                           int32_t* row_token, void* xd, void* ws, size_t ws_bytes, void* stream);

@@ -140,6 +140,7 @@ static moe_status_t check_cfg(const moe_config_t* c) {
     return fail(MOE_ERR_UNSUPPORTED, "dtype must be MOE_DT_F32 or MOE_DT_BF16");
   if (c->act != MOE_ACT_RELU && c->act != MOE_ACT_GELU_TANH)
     return fail(MOE_ERR_UNSUPPORTED, "act must be MOE_ACT_RELU or MOE_ACT_GELU_TANH");
+  if (c->reroute != 0 && c->reroute != 1) return fail(MOE_ERR_INVALID_ARG, "reroute must be 0 or 1");
   return MOE_OK;
 }
 
@@ -161,6 +162,9 @@ static WsLayout layout_of(const moe_config_t& c) {
   L.route_part = off;
   if (route_tc_supported(c))
     off += align256(size_t(route_tc_nsplit(c)) * size_t(c.T) * c.E * sizeof(float));
+  L.reroute = off;
+  if (c.reroute)
+    off += 4 * align256(size_t(c.T) * c.k * sizeof(int32_t)) + 2 * align256(size_t(c.E) * 4);
   L.total = off;
   return L;
 }
@@ -173,6 +177,8 @@ struct Ws {
   float* psum_partial;
   float* route_part;
   unsigned long long* psum_fixed;
+  RerouteBufs rr;  // all NULL unless cfg.reroute
+  int32_t* cand;   // = rr.cand (written by the router)
 };
 
 static moe_status_t get_ws(const moe_config_t& c, void* ws, size_t ws_bytes, Ws* out) {
@@ -190,6 +196,19 @@ static moe_status_t get_ws(const moe_config_t& c, void* ws, size_t ws_bytes, Ws*
   out->psum_partial = reinterpret_cast<float*>(b + L.psum_partial);
   out->route_part = reinterpret_cast<float*>(b + L.route_part);
   out->psum_fixed = reinterpret_cast<unsigned long long*>(b + L.status + kWsPsumFixed);
+  out->rr = RerouteBufs{};
+  out->cand = nullptr;
+  if (c.reroute) {
+    const size_t tk = align256(size_t(c.T) * c.k * sizeof(int32_t));
+    char* r = b + L.reroute;
+    out->cand = reinterpret_cast<int32_t*>(r);
+    out->rr.cand = out->cand;
+    out->rr.ids1 = reinterpret_cast<int32_t*>(r + tk);
+    out->rr.pos0 = reinterpret_cast<int32_t*>(r + 2 * tk);
+    out->rr.pos1 = reinterpret_cast<int32_t*>(r + 3 * tk);
+    out->rr.kept0 = reinterpret_cast<int32_t*>(r + 4 * tk);
+    out->rr.counts1 = reinterpret_cast<int32_t*>(r + 4 * tk + align256(size_t(c.E) * 4));
+  }
   return MOE_OK;
 }
 
@@ -256,19 +275,19 @@ static moe_status_t route_impl(const moe_config_t* cfg, const void* x, const voi
   switch (pick_router(*cfg, aligned16(x) && aligned16(Wr))) {
     case Router::kWarp:
       e = launch_route_warp(*cfg, x, Wr, br, lg, topk_ids, topk_w, w.psum_partial, psum, counter,
-                            sel_bias, st);
+                            sel_bias, w.cand, st);
       break;
     case Router::kTc:
       e = launch_route_tc(*cfg, x, Wr, w.route_part, w.status, st);
       if (e == cudaSuccess)
         e = launch_route_select(*cfg, w.route_part, route_tc_nsplit(*cfg), br, lg, topk_ids,
                                 topk_w, w.psum_fixed, psum, counter, psum_fixed_out == nullptr,
-                                sel_bias, st);
+                                sel_bias, w.cand, st);
       if (e == cudaSuccess && psum_fixed_out) *psum_fixed_out = w.psum_fixed;
       break;
     default:
       e = launch_route_simt(*cfg, x, Wr, br, lg, topk_ids, topk_w, w.psum_partial, psum, counter,
-                            sel_bias, st);
+                            sel_bias, w.cand, st);
       break;
   }
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_route");
@@ -351,7 +370,8 @@ static moe_status_t dispatch_impl(const moe_config_t* cfg, const void* x,
   const int64_t C = capacity_of(cfg->T, cfg->k, cfg->E, cfg->capacity_factor);
   cudaError_t e = launch_dispatch(*cfg, C, x, topk_ids, counts, kept, offsets, slot_row,
                                   row_token, xd, w.chunk_counts, w.status, w.dispatch_counter,
-                                  aux, static_cast<cudaStream_t>(stream));
+                                  aux, cfg->reroute ? &w.rr : nullptr,
+                                  static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_dispatch");
 }
 }  // namespace moe

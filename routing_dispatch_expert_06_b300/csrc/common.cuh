@@ -27,6 +27,7 @@ struct WsLayout {
   size_t chunk_counts;  // int32 [n_chunks, E]: histogram, then chunk bases in place
   size_t psum_partial;  // fp32 [n_route_blocks, E]
   size_t route_part;    // fp32 [nsplit, T, E] partial logits (tensor-core router)
+  size_t reroute;       // reroute only: int32 cand, ids1, pos0, pos1 [T, k]; kept0 [E]
   size_t total;
   int64_t n_chunks;
   int64_t n_route_blocks;
@@ -188,6 +189,7 @@ struct AuxArgs {
   float* l_aux;
   unsigned long long* psum_fixed;
   float* health;
+  const int32_t* counts_f;  // counts for f and health when not the launch's own (reroute)
 };
 
 // Per-token row work (scatter, combine) is done by one warp per (token, part

@@ -31,13 +31,16 @@ static_assert(kDispatchThreads == kChunkTokens, "one token per thread in a chunk
 static_assert(kDispatchThreads == kAuxThreads, "the last histogram block runs the statistics");
 
 // Per-expert exclusive scan over the chunk histograms (in place), the total
-// count and kept = min(count, C), by one block.  A group of tpe lanes (a power
+// count and kept = min(count, C), by one block; with cap_base (a second fill
+// round into the room C - cap_base[e] left by the first), kept =
+// cap_base[e] + min(count, C - cap_base[e]).  A group of tpe lanes (a power
 // of two, as many as the block holds for E experts, at most 32) scans one
 // expert; each lane loads 8 consecutive chunk counts at once, so an expert's
 // n_chunks take ceil(n_chunks / (8·tpe)) rounds of overlapping loads.
 __device__ void scan_chunks_by_expert(int64_t n_chunks, int E, int64_t C,
                                       int32_t* __restrict__ chunk_counts,
-                                      int32_t* __restrict__ counts, int32_t* __restrict__ kept) {
+                                      int32_t* __restrict__ counts, int32_t* __restrict__ kept,
+                                      const int32_t* __restrict__ cap_base) {
   constexpr int U = 8;
   int tpe = 32;
   while (tpe > 1 && tpe * E > int(blockDim.x)) tpe >>= 1;
@@ -73,18 +76,21 @@ __device__ void scan_chunks_by_expert(int64_t n_chunks, int E, int64_t C,
     }
     if (sub == 0) {
       counts[e] = carry;
-      kept[e] = int32_t(carry < C ? carry : C);
+      const int32_t base = cap_base ? cap_base[e] : 0;
+      const int64_t room = C - base;
+      kept[e] = base + int32_t(carry < room ? carry : room);
     }
   }
 }
 
 // Histogram of one chunk; with a completion counter, the last block to
-// finish also runs the per-expert scan.
+// finish also runs the per-expert scan.  skip_neg: ids < 0 are not counted
+// (the second round of a reroute); cap_base: see scan_chunks_by_expert.
 __global__ void __launch_bounds__(kDispatchThreads)
     histogram_kernel(int64_t T, int E, int k, const int32_t* __restrict__ ids,
                      int32_t* __restrict__ chunk_counts, int32_t* status, int* counter,
                      int64_t C, int32_t* __restrict__ counts, int32_t* __restrict__ kept,
-                     AuxArgs aux) {
+                     AuxArgs aux, int skip_neg, const int32_t* __restrict__ cap_base) {
   extern __shared__ int32_t hist[];
   __shared__ int s_last;
   __shared__ float s_red[kAuxThreads];
@@ -99,7 +105,7 @@ __global__ void __launch_bounds__(kDispatchThreads)
       const int e = ids[t * k + r];
       if (e >= 0 && e < E)
         atomicAdd(&hist[e], 1);
-      else
+      else if (!(skip_neg && e < 0))
         set_status(status, MOE_ERR_INVALID_ARG);
     }
   }
@@ -107,15 +113,16 @@ __global__ void __launch_bounds__(kDispatchThreads)
   for (int e = threadIdx.x; e < E; e += blockDim.x)
     chunk_counts[int64_t(blockIdx.x) * E + e] = hist[e];
   if (counter && last_block_to_finish(counter, &s_last)) {
-    scan_chunks_by_expert(gridDim.x, E, C, chunk_counts, counts, kept);
+    scan_chunks_by_expert(gridDim.x, E, C, chunk_counts, counts, kept, cap_base);
+    const int32_t* counts_f = aux.counts_f ? aux.counts_f : counts;
     if (aux.f) {
       if (aux.psum_fixed) psum_from_fixed(E, aux.psum_fixed, aux.psum);
       __syncthreads();
-      aux_stats_block(E, T, aux.alpha, counts, aux.psum, aux.f, aux.pbar, aux.l_aux, s_red);
+      aux_stats_block(E, T, aux.alpha, counts_f, aux.psum, aux.f, aux.pbar, aux.l_aux, s_red);
     }
     if (aux.health) {
       __syncthreads();
-      routing_health_block(E, T, k, counts, kept, aux.health, s_red, &s_kept_sum);
+      routing_health_block(E, T, k, counts_f, kept, aux.health, s_red, &s_kept_sum);
     }
   }
 }
@@ -157,11 +164,42 @@ __global__ void __launch_bounds__(256)
 
 // One CTA per chunk of 256 tokens; warp w owns tokens [32w, 32w+32) of it.
 // Dynamic shared memory: off[E+1] | wbase[8][E] | the chunk's ids [256·k].
+// off[e] = Σ_{e' < e} v[e'] for e <= E (off[E] = total), by one block of
+// kDispatchThreads threads: thread i sums a run of consecutive entries, then a
+// block scan (warp shuffles, then the 8 warp totals) gives each run's start.
+// Ends with the block synchronised.
+__device__ __forceinline__ void block_exclusive_scan(int E, const int32_t* __restrict__ v,
+                                                     int32_t* off, int32_t* part) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int per = (E + kDispatchThreads - 1) / kDispatchThreads;
+  const int lo = tid * per, hi = min(E, lo + per);
+  int32_t run = 0;
+  for (int e = lo; e < hi; ++e) run += v[e];
+  int32_t incl = run;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t u = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += u;
+  }
+  if (lane == 31) part[warp] = incl;
+  __syncthreads();
+  int32_t before = 0;
+  for (int w = 0; w < warp; ++w) before += part[w];
+  if (tid == kDispatchThreads - 1) off[E] = before + incl;
+  int32_t acc = before + incl - run;
+  for (int e = lo; e < hi; ++e) {
+    off[e] = acc;
+    acc += v[e];
+  }
+  __syncthreads();
+}
+
 __global__ void __launch_bounds__(kDispatchThreads)
     assign_kernel(int64_t T, int E, int k, int64_t C, const int32_t* __restrict__ ids,
                   const int32_t* __restrict__ chunk_base, const int32_t* __restrict__ kept,
                   int32_t* __restrict__ offsets, int32_t* __restrict__ slot_row,
-                  int32_t* __restrict__ row_token) {
+                  int32_t* __restrict__ row_token, int positions_only,
+                  const int32_t* __restrict__ cap_base) {
   extern __shared__ int32_t sm[];
   int32_t* off = sm;                       // [E+1]
   int32_t* wbase = sm + E + 1;             // [8][E]
@@ -178,34 +216,16 @@ __global__ void __launch_bounds__(kDispatchThreads)
     for (int i = tid; i < n_ids; i += kDispatchThreads) s_ids[i] = src[i];
   }
 
-  // Expert offsets: exclusive scan of kept[0..E).  Thread i sums a run of
-  // consecutive experts; a block scan (warp shuffles, then the 8 warp
-  // totals) gives each run's start.
-  const int per = (E + kDispatchThreads - 1) / kDispatchThreads;
-  const int lo = tid * per, hi = min(E, lo + per);
-  int32_t run = 0;
-  for (int e = lo; e < hi; ++e) run += kept[e];
-  int32_t incl = run;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int32_t u = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += u;
-  }
-  if (lane == 31) part[warp] = incl;
-  __syncthreads();
-  int32_t before = 0;
-  for (int w = 0; w < warp; ++w) before += part[w];
-  if (tid == kDispatchThreads - 1) off[E] = before + incl;
-  {
-    int32_t acc = before + incl - run;
-    for (int e = lo; e < hi; ++e) {
-      off[e] = acc;
-      acc += kept[e];
-    }
+  // Expert offsets: exclusive scan of kept[0..E) (positions_only: the
+  // per-expert capacity instead, C or C - cap_base[e]).
+  if (positions_only) {
+    for (int e = tid; e < E; e += kDispatchThreads) off[e] = int32_t(C - (cap_base ? cap_base[e] : 0));
+  } else {
+    block_exclusive_scan(E, kept, off, part);
   }
   for (int i = tid; i < 8 * E; i += kDispatchThreads) wbase[i] = 0;
   __syncthreads();
-  if (blockIdx.x == 0)
+  if (blockIdx.x == 0 && !positions_only)
     for (int e = tid; e <= E; e += kDispatchThreads) offsets[e] = off[e];
 
   // Per-warp histograms of this chunk.
@@ -236,7 +256,9 @@ __global__ void __launch_bounds__(kDispatchThreads)
       int32_t row = -1;
       if (e >= 0 && e < E) {
         const int32_t pos = my[e]++;
-        if (pos < C) {
+        if (positions_only) {
+          row = pos < off[e] ? pos : -1;  // off[e] holds the capacity here
+        } else if (pos < C) {
           row = off[e] + pos;
           row_token[row] = int32_t(t);
         }
@@ -244,6 +266,61 @@ __global__ void __launch_bounds__(kDispatchThreads)
       slot_row[t * k + lane] = row;
     }
     __syncwarp();
+  }
+}
+
+// Overflow reroute, step 2: the m-th slot of token t that the first fill
+// dropped (pos0 < 0), in rank order, is offered to cand[t*k + m]; other slots
+// offer nothing (-1).  One thread per token.
+__global__ void __launch_bounds__(256)
+    reroute_offer_kernel(int64_t T, int k, const int32_t* __restrict__ pos0,
+                         const int32_t* __restrict__ cand, int32_t* __restrict__ ids1) {
+  pdl_wait();
+  pdl_trigger();
+  for (int64_t t = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; t < T;
+       t += int64_t(gridDim.x) * blockDim.x) {
+    int m = 0;
+    for (int r = 0; r < k; ++r) {
+      int32_t e = -1;
+      if (pos0[t * k + r] < 0) {
+        e = cand[t * k + m];
+        ++m;
+      }
+      ids1[t * k + r] = e;
+    }
+  }
+}
+
+// Overflow reroute, last step: offsets = exclusive scan of the final kept;
+// a slot kept by the first fill sits at offsets[e] + pos0, a served offer at
+// offsets[e'] + kept0[e'] + pos1 (after the expert's own rows); row_token for
+// every kept row.  Every block forms the offsets in shared memory; block 0
+// writes them.
+__global__ void __launch_bounds__(kDispatchThreads)
+    reroute_finalize_kernel(int64_t T, int E, int k, const int32_t* __restrict__ ids,
+                            const int32_t* __restrict__ ids1, const int32_t* __restrict__ pos0,
+                            const int32_t* __restrict__ pos1, const int32_t* __restrict__ kept0,
+                            const int32_t* __restrict__ kept, int32_t* __restrict__ offsets,
+                            int32_t* __restrict__ slot_row, int32_t* __restrict__ row_token) {
+  extern __shared__ int32_t off[];  // [E+1]
+  __shared__ int32_t part[kDispatchThreads / 32];
+  pdl_wait();
+  pdl_trigger();
+  block_exclusive_scan(E, kept, off, part);
+  if (blockIdx.x == 0)
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) offsets[e] = off[e];
+  const int64_t n = T * k;
+  for (int64_t s = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; s < n;
+       s += int64_t(gridDim.x) * blockDim.x) {
+    int32_t row = -1;
+    if (pos0[s] >= 0) {
+      row = off[ids[s]] + pos0[s];
+    } else if (pos1[s] >= 0) {
+      const int32_t e = ids1[s];
+      row = off[e] + kept0[e] + pos1[s];
+    }
+    slot_row[s] = row;
+    if (row >= 0) row_token[row] = int32_t(s / k);
   }
 }
 
@@ -293,31 +370,69 @@ cudaError_t launch_dispatch(const moe_config_t& c, int64_t C, const void* x,
                             const int32_t* ids, int32_t* counts, int32_t* kept,
                             int32_t* offsets, int32_t* slot_row, int32_t* row_token, void* xd,
                             int32_t* chunk_counts, int32_t* status, int* counter,
-                            const AuxArgs* aux, cudaStream_t st) {
+                            const AuxArgs* aux, const RerouteBufs* rr, cudaStream_t st) {
+  if (rr && !counter) return cudaErrorInvalidValue;
   const int64_t n_chunks = (c.T + kChunkTokens - 1) / kChunkTokens;
-  const AuxArgs aux_v =
-      (aux && counter) ? *aux
-                       : AuxArgs{0.f, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
-  cudaError_t err;
-  err = launch_pdl(histogram_kernel, dim3(unsigned(n_chunks)), dim3(kDispatchThreads),
-                   size_t(c.E) * 4, st, c.T, c.E, c.k, ids, chunk_counts, status, counter, C,
-                   counts, kept, aux_v);
-  count_launch();
-  if (err != cudaSuccess || (err = cudaGetLastError()) != cudaSuccess) return err;
-  if (!counter) {
-    expert_scan_kernel<<<unsigned(c.E), 256, 0, st>>>(n_chunks, c.E, C, chunk_counts, counts,
-                                                       kept);
-    count_launch();
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  }
-  const size_t smem = size_t(c.E + 1 + 8 * c.E + kChunkTokens * c.k) * 4;
-  err = ensure_dynamic_smem(reinterpret_cast<const void*>(assign_kernel), smem);
+  const AuxArgs no_aux{0.f, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
+  const AuxArgs aux_v = (aux && counter) ? *aux : no_aux;
+  const size_t hist_smem = size_t(c.E) * 4;
+  const size_t assign_smem = size_t(c.E + 1 + 8 * c.E + kChunkTokens * c.k) * 4;
+  cudaError_t err = ensure_dynamic_smem(reinterpret_cast<const void*>(assign_kernel), assign_smem);
   if (err != cudaSuccess) return err;
-  err = launch_pdl(assign_kernel, dim3(unsigned(n_chunks)), dim3(kDispatchThreads), smem, st,
-                   c.T, c.E, c.k, C, ids, static_cast<const int32_t*>(chunk_counts),
-                   static_cast<const int32_t*>(kept), offsets, slot_row, row_token);
-  count_launch();
-  if (err != cudaSuccess || (err = cudaGetLastError()) != cudaSuccess) return err;
+  auto histogram = [&](const int32_t* ids_, int32_t* counts_, int32_t* kept_, const AuxArgs& a,
+                       int skip_neg, const int32_t* cap_base) {
+    cudaError_t e = launch_pdl(histogram_kernel, dim3(unsigned(n_chunks)), dim3(kDispatchThreads),
+                               hist_smem, st, c.T, c.E, c.k, ids_, chunk_counts, status, counter,
+                               C, counts_, kept_, a, skip_neg, cap_base);
+    count_launch();
+    return e != cudaSuccess ? e : cudaGetLastError();
+  };
+  auto assign = [&](const int32_t* ids_, const int32_t* kept_, int32_t* slot_row_,
+                    int positions_only, const int32_t* cap_base) {
+    cudaError_t e = launch_pdl(assign_kernel, dim3(unsigned(n_chunks)), dim3(kDispatchThreads),
+                               assign_smem, st, c.T, c.E, c.k, C, ids_,
+                               static_cast<const int32_t*>(chunk_counts), kept_, offsets,
+                               slot_row_, row_token, positions_only, cap_base);
+    count_launch();
+    return e != cudaSuccess ? e : cudaGetLastError();
+  };
+  if (!rr) {
+    if ((err = histogram(ids, counts, kept, aux_v, 0, nullptr)) != cudaSuccess) return err;
+    if (!counter) {
+      expert_scan_kernel<<<unsigned(c.E), 256, 0, st>>>(n_chunks, c.E, C, chunk_counts, counts,
+                                                         kept);
+      count_launch();
+      if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    }
+    if ((err = assign(ids, kept, slot_row, 0, nullptr)) != cudaSuccess) return err;
+  } else {
+    // [MoE 模型原理 §4.3] reroute: first fill (positions only), offers to the
+    // next candidates, second fill into the room left, final rows.
+    if ((err = histogram(ids, counts, rr->kept0, no_aux, 0, nullptr)) != cudaSuccess) return err;
+    if ((err = assign(ids, nullptr, rr->pos0, 1, nullptr)) != cudaSuccess) return err;
+    const int64_t tb = (c.T + 255) / 256;
+    err = launch_pdl(reroute_offer_kernel, dim3(unsigned(tb < 4096 ? tb : 4096)), dim3(256), 0,
+                     st, c.T, c.k, static_cast<const int32_t*>(rr->pos0), rr->cand, rr->ids1);
+    count_launch();
+    if (err != cudaSuccess || (err = cudaGetLastError()) != cudaSuccess) return err;
+    AuxArgs a1 = aux_v;
+    a1.counts_f = counts;  // f and health use the first choices' counts
+    err = histogram(rr->ids1, rr->counts1, kept, a1, 1, rr->kept0);
+    if (err != cudaSuccess) return err;
+    if ((err = assign(rr->ids1, nullptr, rr->pos1, 1, rr->kept0)) != cudaSuccess) return err;
+    const int64_t sb = (c.T * c.k + kDispatchThreads - 1) / kDispatchThreads;
+    const size_t fsmem = size_t(c.E + 1) * 4;
+    err = ensure_dynamic_smem(reinterpret_cast<const void*>(reroute_finalize_kernel), fsmem);
+    if (err != cudaSuccess) return err;
+    err = launch_pdl(reroute_finalize_kernel, dim3(unsigned(sb < 2048 ? sb : 2048)),
+                     dim3(kDispatchThreads), fsmem, st, c.T, c.E, c.k, ids,
+                     static_cast<const int32_t*>(rr->ids1), static_cast<const int32_t*>(rr->pos0),
+                     static_cast<const int32_t*>(rr->pos1),
+                     static_cast<const int32_t*>(rr->kept0), static_cast<const int32_t*>(kept),
+                     offsets, slot_row, row_token);
+    count_launch();
+    if (err != cudaSuccess || (err = cudaGetLastError()) != cudaSuccess) return err;
+  }
   const int elem = c.dtype == MOE_DT_BF16 ? 2 : 4;
   const int64_t row_vecs = int64_t(c.d) * elem / 16;
   const RowSplit rs = row_split(c.T, row_vecs, 128);

@@ -74,6 +74,9 @@ extern "C" moe_status_t moe_dispatch_noalloc(const moe_config_t* cfg, const void
   if (s != MOE_OK) return s;
   if (!x || !topk_ids || !counts || !kept || !offsets || !slot_row || !row_token || !xd)
     return report_error(MOE_ERR_INVALID_ARG, "moe_dispatch_noalloc: NULL tensor");
+  if (cfg->reroute)
+    return report_error(MOE_ERR_UNSUPPORTED,
+                        "moe_dispatch_noalloc: reroute needs the workspace of moe_dispatch");
   if ((reinterpret_cast<uintptr_t>(x) & 15) || (reinterpret_cast<uintptr_t>(xd) & 15))
     return report_error(MOE_ERR_INVALID_ARG,
                         "moe_dispatch_noalloc: x and xd must be 16-byte aligned");
@@ -88,7 +91,7 @@ extern "C" moe_status_t moe_dispatch_noalloc(const moe_config_t* cfg, const void
     return report_error(MOE_ERR_CUDA, "moe_dispatch_noalloc: cudaGetSymbolAddress failed");
   const int64_t C = moe_capacity(cfg);
   e = launch_dispatch(*cfg, C, x, topk_ids, counts, kept, offsets, slot_row, row_token, xd,
-                      scratch, status, nullptr, nullptr, static_cast<cudaStream_t>(stream));
+                      scratch, status, nullptr, nullptr, nullptr, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MOE_OK
                           : report_error(MOE_ERR_CUDA, "moe_dispatch_noalloc: launch failed");
 }

@@ -32,10 +32,12 @@ cudaError_t max_active_clusters(const void* kernel, const cudaLaunchConfig_t& cf
 // last block to finish (counter: a zeroed int in the workspace).
 // sel_bias (every router, nullable): rank experts by the fp32 sum
 // logit + sel_bias; weights, Σp and logits stay those of the logits.
+// cand (every router, nullable, [T,k]): the experts ranked k .. 2k-1 by the
+// same keys (-1 past E), the next candidates of an overflow reroute.
 cudaError_t launch_route_simt(const moe_config_t& c, const void* x, const void* Wr,
                               const float* br, float* logits, int32_t* ids, float* w,
                               float* psum_partial, float* psum, int* counter,
-                              const float* sel_bias, cudaStream_t st);
+                              const float* sel_bias, int32_t* cand, cudaStream_t st);
 
 // Router on CUDA cores for bf16 layers with E <= 32 and W_r small enough for
 // shared memory: one warp per token, 16-byte loads, same outputs.
@@ -43,7 +45,7 @@ bool route_warp_supported(const moe_config_t& c);
 cudaError_t launch_route_warp(const moe_config_t& c, const void* x, const void* Wr,
                               const float* br, float* logits, int32_t* ids, float* w,
                               float* psum_partial, float* psum, int* counter,
-                              const float* sel_bias, cudaStream_t st);
+                              const float* sel_bias, int32_t* cand, cudaStream_t st);
 
 // Router on the tcgen05 tensor cores (bf16, E <= 256): same outputs;
 // psum_partial holds one row per 128-token tile.
@@ -64,20 +66,34 @@ cudaError_t launch_route_tc(const moe_config_t& c, const void* x, const void* Wr
 cudaError_t launch_route_select(const moe_config_t& c, const float* part, int nsplit,
                                 const float* br, float* logits, int32_t* ids, float* w,
                                 unsigned long long* psum_fixed, float* psum, int* counter,
-                                bool finish, const float* sel_bias, cudaStream_t st);
+                                bool finish, const float* sel_bias, int32_t* cand,
+                                cudaStream_t st);
 // One block: the routing-health indicators from counts and kept.
 cudaError_t launch_health(const moe_config_t& c, const int32_t* counts, const int32_t* kept,
                           float* health, cudaStream_t st);
 
+// Workspace buffers of an overflow reroute: cand [T,k] (the router's next
+// candidates), ids1, pos0, pos1 [T,k]; kept0, counts1 [E].
+struct RerouteBufs {
+  const int32_t* cand;
+  int32_t* ids1;
+  int32_t* pos0;
+  int32_t* pos1;
+  int32_t* kept0;
+  int32_t* counts1;
+};
+
 // Dispatch: histogram per chunk, per-expert scan + capacity, positions, row
 // copy.  counter: a zeroed int for the histogram's grid-completion count (the
 // last histogram block then runs the scan, and with aux != NULL also the
-// f / p̄ / L_aux statistics), or NULL for a separate scan kernel.
+// f / p̄ / L_aux statistics), or NULL for a separate scan kernel.  rr (needs
+// counter): the reroute variant (first fill as positions, offers, second
+// fill into the room left, final rows).
 cudaError_t launch_dispatch(const moe_config_t& c, int64_t C, const void* x,
                             const int32_t* ids, int32_t* counts, int32_t* kept,
                             int32_t* offsets, int32_t* slot_row, int32_t* row_token, void* xd,
                             int32_t* chunk_counts, int32_t* status, int* counter,
-                            const AuxArgs* aux, cudaStream_t st);
+                            const AuxArgs* aux, const RerouteBufs* rr, cudaStream_t st);
 
 // Grouped GEMM on CUDA cores over ragged expert row ranges (fp32 or bf16):
 //   out[rows of e] = epi(A[rows of e] · B[e]ᵀ + bias[e]),  A [R,K], B [E,N,K].

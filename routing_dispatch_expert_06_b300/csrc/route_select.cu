@@ -47,6 +47,7 @@ struct SelectArgs {
   const float* sel_bias;           // [E] ranking-only bias, or NULL
   float* logits;                   // [T][E] or NULL
   int32_t* ids;                    // [T][k]
+  int32_t* cand;                   // [T][k] experts ranked k .. 2k-1 (-1 past E), or NULL
   float* w;                        // [T][k]
   unsigned long long* psum_fixed;  // [kPsumReplicas][kPsumFixedMaxE], zero on entry and exit
   float* psum;                     // [E]
@@ -225,7 +226,9 @@ __global__ void __launch_bounds__(kSelWarps * 32)
     }
     float my_v = -INFINITY;
     int my_i = 0;
-    for (int r = 0; r < k; ++r) {
+    // With candidates the rounds continue to rank 2k - 1 (at most E).
+    const int rounds = a.cand ? min(2 * k, E) : k;
+    for (int r = 0; r < rounds; ++r) {
       float lm = key[0];
 #pragma unroll
       for (int j = 1; j < EPL; ++j) lm = fmaxf(lm, key[j]);
@@ -264,6 +267,8 @@ __global__ void __launch_bounds__(kSelWarps * 32)
       a.ids[t * k + sub] = my_i;
       a.w[t * k + sub] = ev * inv;
     }
+    if (a.cand && has_row && sub >= k && sub < 2 * k)
+      a.cand[t * k + sub - k] = sub < rounds ? my_i : -1;
     if (has_row) {
 #pragma unroll
       for (int j = 0; j < EPL; ++j) acc[j] += __float2uint_rn(pr[j] * inv_z * kPsumFixScale);
@@ -322,7 +327,8 @@ cudaError_t launch_epl(const SelectArgs& a, cudaStream_t st) {
 cudaError_t launch_route_select(const moe_config_t& c, const float* part, int nsplit,
                                 const float* br, float* logits, int32_t* ids, float* w,
                                 unsigned long long* psum_fixed, float* psum, int* counter,
-                                bool finish, const float* sel_bias, cudaStream_t st) {
+                                bool finish, const float* sel_bias, int32_t* cand,
+                                cudaStream_t st) {
   if (c.E > kPsumFixedMaxE) return cudaErrorInvalidValue;
   SelectArgs a{};
   a.T = c.T;
@@ -337,6 +343,7 @@ cudaError_t launch_route_select(const moe_config_t& c, const float* part, int ns
   a.sel_bias = sel_bias;
   a.logits = logits;
   a.ids = ids;
+  a.cand = cand;
   a.w = w;
   a.psum_fixed = psum_fixed;
   a.psum = psum;

@@ -46,7 +46,8 @@ __device__ __forceinline__ float warp_sum(float v) {
 // never wins again).
 __device__ __forceinline__ void softmax_topk_warp(float* s_log, float* s_ps, int E, int k,
                                                   int renorm, int64_t t, int32_t* topk_ids,
-                                                  float* topk_w, const float* sel_bias) {
+                                                  float* topk_w, const float* sel_bias,
+                                                  int32_t* cand) {
   const int lane = lane_id();
   float mx = -INFINITY;
   for (int e = lane; e < E; e += 32) mx = fmaxf(mx, s_log[e]);
@@ -59,7 +60,10 @@ __device__ __forceinline__ void softmax_topk_warp(float* s_log, float* s_ps, int
 
   int my_id = -1;
   float my_p = 0.f;
-  for (int r = 0; r < k; ++r) {
+  // With cand (nullable, [T,k]) the rounds continue to rank 2k - 1 (at most
+  // E): the token's next candidates for an overflow reroute.
+  const int rounds = cand ? min(2 * k, E) : k;
+  for (int r = 0; r < rounds; ++r) {
     float bv = -INFINITY;
     int bi = 0x7fffffff;
     for (int e = lane; e < E; e += 32) {
@@ -92,6 +96,7 @@ __device__ __forceinline__ void softmax_topk_warp(float* s_log, float* s_ps, int
     topk_ids[t * k + lane] = my_id;
     topk_w[t * k + lane] = renorm ? my_p / sel : my_p;
   }
+  if (cand && lane >= k && lane < 2 * k) cand[t * k + lane - k] = lane < rounds ? my_id : -1;
 }
 
 template <typename TIn>
@@ -99,7 +104,7 @@ __global__ void __launch_bounds__(256)
     route_simt_kernel(int64_t T, int d, int E, int k, int renorm, const TIn* __restrict__ x,
                       const TIn* __restrict__ Wr, const float* __restrict__ br, float* logits,
                       int32_t* topk_ids, float* topk_w, float* psum_partial, float* psum,
-                      int* counter, const float* __restrict__ sel_bias) {
+                      int* counter, const float* __restrict__ sel_bias, int32_t* cand) {
   __shared__ int s_flag;
   extern __shared__ float smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -132,7 +137,7 @@ __global__ void __launch_bounds__(256)
     if (logits)
       for (int e = lane; e < E; e += 32) logits[t * E + e] = s_log[e];
     __syncwarp();
-    softmax_topk_warp(s_log, s_ps, E, k, renorm, t, topk_ids, topk_w, sel_bias);
+    softmax_topk_warp(s_log, s_ps, E, k, renorm, t, topk_ids, topk_w, sel_bias, cand);
     __syncwarp();
   }
   __syncthreads();
@@ -159,7 +164,7 @@ __global__ void __launch_bounds__(256)
                       const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ Wr,
                       const float* __restrict__ br, float* logits, int32_t* topk_ids,
                       float* topk_w, float* psum_partial, float* psum, int* counter,
-                      const float* __restrict__ sel_bias) {
+                      const float* __restrict__ sel_bias, int32_t* cand) {
   extern __shared__ uint4 s_w[];  // [E][d/8] 16-byte chunks of W_r
   __shared__ float s_log[8][32];
   __shared__ float s_ps[8][32];
@@ -215,7 +220,8 @@ __global__ void __launch_bounds__(256)
     __syncwarp();
     if (logits && lane < E) logits[t * E + lane] = s_log[warp][lane];
     __syncwarp();
-    softmax_topk_warp(s_log[warp], s_ps[warp], E, k, renorm, t, topk_ids, topk_w, sel_bias);
+    softmax_topk_warp(s_log[warp], s_ps[warp], E, k, renorm, t, topk_ids, topk_w, sel_bias,
+                      cand);
     __syncwarp();
   }
   __syncthreads();
@@ -230,7 +236,7 @@ __global__ void __launch_bounds__(256)
 cudaError_t launch_route_simt(const moe_config_t& c, const void* x, const void* Wr,
                               const float* br, float* logits, int32_t* ids, float* w,
                               float* psum_partial, float* psum, int* counter,
-                              const float* sel_bias, cudaStream_t st) {
+                              const float* sel_bias, int32_t* cand, cudaStream_t st) {
   const int64_t nblk = (c.T + kRouteTokensSimt - 1) / kRouteTokensSimt;
   const size_t smem = size_t(16) * c.E * sizeof(float);
   cudaError_t err;
@@ -239,7 +245,8 @@ cudaError_t launch_route_simt(const moe_config_t& c, const void* x, const void* 
     if (err != cudaSuccess) return err;
     route_simt_kernel<float><<<unsigned(nblk), 256, smem, st>>>(
         c.T, c.d, c.E, c.k, c.renormalize, static_cast<const float*>(x),
-        static_cast<const float*>(Wr), br, logits, ids, w, psum_partial, psum, counter, sel_bias);
+        static_cast<const float*>(Wr), br, logits, ids, w, psum_partial, psum, counter, sel_bias,
+        cand);
   } else {
     err = ensure_dynamic_smem(reinterpret_cast<const void*>(route_simt_kernel<__nv_bfloat16>),
                               smem);
@@ -247,7 +254,7 @@ cudaError_t launch_route_simt(const moe_config_t& c, const void* x, const void* 
     route_simt_kernel<__nv_bfloat16><<<unsigned(nblk), 256, smem, st>>>(
         c.T, c.d, c.E, c.k, c.renormalize, static_cast<const __nv_bfloat16*>(x),
         static_cast<const __nv_bfloat16*>(Wr), br, logits, ids, w, psum_partial, psum, counter,
-        sel_bias);
+        sel_bias, cand);
   }
   count_launch();
   return cudaGetLastError();
@@ -260,7 +267,7 @@ bool route_warp_supported(const moe_config_t& c) {
 cudaError_t launch_route_warp(const moe_config_t& c, const void* x, const void* Wr,
                               const float* br, float* logits, int32_t* ids, float* w,
                               float* psum_partial, float* psum, int* counter,
-                              const float* sel_bias, cudaStream_t st) {
+                              const float* sel_bias, int32_t* cand, cudaStream_t st) {
   if (!route_warp_supported(c)) return cudaErrorInvalidValue;
   const int sms = device_sms();
   // Blocks of 8 warps, about 8 tokens per warp, at most 4 blocks per SM; one
@@ -274,7 +281,7 @@ cudaError_t launch_route_warp(const moe_config_t& c, const void* x, const void* 
     kernel<<<grid, 256, smem, st>>>(c.T, c.d, c.E, c.k, c.renormalize,
                                     static_cast<const __nv_bfloat16*>(x),
                                     static_cast<const __nv_bfloat16*>(Wr), br, logits, ids, w,
-                                    psum_partial, psum, counter, sel_bias);
+                                    psum_partial, psum, counter, sel_bias, cand);
     return cudaGetLastError();
   };
   cudaError_t err = c.E <= 8 ? run(route_warp_kernel<8>)

@@ -37,7 +37,7 @@ class Config(ctypes.Structure):
                 ("E", ctypes.c_int32), ("k", ctypes.c_int32),
                 ("capacity_factor", ctypes.c_double), ("renormalize", ctypes.c_int32),
                 ("act", ctypes.c_int32), ("dtype", ctypes.c_int32),
-                ("write_logits", ctypes.c_int32)]
+                ("write_logits", ctypes.c_int32), ("reroute", ctypes.c_int32)]
 
 
 _TENSOR_FIELDS = ["x", "Wr", "br", "W1", "b1", "W2", "b2", "logits", "topk_ids", "topk_w",
@@ -121,17 +121,17 @@ def _stream(stream=None):
 
 
 def config(T, d, d_ff, E, k, capacity_factor, renormalize=True, act="gelu_tanh", dtype="bf16",
-           write_logits=False) -> Config:
+           write_logits=False, reroute=False) -> Config:
     return Config(T=T, d=d, d_ff=d_ff, E=E, k=k, capacity_factor=float(capacity_factor),
                   renormalize=int(bool(renormalize)),
                   act=MOE_ACT_RELU if act == "relu" else MOE_ACT_GELU_TANH,
                   dtype=MOE_DT_BF16 if dtype == "bf16" else MOE_DT_F32,
-                  write_logits=int(bool(write_logits)))
+                  write_logits=int(bool(write_logits)), reroute=int(bool(reroute)))
 
 
-def config_from_workload(wl, write_logits=False) -> Config:
+def config_from_workload(wl, write_logits=False, reroute=False) -> Config:
     return config(wl.T, wl.d, wl.d_ff, wl.E, wl.k, wl.capacity_factor, wl.renormalize, wl.act,
-                  wl.dtype, write_logits)
+                  wl.dtype, write_logits, reroute)
 
 
 def capacity(cfg: Config) -> int:

@@ -66,13 +66,14 @@ def assert_float(got, ref, dtype, what=""):
         assert_rel_rms(got, ref, 1e-4, what)
 
 
-def run_gpu(wl, inp=None, expert_bias=False, alpha=1.0, stages=False, health=False):
+def run_gpu(wl, inp=None, expert_bias=False, alpha=1.0, stages=False, health=False,
+            reroute=False):
     """Run the layer through the C ABI; return (cfg, inputs, outputs, ws).
     An ``inp["sel_bias"]`` routes with the selection-only bias; ``health``
     also asks for the routing-health indicators."""
     if inp is None:
         inp = inputs.make_inputs(wl, "cuda", expert_bias=expert_bias)
-    cfg = moe.config_from_workload(wl, write_logits=True)
+    cfg = moe.config_from_workload(wl, write_logits=True, reroute=reroute)
     ws = moe.workspace(cfg)
     out = moe.allocate(cfg, health=health)
     if stages:
@@ -122,7 +123,7 @@ def oracle_yd(wl, inp, xd_rows, rows, offsets):
 
 
 def check_forward(wl, inp, out, alpha=1.0, full=False, max_rows_check=None, n_tokens=None,
-                  max_experts=None, e2e_tokens=64, seed=0):
+                  max_experts=None, e2e_tokens=64, seed=0, reroute=False):
     """Compare every output of one forward pass with the oracle (routing with
     inp["sel_bias"] when present; out["health"] when present)."""
     sel_bias = h(inp["sel_bias"]) if inp.get("sel_bias") is not None else None
@@ -141,14 +142,15 @@ def check_forward(wl, inp, out, alpha=1.0, full=False, max_rows_check=None, n_to
     assert_rel_rms(logits[tok_l], ref_logits, 1e-5, "logits")
 
     # 2. selection on the device's own logits: ids bit-exact, weights, psum
-    ids_ref, w_ref, psum_ref, _ = oracle.select(logits, k, wl.renormalize, sel_bias=sel_bias)
+    ids_ref, w_ref, psum_ref, _, cand_ref = oracle.select(logits, k, wl.renormalize,
+                                                          sel_bias=sel_bias, want_cand=True)
     np.testing.assert_array_equal(h(out["topk_ids"]), ids_ref, "topk_ids")
     assert_rel_rms(h(out["topk_w"]), w_ref, 1e-4, "topk_w")
     assert_rel_rms(h(out["psum"]), psum_ref, 1e-4, "psum")
 
     # 3. capacity fill: every index bit-exact
     C = oracle.capacity(T, k, E, wl.capacity_factor)
-    fl = oracle.fill(ids_ref, E, C)
+    fl = oracle.fill_reroute(ids_ref, cand_ref, E, C) if reroute else oracle.fill(ids_ref, E, C)
     for name in ["counts", "kept", "offsets", "slot_row"]:
         np.testing.assert_array_equal(h(out[name]), fl[name], name)
     n = int(fl["offsets"][E])

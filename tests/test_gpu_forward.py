@@ -65,15 +65,16 @@ def test_expert_bias_path():
     check_forward(wl, inp, out, full=True)
 
 
-@pytest.mark.parametrize("extras", [False, True], ids=["plain", "sel_bias_health"])
+@pytest.mark.parametrize("extras", [False, True], ids=["plain", "sel_bias_health_reroute"])
 def test_stage_calls_equal_forward_and_are_deterministic(extras):
     wl = W["bf16_t8192_d2048_e64_top6"].replace(T=3000)
     inp = inputs.make_inputs(wl, "cuda")
     if extras:
         inp["sel_bias"] = inputs.selection_bias(wl, "cuda")
-    _, inp, out1, _ = run_gpu(wl, inp=inp, health=extras)
-    _, _, out2, _ = run_gpu(wl, inp=inp, stages=True, health=extras)
-    _, _, out3, _ = run_gpu(wl, inp=inp, health=extras)
+    kw = dict(health=extras, reroute=extras)
+    _, inp, out1, _ = run_gpu(wl, inp=inp, **kw)
+    _, _, out2, _ = run_gpu(wl, inp=inp, stages=True, **kw)
+    _, _, out3, _ = run_gpu(wl, inp=inp, **kw)
     n = int(h(out1["offsets"])[-1])
     names = ["logits", "topk_ids", "topk_w", "psum", "counts", "kept", "offsets",
              "slot_row", "f", "pbar", "l_aux", "y"] + (["health"] if extras else [])
@@ -243,3 +244,33 @@ def test_routing_health_call_matches_oracle():
         torch.cuda.synchronize()
         ref = oracle.routing_health(counts, kept, T, k)
         np.testing.assert_allclose(h(hdev), ref, rtol=1e-4, atol=1e-6)
+
+
+REROUTE_CASES = [
+    ("e64_top6", W["bf16_t8192_d2048_e64_top6"].replace(T=3000)),
+    ("fp32_e8_top2", W["fp32_t512_d128_e8_top2"]),
+    ("heavy_drops", inputs.Workload("heavy_drops", 700, 128, 256, 16, 4, 0.3, True, "gelu_tanh",
+                                    "bf16", 21, "zipf:0.8")),
+    ("decode_t64_e256", W["decode_bf16_t64_d7168_e256_top8"]),
+    ("e8_top1_skewed", W["bf16_t16384_d4096_e8_top1"].replace(T=2048)),
+]
+
+
+@pytest.mark.parametrize("name,wl", REROUTE_CASES, ids=[c[0] for c in REROUTE_CASES])
+def test_forward_with_overflow_reroute(name, wl):
+    # Overflowing slots offered once to the token's next candidate, served
+    # first come into the room left: every index and output against the
+    # oracle's reroute fill; fewer slots are dropped than without it.
+    _, inp, out, _ = run_gpu(wl, expert_bias=True, health=True, reroute=True)
+    check_forward(wl, inp, out, full=wl.T <= 3000, reroute=True)
+    _, _, plain, _ = run_gpu(wl, inp=inp)
+    assert int(h(out["offsets"])[-1]) >= int(h(plain["offsets"])[-1])
+    np.testing.assert_array_equal(h(out["counts"]), h(plain["counts"]))
+
+
+def test_reroute_with_selection_bias():
+    wl = W["bf16_t8192_d2048_e64_top6"].replace(T=2000, capacity_factor=0.8)
+    inp = inputs.make_inputs(wl, "cuda")
+    inp["sel_bias"] = inputs.selection_bias(wl, "cuda")
+    _, inp, out, _ = run_gpu(wl, inp=inp, health=True, reroute=True)
+    check_forward(wl, inp, out, full=True, reroute=True)
