@@ -242,6 +242,8 @@ def main():
                     help="route with a seeded selection-only expert bias")
     ap.add_argument("--health", action="store_true",
                     help="also compute the routing-health indicators in the forward pass")
+    ap.add_argument("--reroute", action="store_true",
+                    help="offer overflowing slots to the token's next candidate")
     args = ap.parse_args()
     wl = inputs.WORKLOADS[args.workload]
 
@@ -273,7 +275,7 @@ def main():
     if world > 1:  # each replica routes its own batch
         g = torch.Generator(device=dev).manual_seed(wl.seed * 1000 + rank)
         inp["x"] = torch.randn(inp["x"].shape, generator=g, device=dev).to(inp["x"].dtype)
-    cfg = moe.config_from_workload(wl, write_logits=False)
+    cfg = moe.config_from_workload(wl, write_logits=False, reroute=args.reroute)
     ws = moe.workspace(cfg, dev)
     out = moe.allocate(cfg, dev, health=args.health)
     stream = torch.cuda.current_stream(dev)
@@ -433,6 +435,7 @@ def main():
                     capacity_factor=wl.capacity_factor, renormalize=wl.renormalize,
                     act=wl.act, parallelism=f"replicas{world}" if world > 1 else "single",
                     sel_bias=bool(args.sel_bias), health=bool(args.health),
+                    reroute=bool(args.reroute),
                     l2="flushed between steps (512 MiB write, then 512 MiB read)"),
         roofline=dict(bound="tensor", kernel=f"{dom} (tcgen05 grouped GEMM)",
                       achieved=dom_tflops, peak=peaks["bf16"], unit="TFLOP/s",
