@@ -120,14 +120,14 @@ int64_t moe_capacity(const moe_config_t* cfg);
 /* Rows of the dispatch buffer to allocate: min(T·k, E·C).  -1 if invalid. */
 int64_t moe_max_rows(const moe_config_t* cfg);
 
-/* Bytes of scratch workspace the stage calls need (80 KiB header with the
+/* Bytes of scratch workspace the stage calls need (272 KiB header with the
  * status word, completion counters and the router's fixed-point column-sum
  * accumulators; per-chunk histograms; per-block probability partial sums; the
  * tensor-core router's fp32 partial logits, nsplit·T·E floats, nsplit > 1 only
  * for small T).  Host only.  A workspace serves one stream at a time. */
 moe_status_t moe_workspace_size(const moe_config_t* cfg, size_t* bytes);
 
-/* Clear the workspace's 80 KiB header: the device status word, the counters
+/* Clear the workspace's 272 KiB header: the device status word, the counters
  * the kernels use to find the last block of a grid and the column-sum
  * accumulators (enqueued on stream; kernels leave them at zero).  Call once after allocating a
  * workspace, and after reading a nonzero status. */
@@ -136,9 +136,9 @@ moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, void* stream);
 /* [MoE 模型原理 §2.1–§2.2] Router: logits s = x W_rᵀ + b_r (fp32 accumulate),
  * softmax, top-k with ties to the lower expert index, combine weights
  * (renormalised over the selected set iff cfg->renormalize), and the column
- * sums psum[i] = Σ_t p_{t,i}, deterministic: a fixed reduction order, or (the
- * tensor-core router) each p_{t,i} rounded to 31 fraction bits and added
- * exactly as 64-bit integers.  logits may be NULL unless cfg->write_logits.
+ * sums psum[i] = Σ_t p_{t,i}, deterministic: per-block partial sums in a
+ * fixed order (each p_{t,i} rounded to 31 fraction bits first with the
+ * tensor-core router), added exactly as 64-bit fixed-point integers.  logits may be NULL unless cfg->write_logits.
  * With cfg->reroute it also leaves each token's next candidates (the experts
  * ranked k .. 2k-1) in the workspace for moe_dispatch. */
 moe_status_t moe_route(const moe_config_t* cfg, const void* x, const void* Wr, const float* br,

@@ -250,10 +250,10 @@ static Router pick_router(const moe_config_t& c, bool aligned) {
 
 namespace moe {
 // moe_route.  psum_fixed_out == NULL: psum is written before return (every
-// router).  Otherwise the tensor-core router leaves Σ_t p in the workspace's
-// fixed-point accumulators and sets *psum_fixed_out to them, for the
-// dispatch's histogram to convert (psum_from_fixed); the other routers write
-// psum and set it to NULL.
+// router).  Otherwise the tensor-core and CUDA-core routers leave Σ_t p in the
+// workspace's fixed-point accumulators and set *psum_fixed_out to them, for
+// the dispatch's histogram to convert (psum_from_fixed); the warp router
+// writes psum and sets it to NULL.
 static moe_status_t route_impl(const moe_config_t* cfg, const void* x, const void* Wr,
                                const float* br, const float* sel_bias, float* logits,
                                int32_t* topk_ids, float* topk_w, float* psum, void* ws,
@@ -286,8 +286,9 @@ static moe_status_t route_impl(const moe_config_t* cfg, const void* x, const voi
       if (e == cudaSuccess && psum_fixed_out) *psum_fixed_out = w.psum_fixed;
       break;
     default:
-      e = launch_route_simt(*cfg, x, Wr, br, lg, topk_ids, topk_w, w.psum_partial, psum, counter,
-                            sel_bias, w.cand, st);
+      e = launch_route_simt(*cfg, x, Wr, br, lg, topk_ids, topk_w, w.psum_fixed, psum, counter,
+                            psum_fixed_out == nullptr, sel_bias, w.cand, st);
+      if (e == cudaSuccess && psum_fixed_out) *psum_fixed_out = w.psum_fixed;
       break;
   }
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_route");

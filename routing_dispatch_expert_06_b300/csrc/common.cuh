@@ -33,11 +33,11 @@ struct WsLayout {
   int64_t n_route_blocks;
 };
 
-// The workspace starts with an 80 KiB header that moe_workspace_init clears:
+// The workspace starts with a 272 KiB header that moe_workspace_init clears:
 // the status word, grid-completion counters, and the router's fixed-point
 // column-sum accumulators (every kernel leaves them at zero).
 constexpr int kPsumReplicas = 32;       // copies of the accumulator, spread over L2
-constexpr int kPsumFixedMaxE = 256;
+constexpr int kPsumFixedMaxE = 1024;
 constexpr size_t kWsRouteCounter = 64;
 constexpr size_t kWsDispatchCounter = 128;
 constexpr size_t kWsPsumFixed = 16384;  // uint64 [kPsumReplicas][kPsumFixedMaxE]

@@ -34,10 +34,13 @@ cudaError_t max_active_clusters(const void* kernel, const cudaLaunchConfig_t& cf
 // logit + sel_bias; weights, Σp and logits stay those of the logits.
 // cand (every router, nullable, [T,k]): the experts ranked k .. 2k-1 by the
 // same keys (-1 past E), the next candidates of an overflow reroute.
+// Σp through the fixed-point accumulator copies psum_fixed; finish: the last
+// block converts them into psum (else psum_from_fixed must run later).
 cudaError_t launch_route_simt(const moe_config_t& c, const void* x, const void* Wr,
                               const float* br, float* logits, int32_t* ids, float* w,
-                              float* psum_partial, float* psum, int* counter,
-                              const float* sel_bias, int32_t* cand, cudaStream_t st);
+                              unsigned long long* psum_fixed, float* psum, int* counter,
+                              bool finish, const float* sel_bias, int32_t* cand,
+                              cudaStream_t st);
 
 // Router on CUDA cores for bf16 layers with E <= 32 and W_r small enough for
 // shared memory: one warp per token, 16-byte loads, same outputs.

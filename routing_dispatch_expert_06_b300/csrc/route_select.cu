@@ -329,7 +329,7 @@ cudaError_t launch_route_select(const moe_config_t& c, const float* part, int ns
                                 unsigned long long* psum_fixed, float* psum, int* counter,
                                 bool finish, const float* sel_bias, int32_t* cand,
                                 cudaStream_t st) {
-  if (c.E > kPsumFixedMaxE) return cudaErrorInvalidValue;
+  if (c.E > 256) return cudaErrorInvalidValue;
   SelectArgs a{};
   a.T = c.T;
   a.E = c.E;

@@ -4,9 +4,14 @@
 // [MoE 模型原理 §2.1] s_t = W_r x_t + b_r, p_t = softmax(s_t);
 // [MoE 模型原理 §2.2] S_t = TopK(p_t, k), p̃ = p/Σ_{S_t} p or raw p.
 //
-// One warp per token.  Lanes split the model width d; each lane keeps 32
-// running dot products (one per expert of the current 32-expert block) over
-// its slice, then a butterfly sum gives the logits.  This is the fp32 router
+// One warp per token (groups of 8 tokens per block).  Lanes split the model
+// width d; each lane keeps 32 running dot products (one per expert of the
+// current 32-expert block) over its slice, then a transposing butterfly gives
+// lane L the logit of expert L of the block.  Column sums of p: per warp over
+// its tokens, per block over its warps (fp32, fixed order), then added as
+// 64-bit fixed-point integers (exact, order-free) into the workspace's
+// accumulator copies, converted by the last block (or later, by the whole
+// layer's dispatch).  This is the fp32 router
 // (tf32 tensor cores could not meet an fp32 logit tolerance) and it also
 // serves bf16 inputs for any E; the tensor-core router covers bf16 at scale.
 #include "common.cuh"
@@ -103,18 +108,20 @@ template <typename TIn>
 __global__ void __launch_bounds__(256)
     route_simt_kernel(int64_t T, int d, int E, int k, int renorm, const TIn* __restrict__ x,
                       const TIn* __restrict__ Wr, const float* __restrict__ br, float* logits,
-                      int32_t* topk_ids, float* topk_w, float* psum_partial, float* psum,
-                      int* counter, const float* __restrict__ sel_bias, int32_t* cand) {
+                      int32_t* topk_ids, float* topk_w, unsigned long long* psum_fixed,
+                      float* psum, int* counter, int finish, const float* __restrict__ sel_bias,
+                      int32_t* cand) {
   __shared__ int s_flag;
   extern __shared__ float smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float* s_log = smem + warp * E;
   float* s_ps = smem + 8 * E + warp * E;
   for (int e = lane; e < E; e += 32) s_ps[e] = 0.f;
-  const int64_t t0 = int64_t(blockIdx.x) * kRouteTokensSimt;
-  for (int j = warp; j < kRouteTokensSimt; j += 8) {
-    const int64_t t = t0 + j;
-    if (t >= T) break;
+  // Groups of 8 tokens, one per warp: group b, b + grid, ...
+  const int64_t n_groups = (T + 7) / 8;
+  for (int64_t grp = blockIdx.x; grp < n_groups; grp += gridDim.x) {
+    const int64_t t = grp * 8 + warp;
+    if (t >= T) continue;  // warp-uniform
     const TIn* xr = x + t * d;
     for (int e0 = 0; e0 < E; e0 += 32) {
       const int ne = min(32, E - e0);
@@ -127,11 +134,20 @@ __global__ void __launch_bounds__(256)
         for (int i = 0; i < 32; ++i)
           if (i < ne) acc[i] = fmaf(xv, to_f32(Wr[int64_t(e0 + i) * d + c]), acc[i]);
       }
+      // Transposing butterfly: at offset o the lanes with bit o set keep the
+      // upper half of the values and send the lower half; after the five
+      // steps lane L holds the full sum of value L (fixed order).
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        float v = warp_sum(acc[i]);
-        if (lane == i && i < ne) s_log[e0 + i] = v + br[e0 + i];
+      for (int half = 16; half >= 1; half >>= 1) {
+        const bool upper = (lane & half) != 0;
+#pragma unroll
+        for (int j = 0; j < half; ++j) {
+          const float send = upper ? acc[j] : acc[j + half];
+          const float keep = upper ? acc[j + half] : acc[j];
+          acc[j] = keep + __shfl_xor_sync(0xffffffffu, send, half);
+        }
       }
+      if (lane < ne) s_log[e0 + lane] = acc[0] + br[e0 + lane];
     }
     __syncwarp();
     if (logits)
@@ -141,12 +157,16 @@ __global__ void __launch_bounds__(256)
     __syncwarp();
   }
   __syncthreads();
+  // Column sums: the block's warps in order (fp32), then one fixed-point
+  // atomic per column into this block's copy of the accumulator.
+  unsigned long long* rep = psum_fixed + (blockIdx.x % kPsumReplicas) * kPsumFixedMaxE;
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     float s = 0.f;
     for (int w = 0; w < 8; ++w) s += smem[8 * E + w * E + e];
-    psum_partial[int64_t(blockIdx.x) * E + e] = s;
+    const unsigned long long fx = __double2ull_rn(double(s) * double(kPsumFixScale));
+    if (fx) atomicAdd(rep + e, fx);
   }
-  if (last_block_to_finish(counter, &s_flag)) sum_partials_rows(gridDim.x, E, psum_partial, psum);
+  if (finish && last_block_to_finish(counter, &s_flag)) psum_from_fixed(E, psum_fixed, psum);
 }
 
 // Router on CUDA cores for small expert counts (bf16, E <= 32, W_r small
@@ -235,9 +255,14 @@ __global__ void __launch_bounds__(256)
 
 cudaError_t launch_route_simt(const moe_config_t& c, const void* x, const void* Wr,
                               const float* br, float* logits, int32_t* ids, float* w,
-                              float* psum_partial, float* psum, int* counter,
-                              const float* sel_bias, int32_t* cand, cudaStream_t st) {
-  const int64_t nblk = (c.T + kRouteTokensSimt - 1) / kRouteTokensSimt;
+                              unsigned long long* psum_fixed, float* psum, int* counter,
+                              bool finish, const float* sel_bias, int32_t* cand,
+                              cudaStream_t st) {
+  // Groups of 8 tokens; at most kSimtMaxBlocks blocks (a constant, so each
+  // block's share of tokens depends on T only).
+  constexpr int64_t kSimtMaxBlocks = 1184;
+  const int64_t groups = (c.T + 7) / 8;
+  const int64_t nblk = groups < kSimtMaxBlocks ? groups : kSimtMaxBlocks;
   const size_t smem = size_t(16) * c.E * sizeof(float);
   cudaError_t err;
   if (c.dtype == MOE_DT_F32) {
@@ -245,16 +270,16 @@ cudaError_t launch_route_simt(const moe_config_t& c, const void* x, const void* 
     if (err != cudaSuccess) return err;
     route_simt_kernel<float><<<unsigned(nblk), 256, smem, st>>>(
         c.T, c.d, c.E, c.k, c.renormalize, static_cast<const float*>(x),
-        static_cast<const float*>(Wr), br, logits, ids, w, psum_partial, psum, counter, sel_bias,
-        cand);
+        static_cast<const float*>(Wr), br, logits, ids, w, psum_fixed, psum, counter,
+        finish ? 1 : 0, sel_bias, cand);
   } else {
     err = ensure_dynamic_smem(reinterpret_cast<const void*>(route_simt_kernel<__nv_bfloat16>),
                               smem);
     if (err != cudaSuccess) return err;
     route_simt_kernel<__nv_bfloat16><<<unsigned(nblk), 256, smem, st>>>(
         c.T, c.d, c.E, c.k, c.renormalize, static_cast<const __nv_bfloat16*>(x),
-        static_cast<const __nv_bfloat16*>(Wr), br, logits, ids, w, psum_partial, psum, counter,
-        sel_bias, cand);
+        static_cast<const __nv_bfloat16*>(Wr), br, logits, ids, w, psum_fixed, psum, counter,
+        finish ? 1 : 0, sel_bias, cand);
   }
   count_launch();
   return cudaGetLastError();
