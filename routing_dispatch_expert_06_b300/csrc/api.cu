@@ -149,9 +149,7 @@ static size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 static WsLayout layout_of(const moe_config_t& c) {
   WsLayout L{};
   L.n_chunks = (c.T + kChunkTokens - 1) / kChunkTokens;
-  const int64_t rb_simt = (c.T + kRouteTokensSimt - 1) / kRouteTokensSimt;
-  const int64_t rb_tc = (c.T + kRouteTileM - 1) / kRouteTileM;
-  L.n_route_blocks = rb_simt > rb_tc ? rb_simt : rb_tc;
+  L.n_route_blocks = (c.T + kRouteTokensSimt - 1) / kRouteTokensSimt;
   size_t off = 0;
   L.status = off;
   off += kWsHeaderBytes;

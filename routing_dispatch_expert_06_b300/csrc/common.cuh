@@ -12,7 +12,7 @@ namespace moe {
 
 // Tokens per dispatch chunk (one CTA of the histogram / assign kernels).
 constexpr int kChunkTokens = 256;
-// Tokens per router CTA in the SIMT router (one psum partial row per CTA).
+// Tokens per CTA of the warp router (one psum partial row per CTA).
 constexpr int kRouteTokensSimt = 64;
 // Rows per router tile in the tensor-core router.
 constexpr int kRouteTileM = 128;
@@ -25,9 +25,9 @@ constexpr size_t kRouteWarpSmemMax = 96 * 1024;
 struct WsLayout {
   size_t status;        // int32 status word
   size_t chunk_counts;  // int32 [n_chunks, E]: histogram, then chunk bases in place
-  size_t psum_partial;  // fp32 [n_route_blocks, E]
+  size_t psum_partial;  // fp32 [n_route_blocks, E] (warp router)
   size_t route_part;    // fp32 [nsplit, T, E] partial logits (tensor-core router)
-  size_t reroute;       // reroute only: int32 cand, ids1, pos0, pos1 [T, k]; kept0 [E]
+  size_t reroute;       // reroute only: int32 cand, ids1, pos0, pos1 [T, k]; kept0, counts1 [E]
   size_t total;
   int64_t n_chunks;
   int64_t n_route_blocks;

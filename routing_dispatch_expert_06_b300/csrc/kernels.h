@@ -50,11 +50,10 @@ cudaError_t launch_route_warp(const moe_config_t& c, const void* x, const void* 
                               float* psum_partial, float* psum, int* counter,
                               const float* sel_bias, int32_t* cand, cudaStream_t st);
 
-// Router on the tcgen05 tensor cores (bf16, E <= 256): same outputs;
-// psum_partial holds one row per 128-token tile.
-// When T is small, nsplit CTAs share a tile's reduction over d through
-// split_part [n_tiles, nsplit, NP, 128] fp32 and split_count [n_tiles] (zeroed
-// ints, left zeroed).
+// Router logits on the tcgen05 tensor cores (bf16, E <= 256), followed by
+// route_select_kernel for softmax, top-k, weights and Σp.  When T is small,
+// nsplit CTAs share a 128-token tile's reduction over d, each writing its own
+// partial logits.
 bool route_tc_supported(const moe_config_t& c);
 int route_tc_nsplit(const moe_config_t& c);
 int route_tc_np(const moe_config_t& c);

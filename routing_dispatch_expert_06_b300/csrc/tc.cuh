@@ -85,26 +85,6 @@ __device__ __forceinline__ void tma_load_3d(const CUtensorMap* m, uint64_t* bar,
       : "memory");
 }
 
-// Bring `bytes` contiguous bytes at a global address into L2 (no completion
-// signal); addr and bytes must be multiples of 16.
-__device__ __forceinline__ void bulk_prefetch_l2(const void* addr, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(addr), "r"(bytes) : "memory");
-}
-
-// Bring a tensor tile into L2 ahead of its load (no shared memory, no
-// completion signal).  A prefetch past the tensor's bounds reads nothing.
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* m, int32_t x, int32_t y) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(m),
-               "r"(x), "r"(y)
-               : "memory");
-}
-__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* m, int32_t x, int32_t y,
-                                                int32_t z) {
-  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(m),
-               "r"(x), "r"(y), "r"(z)
-               : "memory");
-}
-
 // ---- programmatic dependent launch ---------------------------------------------
 // Let the next kernel in the stream (launched with programmatic stream
 // serialisation) start once every CTA of this grid has signalled or exited.
