@@ -117,3 +117,30 @@ def test_small_workspace_rejected(lib):
 def test_status_strings(lib):
     for code, name in [(0, "MOE_OK"), (1, "MOE_ERR_INVALID_ARG"), (5, "MOE_ERR_TIMEOUT")]:
         assert lib.moe_status_string(code).decode() == name
+
+
+def test_reroute_flag_checked_and_sized(lib):
+    # reroute must be 0 or 1; with it the workspace grows by the candidate,
+    # offer and position arrays (4 × T·k int32) and two [E] arrays.
+    base = cfg_for(4096, 1024, 4096, 8, 2, 1.25)
+    rr = cfg_for(4096, 1024, 4096, 8, 2, 1.25, reroute=True)
+    n0, n1 = moe.workspace_size(base), moe.workspace_size(rr)
+    assert n1 - n0 >= 4 * 4096 * 2 * 4 + 2 * 8 * 4
+    bad = cfg_for(64, 64, 64, 8, 2, 1.0)
+    bad.reroute = 2
+    n = ctypes.c_size_t(0)
+    assert lib.moe_workspace_size(ctypes.byref(bad), ctypes.byref(n)) == moe.MOE_ERR_INVALID_ARG
+
+
+def test_workspace_header_holds_the_column_sum_accumulators(lib):
+    # moe_workspace_init clears the header; the smallest valid workspace is at
+    # least that large (status word, counters, 32 × 1024 uint64 accumulators).
+    assert moe.workspace_size(cfg_for(1, 8, 8, 1, 1, 1.0)) >= 16384 + 32 * 1024 * 8
+
+
+def test_new_entry_points_reject_null_arguments(lib):
+    cfg = cfg_for(64, 64, 64, 8, 2, 1.0)
+    assert lib.moe_routing_health(ctypes.byref(cfg), None, None, None, None) == \
+        moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_route_sel(ctypes.byref(cfg), None, None, None, None, None, None, None, None,
+                             None, 0, None) == moe.MOE_ERR_INVALID_ARG
