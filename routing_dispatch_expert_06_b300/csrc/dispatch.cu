@@ -86,18 +86,18 @@ __device__ void scan_chunks_by_expert(int64_t n_chunks, int E, int64_t C,
 // Histogram of one chunk; with a completion counter, the last block to
 // finish also runs the per-expert scan.  skip_neg: ids < 0 are not counted
 // (the second round of a reroute); cap_base: see scan_chunks_by_expert.
-__global__ void __launch_bounds__(kDispatchThreads)
-    histogram_kernel(int64_t T, int E, int k, const int32_t* __restrict__ ids,
-                     int32_t* __restrict__ chunk_counts, int32_t* status, int* counter,
-                     int64_t C, int32_t* __restrict__ counts, int32_t* __restrict__ kept,
-                     AuxArgs aux, int skip_neg, const int32_t* __restrict__ cap_base) {
-  extern __shared__ int32_t hist[];
+__device__ __forceinline__ void histogram_body(int64_t T, int E, int k,
+                                               const int32_t* __restrict__ ids,
+                                               int32_t* __restrict__ chunk_counts,
+                                               int32_t* status, int* counter, int64_t C,
+                                               int32_t* __restrict__ counts,
+                                               int32_t* __restrict__ kept, const AuxArgs& aux,
+                                               int skip_neg, const int32_t* __restrict__ cap_base,
+                                               int32_t* hist) {
   __shared__ int s_last;
   __shared__ float s_red[kAuxThreads];
   __shared__ unsigned long long s_kept_sum;
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
-  pdl_wait();
-  pdl_trigger();
   __syncthreads();
   const int64_t t = int64_t(blockIdx.x) * kChunkTokens + threadIdx.x;
   if (t < T) {
@@ -125,6 +125,18 @@ __global__ void __launch_bounds__(kDispatchThreads)
       routing_health_block(E, T, k, counts_f, kept, aux.health, s_red, &s_kept_sum);
     }
   }
+}
+
+__global__ void __launch_bounds__(kDispatchThreads)
+    histogram_kernel(int64_t T, int E, int k, const int32_t* __restrict__ ids,
+                     int32_t* __restrict__ chunk_counts, int32_t* status, int* counter,
+                     int64_t C, int32_t* __restrict__ counts, int32_t* __restrict__ kept,
+                     AuxArgs aux, int skip_neg, const int32_t* __restrict__ cap_base) {
+  extern __shared__ int32_t hist[];
+  pdl_wait();
+  pdl_trigger();
+  histogram_body(T, E, k, ids, chunk_counts, status, counter, C, counts, kept, aux, skip_neg,
+                 cap_base, hist);
 }
 
 // One CTA per expert: exclusive scan of that expert's chunk counts (in place),
@@ -194,21 +206,20 @@ __device__ __forceinline__ void block_exclusive_scan(int E, const int32_t* __res
   __syncthreads();
 }
 
-__global__ void __launch_bounds__(kDispatchThreads)
-    assign_kernel(int64_t T, int E, int k, int64_t C, const int32_t* __restrict__ ids,
-                  const int32_t* __restrict__ chunk_base, const int32_t* __restrict__ kept,
-                  int32_t* __restrict__ offsets, int32_t* __restrict__ slot_row,
-                  int32_t* __restrict__ row_token, int positions_only,
-                  const int32_t* __restrict__ cap_base) {
-  extern __shared__ int32_t sm[];
+__device__ __forceinline__ void assign_body(int64_t T, int E, int k, int64_t C,
+                                            const int32_t* __restrict__ ids,
+                                            const int32_t* __restrict__ chunk_base,
+                                            const int32_t* __restrict__ kept,
+                                            int32_t* __restrict__ offsets,
+                                            int32_t* __restrict__ slot_row,
+                                            int32_t* __restrict__ row_token, int positions_only,
+                                            const int32_t* __restrict__ cap_base, int32_t* sm) {
   int32_t* off = sm;                       // [E+1]
   int32_t* wbase = sm + E + 1;             // [8][E]
   int32_t* s_ids = wbase + 8 * E;          // [256·k]
   __shared__ int32_t part[kDispatchThreads];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t chunk0 = int64_t(blockIdx.x) * kChunkTokens;
-  pdl_wait();
-  pdl_trigger();
   {
     // The chunk's ids, coalesced, once.
     const int64_t n_ids = (T - chunk0 < kChunkTokens ? T - chunk0 : kChunkTokens) * k;
@@ -267,6 +278,39 @@ __global__ void __launch_bounds__(kDispatchThreads)
     }
     __syncwarp();
   }
+}
+
+__global__ void __launch_bounds__(kDispatchThreads)
+    assign_kernel(int64_t T, int E, int k, int64_t C, const int32_t* __restrict__ ids,
+                  const int32_t* __restrict__ chunk_base, const int32_t* __restrict__ kept,
+                  int32_t* __restrict__ offsets, int32_t* __restrict__ slot_row,
+                  int32_t* __restrict__ row_token, int positions_only,
+                  const int32_t* __restrict__ cap_base) {
+  extern __shared__ int32_t sm[];
+  pdl_wait();
+  pdl_trigger();
+  assign_body(T, E, k, C, ids, chunk_base, kept, offsets, slot_row, row_token, positions_only,
+              cap_base, sm);
+}
+
+// A call with a single chunk (T <= 256, e.g. a decode step): histogram, scan,
+// statistics and positions in one block, so one launch instead of two.  The
+// block's own global writes (chunk base, counts, kept) are visible to it
+// after the barrier.
+__global__ void __launch_bounds__(kDispatchThreads)
+    dispatch_one_chunk_kernel(int64_t T, int E, int k, int64_t C,
+                              const int32_t* __restrict__ ids, int32_t* __restrict__ chunk_counts,
+                              int32_t* status, int* counter, int32_t* __restrict__ counts,
+                              int32_t* __restrict__ kept, AuxArgs aux,
+                              int32_t* __restrict__ offsets, int32_t* __restrict__ slot_row,
+                              int32_t* __restrict__ row_token) {
+  extern __shared__ int32_t sm[];
+  pdl_wait();
+  pdl_trigger();
+  histogram_body(T, E, k, ids, chunk_counts, status, counter, C, counts, kept, aux, 0, nullptr,
+                 sm);
+  __syncthreads();
+  assign_body(T, E, k, C, ids, chunk_counts, kept, offsets, slot_row, row_token, 0, nullptr, sm);
 }
 
 // Overflow reroute, step 2: the m-th slot of token t that the first fill
@@ -396,7 +440,16 @@ cudaError_t launch_dispatch(const moe_config_t& c, int64_t C, const void* x,
     count_launch();
     return e != cudaSuccess ? e : cudaGetLastError();
   };
-  if (!rr) {
+  if (!rr && counter && n_chunks == 1) {
+    err = ensure_dynamic_smem(reinterpret_cast<const void*>(dispatch_one_chunk_kernel),
+                              assign_smem);
+    if (err != cudaSuccess) return err;
+    err = launch_pdl(dispatch_one_chunk_kernel, dim3(1), dim3(kDispatchThreads), assign_smem, st,
+                     c.T, c.E, c.k, C, ids, chunk_counts, status, counter, counts, kept, aux_v,
+                     offsets, slot_row, row_token);
+    count_launch();
+    if (err != cudaSuccess || (err = cudaGetLastError()) != cudaSuccess) return err;
+  } else if (!rr) {
     if ((err = histogram(ids, counts, kept, aux_v, 0, nullptr)) != cudaSuccess) return err;
     if (!counter) {
       expert_scan_kernel<<<unsigned(c.E), 256, 0, st>>>(n_chunks, c.E, C, chunk_counts, counts,
