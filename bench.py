@@ -193,6 +193,28 @@ def cpu_oracle_sample(wl, host, budget_s: float = 15.0, seed_tokens: int = 8):
                        f"{S} tokens); {dt:.2f} s")
 
 
+def max_over_ranks(value, dist=None, device=None):
+    """The slowest rank's value (an all-reduce MAX over the process group;
+    the value itself without one)."""
+    t = torch.tensor([float(value)], dtype=torch.float64)
+    if dist is not None:
+        if device is not None:
+            t = t.to(device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world, tokens_per_rank, steps, max_ms):
+    """Whole-job throughput of independent replicas: the tokens of all ranks
+    over the slowest rank's time for the timed steps."""
+    return world * tokens_per_rank * steps / (max_ms * 1e-3)
+
+
+def replica_seed(seed, rank):
+    """Seed of rank `rank`'s own batch (every replica routes different tokens)."""
+    return seed * 1000 + rank
+
+
 def run_reference(args, wl, rank, world):
     if rank != 0:
         return 0
@@ -273,7 +295,7 @@ def main():
     if args.sel_bias:
         inp["sel_bias"] = inputs.selection_bias(wl, dev)
     if world > 1:  # each replica routes its own batch
-        g = torch.Generator(device=dev).manual_seed(wl.seed * 1000 + rank)
+        g = torch.Generator(device=dev).manual_seed(replica_seed(wl.seed, rank))
         inp["x"] = torch.randn(inp["x"].shape, generator=g, device=dev).to(inp["x"].dtype)
     cfg = moe.config_from_workload(wl, write_logits=False, reroute=args.reroute)
     ws = moe.workspace(cfg, dev)
@@ -365,11 +387,7 @@ def main():
         total_ms += evs[s_][0].elapsed_time(evs[s_][1])
         for i, name in enumerate(STAGES):
             stage_ms[name] += sevs[s_][i].elapsed_time(sevs[s_][i + 1])
-    t = torch.tensor([total_ms], dtype=torch.float64)
-    if dist is not None:
-        t = t.to(dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    max_ms = float(t.item())
+    max_ms = max_over_ranks(total_ms, dist, dev)
 
     offsets = out["offsets"].cpu()
     n_kept = int(offsets[-1])
@@ -411,18 +429,14 @@ def main():
         torch.cuda.synchronize(dev)
         e2e_ms += e_start.elapsed_time(e_end)
     e2e_ms /= e2e_steps
-    te = torch.tensor([e2e_ms], dtype=torch.float64)
-    if dist is not None:
-        te = te.to(dev)
-        dist.all_reduce(te, op=dist.ReduceOp.MAX)
-    e2e_ms = float(te.item())
+    e2e_ms = max_over_ranks(e2e_ms, dist, dev)
 
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
         return 0
 
-    value = world * wl.T * K / (max_ms * 1e-3)
+    value = job_tokens_per_s(world, wl.T, K, max_ms)
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         cpu = cpu_oracle_sample(wl, host_inputs(wl, inp))
