@@ -239,6 +239,14 @@ moe_status_t moe_aux_stats(const moe_config_t* cfg, const int32_t* counts, const
 moe_status_t moe_forward(const moe_config_t* cfg, const moe_tensors_t* t, float alpha, void* ws,
                          size_t ws_bytes, void* stream);
 
+/* Self-test of the bounded waits every kernel uses: one block waits on an
+ * mbarrier that nothing signals, gives up after limit_ns nanoseconds (the
+ * kernels' own limit is 4 s; 1e6 <= limit_ns <= 4e9) and records
+ * MOE_ERR_TIMEOUT in the workspace status word, then returns.  Read it with
+ * moe_get_device_status; moe_workspace_init clears it.  For tests. */
+moe_status_t moe_selftest_wait_timeout(void* ws, size_t ws_bytes, int64_t limit_ns,
+                                       void* stream);
+
 /* Read the workspace's device status word (a blocking copy; call after the
  * stream that used ws has been synchronised).  *status is MOE_OK or the
  * first asynchronous error recorded. */

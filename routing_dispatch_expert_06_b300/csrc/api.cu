@@ -491,6 +491,17 @@ moe_status_t moe_forward(const moe_config_t* cfg, const moe_tensors_t* t, float 
   return moe_combine(cfg, t->yd, t->slot_row, t->topk_w, t->y, stream);
 }
 
+moe_status_t moe_selftest_wait_timeout(void* ws, size_t ws_bytes, int64_t limit_ns,
+                                       void* stream) {
+  if (!ws || ws_bytes < kWsHeaderBytes)
+    return fail(MOE_ERR_INVALID_ARG, "moe_selftest_wait_timeout: workspace too small");
+  if (limit_ns < 1000000 || limit_ns > 4000000000LL)
+    return fail(MOE_ERR_INVALID_ARG, "moe_selftest_wait_timeout: limit_ns out of range");
+  cudaError_t e = launch_wait_timeout_selftest(static_cast<int32_t*>(ws), uint64_t(limit_ns),
+                                               static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_selftest_wait_timeout");
+}
+
 moe_status_t moe_get_device_status(const void* ws, int32_t* status) {
   if (!ws || !status) return fail(MOE_ERR_INVALID_ARG, "moe_get_device_status: NULL argument");
   cudaError_t e = cudaMemcpy(status, ws, sizeof(int32_t), cudaMemcpyDeviceToHost);

@@ -70,6 +70,9 @@ cudaError_t launch_route_select(const moe_config_t& c, const float* part, int ns
                                 unsigned long long* psum_fixed, float* psum, int* counter,
                                 bool finish, const float* sel_bias, int32_t* cand,
                                 cudaStream_t st);
+// One block waits on an mbarrier nothing signals, gives up after limit_ns and
+// records MOE_ERR_TIMEOUT in *status (self-test of the bounded waits).
+cudaError_t launch_wait_timeout_selftest(int32_t* status, uint64_t limit_ns, cudaStream_t st);
 // One block: the routing-health indicators from counts and kept.
 cudaError_t launch_health(const moe_config_t& c, const int32_t* counts, const int32_t* kept,
                           float* health, cudaStream_t st);

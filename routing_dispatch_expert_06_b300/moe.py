@@ -81,6 +81,7 @@ def load():
         "moe_aux_stats": (st, [cfgp, _P, _P, ctypes.c_float, _P, _P, _P, _P]),
         "moe_forward": (st, [cfgp, ctypes.POINTER(Tensors), ctypes.c_float, _P, sz, _P]),
         "moe_get_device_status": (st, [_P, ctypes.POINTER(ctypes.c_int32)]),
+        "moe_selftest_wait_timeout": (st, [_P, sz, i64, _P]),
         "moe_launch_count": (i64, []),
         "moe_status_string": (ctypes.c_char_p, [st]),
         "moe_last_error": (ctypes.c_char_p, []),
@@ -299,6 +300,17 @@ def forward_stages(cfg, inputs: dict, out: dict, ws, alpha=0.01, stream=None, ev
     if out.get("health") is not None:
         routing_health(cfg, out["counts"], out["kept"], out["health"], s)
     mark(6)
+
+
+def selftest_wait_timeout(ws, limit_ns: int, stream=None):
+    """moe_selftest_wait_timeout: a bounded wait that must give up and record
+    MOE_ERR_TIMEOUT in the workspace status word."""
+    _check(load().moe_selftest_wait_timeout(_ptr(ws), ws.numel(), int(limit_ns), _stream(stream)))
+
+
+def workspace_init(ws, stream=None):
+    """Clear a workspace's header (status word, counters, accumulators)."""
+    _check(load().moe_workspace_init(_ptr(ws), ws.numel(), _stream(stream)))
 
 
 def device_status(ws) -> int:

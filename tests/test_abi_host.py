@@ -144,3 +144,7 @@ def test_new_entry_points_reject_null_arguments(lib):
         moe.MOE_ERR_INVALID_ARG
     assert lib.moe_route_sel(ctypes.byref(cfg), None, None, None, None, None, None, None, None,
                              None, 0, None) == moe.MOE_ERR_INVALID_ARG
+
+
+def test_selftest_rejects_bad_arguments(lib):
+    assert lib.moe_selftest_wait_timeout(None, 0, 10**7, None) == moe.MOE_ERR_INVALID_ARG

@@ -274,3 +274,29 @@ def test_reroute_with_selection_bias():
     inp["sel_bias"] = inputs.selection_bias(wl, "cuda")
     _, inp, out, _ = run_gpu(wl, inp=inp, health=True, reroute=True)
     check_forward(wl, inp, out, full=True, reroute=True)
+
+
+def test_bounded_wait_gives_up_and_reports_timeout():
+    # A wait on a barrier that nothing signals (the same bounded wait the
+    # tensor-core kernels use) must give up after its limit, record
+    # MOE_ERR_TIMEOUT in the status word and leave the context usable.
+    import time
+
+    wl = W["bf16_t4096_d1024_e8_top2"]
+    cfg = moe.config_from_workload(wl, write_logits=True)
+    ws = moe.workspace(cfg)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    moe.selftest_wait_timeout(ws, 50_000_000)  # 50 ms
+    torch.cuda.synchronize()
+    assert time.time() - t0 < 5.0
+    assert moe.device_status(ws) == moe.MOE_ERR_TIMEOUT
+    moe.workspace_init(ws)
+    torch.cuda.synchronize()
+    assert moe.device_status(ws) == moe.MOE_OK
+    inp = inputs.make_inputs(wl, "cuda")
+    out = moe.allocate(cfg)
+    moe.forward(cfg, inp, out, ws, 1.0)
+    torch.cuda.synchronize()
+    assert moe.device_status(ws) == moe.MOE_OK
+    check_forward(wl, inp, out, n_tokens=256)
