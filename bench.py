@@ -137,14 +137,17 @@ def kernel_traffic(kernel: str, workload: str, src_file: str):
     return float(m_t.group(1))
 
 
-def algorithmic(wl, n_kept: int, t_kept: int):
-    """Bytes / FLOPs the method must move or compute per forward pass."""
+def algorithmic(wl, n_kept: int, t_kept: int, fused: bool = False):
+    """Bytes / FLOPs the method must move or compute per forward pass
+    (``fused``: the dispatch moves no rows, only ids, positions and
+    row_token; the first GEMM reads the token rows itself)."""
     b = 2 if wl.dtype == "bf16" else 4
     T, d, d_ff, E, k = wl.T, wl.d, wl.d_ff, wl.E, wl.k
+    rows = 0 if fused else t_kept * d * b + n_kept * d * b
     return dict(
         route_bytes=T * d * b + E * d * b + T * k * 8,
         route_flops=2 * T * d * E,
-        dispatch_bytes=t_kept * d * b + n_kept * d * b + T * k * 8 + n_kept * 4,
+        dispatch_bytes=rows + T * k * 8 + n_kept * 4,
         ffn_up_flops=2 * n_kept * d * d_ff,
         ffn_down_flops=2 * n_kept * d * d_ff,
         combine_bytes=n_kept * d * b + T * k * 8 + T * d * b,
@@ -266,6 +269,8 @@ def main():
                     help="also compute the routing-health indicators in the forward pass")
     ap.add_argument("--reroute", action="store_true",
                     help="offer overflowing slots to the token's next candidate")
+    ap.add_argument("--fuse-dispatch", action="store_true",
+                    help="no dispatch buffer: the first GEMM gathers the token rows")
     args = ap.parse_args()
     wl = inputs.WORKLOADS[args.workload]
 
@@ -297,7 +302,8 @@ def main():
     if world > 1:  # each replica routes its own batch
         g = torch.Generator(device=dev).manual_seed(replica_seed(wl.seed, rank))
         inp["x"] = torch.randn(inp["x"].shape, generator=g, device=dev).to(inp["x"].dtype)
-    cfg = moe.config_from_workload(wl, write_logits=False, reroute=args.reroute)
+    cfg = moe.config_from_workload(wl, write_logits=False, reroute=args.reroute,
+                                   fuse_dispatch=args.fuse_dispatch)
     ws = moe.workspace(cfg, dev)
     out = moe.allocate(cfg, dev, health=args.health)
     stream = torch.cuda.current_stream(dev)
@@ -325,8 +331,10 @@ def main():
         "route": lambda: moe.route(cfg, inp["x"], inp["Wr"], inp["br"], out, ws,
                                    sel_bias=inp.get("sel_bias")),
         "dispatch": lambda: moe.dispatch(cfg, inp["x"], out["topk_ids"], out, ws),
-        "ffn_up": lambda: moe.ffn_up(cfg, out["xd"], out["offsets"], inp["W1"], inp["b1"],
-                                     out["H"], ws),
+        "ffn_up": (lambda: moe.ffn_up_gather(cfg, inp["x"], out["row_token"], out["offsets"],
+                                             inp["W1"], inp["b1"], out["H"], ws))
+        if args.fuse_dispatch else
+        (lambda: moe.ffn_up(cfg, out["xd"], out["offsets"], inp["W1"], inp["b1"], out["H"], ws)),
         "ffn_down": lambda: moe.ffn_down(cfg, out["H"], out["offsets"], inp["W2"], inp["b2"],
                                          out["yd"], ws),
         "combine": lambda: moe.combine(cfg, out["yd"], out["slot_row"], out["topk_w"], out["y"]),
@@ -394,14 +402,15 @@ def main():
     touched = int((out["kept"].cpu() > 0).sum())
     slot = out["slot_row"].cpu()
     t_kept = int((slot >= 0).any(dim=1).sum())
-    alg = algorithmic(wl, n_kept, t_kept)
+    alg = algorithmic(wl, n_kept, t_kept, fused=args.fuse_dispatch)
     peaks = load_peaks()
     mean = {k: v / K for k, v in stage_ms.items()}
     ffn_ms = mean["ffn_up"] + mean["ffn_down"]
     dom = "ffn_up" if mean["ffn_up"] >= mean["ffn_down"] else "ffn_down"
     dom_tflops = alg[f"{dom}_flops"] / (mean[dom] * 1e-3) / 1e12
-    traffic = kernel_traffic(dom, wl.name, os.path.join(ROOT, "routing_dispatch_expert_06_b300",
-                                                        "csrc", "ffn_tc.cu"))
+    dom_kernel = "ffn_up_gather" if (dom == "ffn_up" and args.fuse_dispatch) else dom
+    traffic = kernel_traffic(dom_kernel, wl.name, os.path.join(
+        ROOT, "routing_dispatch_expert_06_b300", "csrc", "ffn_tc.cu"))
 
     # e2e: the public call with host buffers, H2D of x and D2H of y inside
     x_host = inp["x"].cpu().pin_memory()
@@ -449,9 +458,9 @@ def main():
                     capacity_factor=wl.capacity_factor, renormalize=wl.renormalize,
                     act=wl.act, parallelism=f"replicas{world}" if world > 1 else "single",
                     sel_bias=bool(args.sel_bias), health=bool(args.health),
-                    reroute=bool(args.reroute),
+                    reroute=bool(args.reroute), fuse_dispatch=bool(args.fuse_dispatch),
                     l2="flushed between steps (512 MiB write, then 512 MiB read)"),
-        roofline=dict(bound="tensor", kernel=f"{dom} (tcgen05 grouped GEMM)",
+        roofline=dict(bound="tensor", kernel=f"{dom_kernel} (tcgen05 grouped GEMM)",
                       achieved=dom_tflops, peak=peaks["bf16"], unit="TFLOP/s",
                       frac=dom_tflops / peaks["bf16"], traffic=traffic,
                       peak_source=f"{peaks['source']} bf16 burst"),

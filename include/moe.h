@@ -76,6 +76,7 @@ typedef struct moe_config {
   int32_t dtype;            /* MOE_DT_* : x, weights, xd, H, yd, y */
   int32_t write_logits;     /* 1: moe_route also writes fp32 logits[T,E] */
   int32_t reroute;          /* 1: overflow goes to the next candidate (§4.3) */
+  int32_t fuse_dispatch;    /* 1: no xd; the first GEMM gathers x rows (moe_ffn_up_gather) */
 } moe_config_t;
 
 /* Every tensor of one forward pass (all device pointers). */
@@ -155,7 +156,9 @@ moe_status_t moe_route(const moe_config_t* cfg, const void* x, const void* Wr, c
  * (token, rank) order into the room each expert has left, and an expert's
  * rerouted rows follow its own.  counts stay the first choices' (f_i is over
  * S_t); kept, offsets, slot_row and row_token are final; a rerouted slot keeps
- * its combine weight. */
+ * its combine weight.
+ * With cfg->fuse_dispatch no row is copied: xd may be NULL and is not
+ * written (moe_ffn_up_gather reads the rows from x). */
 moe_status_t moe_dispatch(const moe_config_t* cfg, const void* x, const int32_t* topk_ids,
                           int32_t* counts, int32_t* kept, int32_t* offsets, int32_t* slot_row,
                           int32_t* row_token, void* xd, void* ws, size_t ws_bytes, void* stream);
@@ -186,6 +189,21 @@ moe_status_t moe_dispatch_noalloc(const moe_config_t* cfg, const void* x,
 moe_status_t moe_ffn_up(const moe_config_t* cfg, const void* xd, const int32_t* offsets,
                         const void* W1, const float* b1, void* H, void* ws, size_t ws_bytes,
                         void* stream);
+
+/* moe_ffn_up with the permutation folded into the GEMM's operand load (the
+ * fused permutation/dispatch kernel of [MoE Gate 分布式通信 mianshidashi,
+ * 06]): H[row] = σ(x[row_token[row]] W1[e]ᵀ + b1[e]) for the rows of each
+ * expert e, so the dispatch buffer xd is neither written nor read.  Same
+ * result, bit for bit, as moe_ffn_up on the xd that moe_dispatch would write.
+ *  - x [T, d] and row_token (from moe_dispatch) are device pointers; x, W1
+ *    and H 16-byte aligned; a row_token entry outside [0, T) reads as a zero
+ *    row;
+ *  - bf16 layers on the tensor-core GEMM only: MOE_ERR_UNSUPPORTED (no
+ *    launch) for fp32 layers and for layers with at most 64 rows per expert
+ *    (min(C, T·k) <= 64, the swapped decode GEMM). */
+moe_status_t moe_ffn_up_gather(const moe_config_t* cfg, const void* x, const int32_t* row_token,
+                               const int32_t* offsets, const void* W1, const float* b1, void* H,
+                               void* ws, size_t ws_bytes, void* stream);
 
 /* [MoE 模型原理 §1] Second expert GEMM: yd[rows of e] = H W2[e]ᵀ + b2[e]. */
 moe_status_t moe_ffn_down(const moe_config_t* cfg, const void* H, const int32_t* offsets,
@@ -233,9 +251,12 @@ moe_status_t moe_aux_stats(const moe_config_t* cfg, const int32_t* counts, const
  * arithmetic and results as moe_aux_stats; psum is also formed there from the
  * router's fixed-point column sums).  t->sel_bias (optional) routes as
  * moe_route_sel; t->health (optional) receives moe_routing_health's
- * indicators, computed in the same dispatch launch.  If it returns an error after the router
- * was enqueued, call moe_workspace_init before the next call on that
- * workspace. */
+ * indicators, computed in the same dispatch launch.  With cfg->fuse_dispatch
+ * t->xd may be NULL: the dispatch writes positions and row_token only and
+ * the first GEMM runs as moe_ffn_up_gather (MOE_ERR_UNSUPPORTED, before any
+ * launch, where that call is unsupported); every other output is identical.
+ * If it returns an error after the router was enqueued, call
+ * moe_workspace_init before the next call on that workspace. */
 moe_status_t moe_forward(const moe_config_t* cfg, const moe_tensors_t* t, float alpha, void* ws,
                          size_t ws_bytes, void* stream);
 

@@ -141,6 +141,8 @@ static moe_status_t check_cfg(const moe_config_t* c) {
   if (c->act != MOE_ACT_RELU && c->act != MOE_ACT_GELU_TANH)
     return fail(MOE_ERR_UNSUPPORTED, "act must be MOE_ACT_RELU or MOE_ACT_GELU_TANH");
   if (c->reroute != 0 && c->reroute != 1) return fail(MOE_ERR_INVALID_ARG, "reroute must be 0 or 1");
+  if (c->fuse_dispatch != 0 && c->fuse_dispatch != 1)
+    return fail(MOE_ERR_INVALID_ARG, "fuse_dispatch must be 0 or 1");
   return MOE_OK;
 }
 
@@ -225,6 +227,12 @@ static bool use_tc_gemm(const moe_config_t& c) {
   if (c.dtype != MOE_DT_BF16) return false;
   const char* v = std::getenv("MOE_FFN_IMPL");
   return !(v && std::strcmp(v, "simt") == 0);
+}
+
+// The gathering first GEMM exists for the regular tcgen05 kernel only (bf16,
+// more than 64 rows per expert possible).
+static bool gather_supported(const moe_config_t& c) {
+  return use_tc_gemm(c) && !gemm_swap_applies(rows_per_expert_max(&c));
 }
 
 // Which router runs.  bf16 layers: the tcgen05 router for E <= 256, else the
@@ -360,9 +368,13 @@ static moe_status_t dispatch_impl(const moe_config_t* cfg, const void* x,
                                   void* stream) {
   moe_status_t s = check_cfg(cfg);
   if (s != MOE_OK) return s;
-  if (!x || !topk_ids || !counts || !kept || !offsets || !slot_row || !row_token || !xd)
+  if (!x || !topk_ids || !counts || !kept || !offsets || !slot_row || !row_token ||
+      (!xd && !cfg->fuse_dispatch))
     return fail(MOE_ERR_INVALID_ARG, "moe_dispatch: NULL tensor");
-  if (!aligned16(x) || !aligned16(xd))
+  // With fuse_dispatch the rows are not copied (xd may be NULL, and is not
+  // written).
+  if (cfg->fuse_dispatch) xd = nullptr;
+  if (!aligned16(x) || (xd && !aligned16(xd)))
     return fail(MOE_ERR_INVALID_ARG, "moe_dispatch: x and xd must be 16-byte aligned");
   Ws w;
   if ((s = get_ws(*cfg, ws, ws_bytes, &w)) != MOE_OK) return s;
@@ -408,6 +420,27 @@ moe_status_t moe_ffn_up(const moe_config_t* cfg, const void* xd, const int32_t* 
           : launch_gemm_tc(cfg->E, cfg->d_ff, cfg->d, R, offsets, xd, W1, b1, cfg->act, H,
                            w.status, st);
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_ffn_up");
+}
+
+moe_status_t moe_ffn_up_gather(const moe_config_t* cfg, const void* x, const int32_t* row_token,
+                               const int32_t* offsets, const void* W1, const float* b1, void* H,
+                               void* ws, size_t ws_bytes, void* stream) {
+  moe_status_t s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  if (!x || !row_token || !offsets || !W1 || !b1 || !H)
+    return fail(MOE_ERR_INVALID_ARG, "moe_ffn_up_gather: NULL tensor");
+  if (!aligned16(x) || !aligned16(W1) || !aligned16(H))
+    return fail(MOE_ERR_INVALID_ARG, "moe_ffn_up_gather: x, W1, H must be 16-byte aligned");
+  if (!gather_supported(*cfg))
+    return fail(MOE_ERR_UNSUPPORTED,
+                "moe_ffn_up_gather: needs bf16 and the tensor-core GEMM for more than 64 rows "
+                "per expert");
+  Ws w;
+  if ((s = get_ws(*cfg, ws, ws_bytes, &w)) != MOE_OK) return s;
+  cudaError_t e = launch_gemm_tc_gather(cfg->E, cfg->d_ff, cfg->d, moe_max_rows(cfg), offsets, x,
+                                        cfg->T, row_token, W1, b1, cfg->act, H, w.status,
+                                        static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_ffn_up_gather");
 }
 
 moe_status_t moe_ffn_down(const moe_config_t* cfg, const void* H, const int32_t* offsets,
@@ -473,7 +506,12 @@ moe_status_t moe_forward(const moe_config_t* cfg, const moe_tensors_t* t, float 
   if (!t) return fail(MOE_ERR_INVALID_ARG, "moe_forward: tensors is NULL");
   if (!t->f || !t->pbar || !t->l_aux)
     return fail(MOE_ERR_INVALID_ARG, "moe_aux_stats: NULL tensor");
-  moe_status_t s;
+  moe_status_t s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  if (cfg->fuse_dispatch && !gather_supported(*cfg))
+    return fail(MOE_ERR_UNSUPPORTED,
+                "moe_forward: fuse_dispatch needs bf16 and the tensor-core GEMM for more than 64 "
+                "rows per expert");
   unsigned long long* psum_fixed = nullptr;
   if ((s = route_impl(cfg, t->x, t->Wr, t->br, t->sel_bias, t->logits, t->topk_ids, t->topk_w,
                       t->psum, ws, ws_bytes, &psum_fixed, stream)) != MOE_OK)
@@ -485,9 +523,16 @@ moe_status_t moe_forward(const moe_config_t* cfg, const moe_tensors_t* t, float 
   if ((s = dispatch_impl(cfg, t->x, t->topk_ids, t->counts, t->kept, t->offsets, t->slot_row,
                          t->row_token, t->xd, ws, ws_bytes, &aux, stream)) != MOE_OK)
     return s;
-  if ((s = moe_expert_ffn(cfg, t->xd, t->offsets, t->W1, t->b1, t->W2, t->b2, t->H, t->yd, ws,
-                          ws_bytes, stream)) != MOE_OK)
+  if (cfg->fuse_dispatch) {
+    if ((s = moe_ffn_up_gather(cfg, t->x, t->row_token, t->offsets, t->W1, t->b1, t->H, ws,
+                               ws_bytes, stream)) != MOE_OK ||
+        (s = moe_ffn_down(cfg, t->H, t->offsets, t->W2, t->b2, t->yd, ws, ws_bytes, stream)) !=
+            MOE_OK)
+      return s;
+  } else if ((s = moe_expert_ffn(cfg, t->xd, t->offsets, t->W1, t->b1, t->W2, t->b2, t->H, t->yd,
+                                 ws, ws_bytes, stream)) != MOE_OK) {
     return s;
+  }
   return moe_combine(cfg, t->yd, t->slot_row, t->topk_w, t->y, stream);
 }
 

@@ -486,6 +486,7 @@ cudaError_t launch_dispatch(const moe_config_t& c, int64_t C, const void* x,
     count_launch();
     if (err != cudaSuccess || (err = cudaGetLastError()) != cudaSuccess) return err;
   }
+  if (!xd) return cudaSuccess;  // the first GEMM gathers the rows itself
   const int elem = c.dtype == MOE_DT_BF16 ? 2 : 4;
   const int64_t row_vecs = int64_t(c.d) * elem / 16;
   const RowSplit rs = row_split(c.T, row_vecs, 128);

@@ -136,12 +136,19 @@ __device__ __forceinline__ float epi_act(float u) {
   return u;
 }
 
-template <int ACT, bool PAIR>
+// GATHER: the A rows are not read from a dispatch buffer but gathered from
+// the token matrix x [gx_rows, K] through row_token (A[row] = x[row_token[row]],
+// tmA a 64 × 1-box map over x): the permutation of [MoE 模型原理 §5] folded
+// into the first GEMM's operand load, the fused permutation/dispatch kernel
+// of [MoE Gate 分布式通信 mianshidashi, 06].  Every lane of warp 0 then
+// issues TMA gather4 copies of four rows each, while lane 0 still loads B.
+template <int ACT, bool PAIR, bool GATHER>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    int E, int N, int K, int BN, const int32_t* __restrict__ offsets,
                    const float* __restrict__ bias, __nv_bfloat16* __restrict__ out,
-                   int64_t max_rows, int32_t* status, int stages, int set) {
+                   int64_t max_rows, int32_t* status, int stages, int set,
+                   const int32_t* __restrict__ row_token, int64_t gx_rows) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages];
   __shared__ uint64_t tfull_bar[2], tempty_bar[2], drain_bar;
@@ -246,7 +253,68 @@ __global__ void __launch_bounds__(kThreads, 1)
     set_status(status, MOE_ERR_TIMEOUT);
   };
 
-  if (warp == 0 && lane == 0) {
+  if (warp == 0 && GATHER) {
+    // ---------------- gathering producer (whole warp) ----------------
+    // Lane j gathers rows 4j .. 4j+3 of the 128-row A tile with one TMA
+    // gather4 per k-block into bytes [512j, 512j + 512) of the stage: the
+    // same 128-byte-swizzled layout a 64 × 128 box would write (each stage is
+    // 1024-byte aligned).  Rows past the expert's end read token row 0 (they
+    // are computed but never stored); lane 0 waits for the slot, posts the
+    // stage's byte count and loads B.
+    int stage = 0;
+    uint32_t phase = 0;
+    int64_t issued = 0;
+    bool ok = true;
+    for (int64_t i = first_tile; i < total && ok; i += tile_step) {
+      const TileCoord c =
+          tile_coord(i, s_mt, E, n_tn, s_off, BN, rows_per_tile, int(rank), set);
+      int32_t t4[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int g = c.m0 + 4 * lane + q;
+        const int32_t t = g < c.m_end ? row_token[g] : 0;
+        t4[q] = (t >= 0 && int64_t(t) < gx_rows) ? t : 0;
+      }
+      for (int kb = 0; kb < nk; ++kb) {
+        int free_slot = 1;
+        if (lane == 0)
+          free_slot = tc::mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, kWaitLimitNs);
+        if (!__shfl_sync(0xffffffffu, free_slot, 0)) {
+          if (lane == 0) give_up();
+          ok = false;
+          break;
+        }
+        uint8_t* dst = sA + stage * a_bytes + lane * 512;
+        if constexpr (PAIR) {
+          const uint32_t bar = tc::mapa(tc::smem_u32(&full_bar[stage]), 0);
+          if (lane == 0) {
+            if (rank == 0) tc::mbar_arrive_expect_tx(&full_bar[stage], 2 * (a_bytes + b_bytes));
+            tc::tma_load_3d_pair(&tmB, bar, sB + stage * b_bytes, kb * kTileK,
+                                 c.n0 + int(rank) * bn_cta, c.e);
+          }
+          __syncwarp();
+          tc::tma_gather4_pair(&tmA, bar, dst, kb * kTileK, t4[0], t4[1], t4[2], t4[3]);
+        } else {
+          if (lane == 0) {
+            tc::mbar_arrive_expect_tx(&full_bar[stage], a_bytes + b_bytes);
+            tc::tma_load_3d(&tmB, &full_bar[stage], sB + stage * b_bytes, kb * kTileK, c.n0,
+                            c.e);
+          }
+          __syncwarp();
+          tc::tma_gather4(&tmA, &full_bar[stage], dst, kb * kTileK, t4[0], t4[1], t4[2], t4[3]);
+        }
+        ++issued;
+        if (++stage == stages) stage = 0, phase ^= 1u;
+      }
+    }
+    // Drain as the TMA producer does: the last `stages` stages land before
+    // the CTA exits.
+    if (rank == 0 && lane == 0) {
+      const int64_t first = issued > stages ? issued - stages : 0;
+      for (int64_t j = first; j < issued; ++j)
+        tc::mbar_wait(&full_bar[j % stages], uint32_t((j / stages) & 1), nullptr, kWaitLimitNs);
+    }
+  } else if (warp == 0 && lane == 0) {
     // ---------------- TMA producer ----------------
     int stage = 0;
     uint32_t phase = 0;
@@ -486,13 +554,21 @@ bool use_pair() {
   return !(v && std::strcmp(v, "0") == 0);
 }
 
-template <bool PAIR>
+// Gathered A rows (GATHER): row_token and the rows of the token matrix,
+// else unused.
+struct Gather {
+  const int32_t* row_token;
+  int64_t gx_rows;
+};
+
+template <bool PAIR, bool GATHER>
 cudaError_t launch_variant(int act, const CUtensorMap& tmA, const CUtensorMap& tmB, int E, int N,
                            int K, int BN, const int32_t* offsets, const float* bias, void* out,
-                           int64_t max_rows, int32_t* status, int set, cudaStream_t st) {
+                           int64_t max_rows, int32_t* status, int set, const Gather& g,
+                           cudaStream_t st) {
   const int sms = device_sms();
   const size_t static_smem =
-      kernel_static_smem(reinterpret_cast<const void*>(gemm_tc_kernel<kActNone, PAIR>));
+      kernel_static_smem(reinterpret_cast<const void*>(gemm_tc_kernel<kActNone, PAIR, false>));
   // As many pipeline stages as fit beside the epilogue buffers and the
   // kernel's static shared memory.
   const int bn_cta = PAIR ? BN / 2 : BN;
@@ -535,13 +611,97 @@ cudaError_t launch_variant(int act, const CUtensorMap& tmA, const CUtensorMap& t
     cfg.attrs = attr;
     cfg.numAttrs += 1;
     e = cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, E, N, K, BN, offsets, bias,
-                           static_cast<__nv_bfloat16*>(out), max_rows, status, stages, set);
+                           static_cast<__nv_bfloat16*>(out), max_rows, status, stages, set,
+                           g.row_token, g.gx_rows);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
   };
-  return act == MOE_ACT_RELU        ? run(gemm_tc_kernel<MOE_ACT_RELU, PAIR>)
-         : act == MOE_ACT_GELU_TANH ? run(gemm_tc_kernel<MOE_ACT_GELU_TANH, PAIR>)
-                                    : run(gemm_tc_kernel<kActNone, PAIR>);
+  if constexpr (GATHER) {
+    // Only the first GEMM gathers, and it always has an activation.
+    return act == MOE_ACT_RELU        ? run(gemm_tc_kernel<MOE_ACT_RELU, PAIR, true>)
+           : act == MOE_ACT_GELU_TANH ? run(gemm_tc_kernel<MOE_ACT_GELU_TANH, PAIR, true>)
+                                      : cudaErrorInvalidValue;
+  } else {
+    return act == MOE_ACT_RELU        ? run(gemm_tc_kernel<MOE_ACT_RELU, PAIR, false>)
+           : act == MOE_ACT_GELU_TANH ? run(gemm_tc_kernel<MOE_ACT_GELU_TANH, PAIR, false>)
+                                      : run(gemm_tc_kernel<kActNone, PAIR, false>);
+  }
+}
+
+template <bool GATHER>
+cudaError_t launch_sets(int act, const CUtensorMap& tmA, const CUtensorMap& tmB_cta,
+                        const CUtensorMap* tmB_pair, int E, int N, int K, int BN,
+                        const int32_t* offsets, const float* bias, void* out, int64_t max_rows,
+                        int32_t* status, const Gather& g, cudaStream_t st) {
+  cudaError_t err;
+  if (tmB_pair && E >= kTailSplitMinExperts) {
+    // CTA pairs take every expert's whole 256-row tiles (and a last one with
+    // more than 128 rows); one-CTA tiles take the remaining 1..128 rows, so
+    // no pair computes a 128-row half that lies past its expert's end.
+    err = launch_variant<true, GATHER>(act, tmA, *tmB_pair, E, N, K, BN, offsets, bias, out,
+                                       max_rows, status, kPairBody, g, st);
+    if (err != cudaSuccess) return err;
+    count_launch();
+    err = launch_variant<false, GATHER>(act, tmA, tmB_cta, E, N, K, BN, offsets, bias, out,
+                                        max_rows, status, kTail, g, st);
+  } else if (tmB_pair) {
+    err = launch_variant<true, GATHER>(act, tmA, *tmB_pair, E, N, K, BN, offsets, bias, out,
+                                       max_rows, status, kAllTiles, g, st);
+  } else {
+    err = launch_variant<false, GATHER>(act, tmA, tmB_cta, E, N, K, BN, offsets, bias, out,
+                                        max_rows, status, kAllTiles, g, st);
+  }
+  if (err != cudaSuccess) return err;
+  count_launch();
+  return cudaSuccess;
+}
+
+}  // namespace
+
+namespace {
+
+// A tensor map over A [rows, K] (K contiguous): 64 × 128 boxes over the
+// dispatch buffer, or 64 × 1 boxes (the gather4 form) over the token matrix.
+bool encode_a(EncodeTiledFn encode, CUtensorMap* m, const void* A, int K, int64_t rows,
+              int box_rows) {
+  const cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(rows)};
+  const cuuint64_t strides[1] = {cuuint64_t(K) * 2};
+  const cuuint32_t box[2] = {kTileK, cuuint32_t(box_rows)};
+  const cuuint32_t es[2] = {1, 1};
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(A), dims, strides, box,
+                es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// B tiles of BN rows (one CTA) or BN/2 rows (each CTA of a pair).
+bool encode_b(EncodeTiledFn encode, CUtensorMap* m, const void* B, int E, int N, int K,
+              int box_rows) {
+  const cuuint64_t dims[3] = {cuuint64_t(K), cuuint64_t(N), cuuint64_t(E)};
+  const cuuint64_t strides[2] = {cuuint64_t(K) * 2, cuuint64_t(N) * K * 2};
+  const cuuint32_t box[3] = {kTileK, cuuint32_t(box_rows), 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(B), dims, strides, box,
+                es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool GATHER>
+cudaError_t launch_gemm(int E, int N, int K, int64_t max_rows, const int32_t* offsets,
+                        const void* A, int64_t a_rows, const void* B, const float* bias, int act,
+                        void* out, int32_t* status, const Gather& g, cudaStream_t st) {
+  if (E > kMaxExperts) return cudaErrorInvalidValue;
+  EncodeTiledFn encode = get_encode();
+  if (!encode) return cudaErrorNotSupported;
+  const int BN = pick_bn(N);
+  CUtensorMap tmA, tmB_cta, tmB_pair;
+  if (!encode_a(encode, &tmA, A, K, a_rows, GATHER ? 1 : kTileM)) return cudaErrorInvalidValue;
+  if (!encode_b(encode, &tmB_cta, B, E, N, K, BN)) return cudaErrorInvalidValue;
+  const bool pair = use_pair();
+  if (pair && !encode_b(encode, &tmB_pair, B, E, N, K, BN / 2)) return cudaErrorInvalidValue;
+  return launch_sets<GATHER>(act, tmA, tmB_cta, pair ? &tmB_pair : nullptr, E, N, K, BN, offsets,
+                             bias, out, max_rows, status, g, st);
 }
 
 }  // namespace
@@ -549,61 +709,18 @@ cudaError_t launch_variant(int act, const CUtensorMap& tmA, const CUtensorMap& t
 cudaError_t launch_gemm_tc(int E, int N, int K, int64_t max_rows, const int32_t* offsets,
                            const void* A, const void* B, const float* bias, int act, void* out,
                            int32_t* status, cudaStream_t st) {
-  if (E > kMaxExperts) return cudaErrorInvalidValue;
-  EncodeTiledFn encode = get_encode();
-  if (!encode) return cudaErrorNotSupported;
-  const int BN = pick_bn(N);
-  const bool pair = use_pair();
-  CUtensorMap tmA;
-  {
-    const cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(max_rows)};
-    const cuuint64_t strides[1] = {cuuint64_t(K) * 2};
-    const cuuint32_t box[2] = {kTileK, kTileM};
-    const cuuint32_t es[2] = {1, 1};
-    if (encode(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(A), dims, strides, box,
-               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
-  // B tiles of BN rows (one CTA) or BN/2 rows (each CTA of a pair).
-  auto encode_b = [&](CUtensorMap* m, int box_rows) {
-    const cuuint64_t dims[3] = {cuuint64_t(K), cuuint64_t(N), cuuint64_t(E)};
-    const cuuint64_t strides[2] = {cuuint64_t(K) * 2, cuuint64_t(N) * K * 2};
-    const cuuint32_t box[3] = {kTileK, cuuint32_t(box_rows), 1};
-    const cuuint32_t es[3] = {1, 1, 1};
-    return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(B), dims, strides,
-                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-  };
-  CUtensorMap tmB_cta;
-  if (!encode_b(&tmB_cta, BN)) return cudaErrorInvalidValue;
-  cudaError_t err;
-  if (pair && E >= kTailSplitMinExperts) {
-    // CTA pairs take every expert's whole 256-row tiles (and a last one with
-    // more than 128 rows); one-CTA tiles take the remaining 1..128 rows, so
-    // no pair computes a 128-row half that lies past its expert's end.
-    CUtensorMap tmB_pair;
-    if (!encode_b(&tmB_pair, BN / 2)) return cudaErrorInvalidValue;
-    err = launch_variant<true>(act, tmA, tmB_pair, E, N, K, BN, offsets, bias, out, max_rows,
-                               status, kPairBody, st);
-    if (err != cudaSuccess) return err;
-    count_launch();
-    err = launch_variant<false>(act, tmA, tmB_cta, E, N, K, BN, offsets, bias, out, max_rows,
-                                status, kTail, st);
-  } else if (pair) {
-    CUtensorMap tmB_pair;
-    if (!encode_b(&tmB_pair, BN / 2)) return cudaErrorInvalidValue;
-    err = launch_variant<true>(act, tmA, tmB_pair, E, N, K, BN, offsets, bias, out, max_rows,
-                               status, kAllTiles, st);
-  } else {
-    err = launch_variant<false>(act, tmA, tmB_cta, E, N, K, BN, offsets, bias, out, max_rows,
-                                status, kAllTiles, st);
-  }
-  if (err != cudaSuccess) return err;
-  count_launch();
-  return cudaSuccess;
+  const Gather none{nullptr, 0};
+  return launch_gemm<false>(E, N, K, max_rows, offsets, A, max_rows, B, bias, act, out, status,
+                            none, st);
+}
+
+cudaError_t launch_gemm_tc_gather(int E, int N, int K, int64_t max_rows, const int32_t* offsets,
+                                  const void* x, int64_t T, const int32_t* row_token,
+                                  const void* B, const float* bias, int act, void* out,
+                                  int32_t* status, cudaStream_t st) {
+  if (act != MOE_ACT_RELU && act != MOE_ACT_GELU_TANH) return cudaErrorInvalidValue;
+  const Gather g{row_token, T};
+  return launch_gemm<true>(E, N, K, max_rows, offsets, x, T, B, bias, act, out, status, g, st);
 }
 
 }  // namespace moe

@@ -93,7 +93,8 @@ struct RerouteBufs {
 // last histogram block then runs the scan, and with aux != NULL also the
 // f / p̄ / L_aux statistics), or NULL for a separate scan kernel.  rr (needs
 // counter): the reroute variant (first fill as positions, offers, second
-// fill into the room left, final rows).
+// fill into the room left, final rows).  xd == NULL: positions and row_token
+// only, no row copy (the first GEMM then gathers its rows).
 cudaError_t launch_dispatch(const moe_config_t& c, int64_t C, const void* x,
                             const int32_t* ids, int32_t* counts, int32_t* kept,
                             int32_t* offsets, int32_t* slot_row, int32_t* row_token, void* xd,
@@ -111,6 +112,13 @@ cudaError_t launch_gemm_simt(int dtype, int E, int N, int K, int64_t max_rows,
 cudaError_t launch_gemm_tc(int E, int N, int K, int64_t max_rows, const int32_t* offsets,
                            const void* A, const void* B, const float* bias, int act,
                            void* out, int32_t* status, cudaStream_t st);
+// The same GEMM with its A rows gathered from the token matrix x [T, K]:
+// A[row] = x[row_token[row]] (the dispatch buffer is never written).  act must
+// be an activation (the first GEMM).
+cudaError_t launch_gemm_tc_gather(int E, int N, int K, int64_t max_rows, const int32_t* offsets,
+                                  const void* x, int64_t T, const int32_t* row_token,
+                                  const void* B, const float* bias, int act, void* out,
+                                  int32_t* status, cudaStream_t st);
 // The same GEMM with the operands' roles swapped (MMA M over weight rows, N
 // over an expert's rows), for layers where no expert holds more than
 // rows_per_expert_max <= 64 rows (gemm_swap_applies).

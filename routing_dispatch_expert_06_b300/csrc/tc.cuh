@@ -161,6 +161,32 @@ __device__ __forceinline__ void tma_load_3d_pair(const CUtensorMap* m, uint32_t 
       : "memory");
 }
 
+// Row gather: four rows (y0..y3) of 64 bf16 columns from column x of a 2-D
+// tensor map whose box is 64 × 1, written as four consecutive 128-byte rows
+// at dst with the map's swizzle (a row's pattern follows its shared-memory
+// address, so a 512-byte aligned dst inside a 1024-byte atom continues it).
+__device__ __forceinline__ void tma_gather4(const CUtensorMap* m, uint64_t* bar, void* dst,
+                                            int32_t x, int32_t y0, int32_t y1, int32_t y2,
+                                            int32_t y3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(m), "r"(smem_u32(bar)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3)
+      : "memory");
+}
+// The same for a CTA pair: completion on the barrier at the shared::cluster
+// address bar_cluster (the even CTA's).
+__device__ __forceinline__ void tma_gather4_pair(const CUtensorMap* m, uint32_t bar_cluster,
+                                                 void* dst, int32_t x, int32_t y0, int32_t y1,
+                                                 int32_t y2, int32_t y3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile::gather4"
+      ".mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(
+          smem_u32(dst)),
+      "l"(m), "r"(bar_cluster), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3)
+      : "memory");
+}
+
 // ---- tcgen05 ----------------------------------------------------------------
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(

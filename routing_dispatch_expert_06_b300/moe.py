@@ -37,7 +37,8 @@ class Config(ctypes.Structure):
                 ("E", ctypes.c_int32), ("k", ctypes.c_int32),
                 ("capacity_factor", ctypes.c_double), ("renormalize", ctypes.c_int32),
                 ("act", ctypes.c_int32), ("dtype", ctypes.c_int32),
-                ("write_logits", ctypes.c_int32), ("reroute", ctypes.c_int32)]
+                ("write_logits", ctypes.c_int32), ("reroute", ctypes.c_int32),
+                ("fuse_dispatch", ctypes.c_int32)]
 
 
 _TENSOR_FIELDS = ["x", "Wr", "br", "W1", "b1", "W2", "b2", "logits", "topk_ids", "topk_w",
@@ -75,6 +76,7 @@ def load():
         "moe_dispatch": (st, [cfgp, _P, _P, _P, _P, _P, _P, _P, _P, _P, sz, _P]),
         "moe_dispatch_noalloc": (st, [cfgp, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
         "moe_ffn_up": (st, [cfgp, _P, _P, _P, _P, _P, _P, sz, _P]),
+        "moe_ffn_up_gather": (st, [cfgp, _P, _P, _P, _P, _P, _P, _P, sz, _P]),
         "moe_ffn_down": (st, [cfgp, _P, _P, _P, _P, _P, _P, sz, _P]),
         "moe_expert_ffn": (st, [cfgp, _P, _P, _P, _P, _P, _P, _P, _P, _P, sz, _P]),
         "moe_combine": (st, [cfgp, _P, _P, _P, _P, _P]),
@@ -122,17 +124,18 @@ def _stream(stream=None):
 
 
 def config(T, d, d_ff, E, k, capacity_factor, renormalize=True, act="gelu_tanh", dtype="bf16",
-           write_logits=False, reroute=False) -> Config:
+           write_logits=False, reroute=False, fuse_dispatch=False) -> Config:
     return Config(T=T, d=d, d_ff=d_ff, E=E, k=k, capacity_factor=float(capacity_factor),
                   renormalize=int(bool(renormalize)),
                   act=MOE_ACT_RELU if act == "relu" else MOE_ACT_GELU_TANH,
                   dtype=MOE_DT_BF16 if dtype == "bf16" else MOE_DT_F32,
-                  write_logits=int(bool(write_logits)), reroute=int(bool(reroute)))
+                  write_logits=int(bool(write_logits)), reroute=int(bool(reroute)),
+                  fuse_dispatch=int(bool(fuse_dispatch)))
 
 
-def config_from_workload(wl, write_logits=False, reroute=False) -> Config:
+def config_from_workload(wl, write_logits=False, reroute=False, fuse_dispatch=False) -> Config:
     return config(wl.T, wl.d, wl.d_ff, wl.E, wl.k, wl.capacity_factor, wl.renormalize, wl.act,
-                  wl.dtype, write_logits, reroute)
+                  wl.dtype, write_logits, reroute, fuse_dispatch)
 
 
 def capacity(cfg: Config) -> int:
@@ -169,7 +172,7 @@ def workspace(cfg: Config, device="cuda", stream=None) -> torch.Tensor:
 def allocate(cfg: Config, device="cuda", health: bool = False) -> dict:
     """Allocate every output and intermediate tensor of one forward pass
     (``health``: also the 4 routing-health indicators, which forward() then
-    computes)."""
+    computes; with ``cfg.fuse_dispatch`` there is no dispatch buffer xd)."""
     dt = act_dtype(cfg)
     T, d, d_ff, E, k = cfg.T, cfg.d, cfg.d_ff, cfg.E, cfg.k
     R = max(max_rows(cfg), 1)
@@ -184,7 +187,7 @@ def allocate(cfg: Config, device="cuda", health: bool = False) -> dict:
         offsets=torch.empty(E + 1, dtype=torch.int32, **z),
         slot_row=torch.empty((T, k), dtype=torch.int32, **z),
         row_token=torch.empty(R, dtype=torch.int32, **z),
-        xd=torch.empty((R, d), dtype=dt, **z),
+        xd=None if cfg.fuse_dispatch else torch.empty((R, d), dtype=dt, **z),
         H=torch.empty((R, d_ff), dtype=dt, **z),
         yd=torch.empty((R, d), dtype=dt, **z),
         y=torch.empty((T, d), dtype=dt, **z),
@@ -218,7 +221,7 @@ def routing_health(cfg, counts, kept, health, stream=None):
 def dispatch(cfg, x, topk_ids, out, ws, stream=None):
     _check(load().moe_dispatch(ctypes.byref(cfg), _ptr(x), _ptr(topk_ids), _ptr(out["counts"]),
                                _ptr(out["kept"]), _ptr(out["offsets"]), _ptr(out["slot_row"]),
-                               _ptr(out["row_token"]), _ptr(out["xd"]), _ptr(ws), ws.numel(),
+                               _ptr(out["row_token"]), _ptr(out.get("xd")), _ptr(ws), ws.numel(),
                                _stream(stream)))
 
 
@@ -234,6 +237,13 @@ def dispatch_noalloc(cfg, x, topk_ids, out, status=None, stream=None):
 def ffn_up(cfg, xd, offsets, W1, b1, H, ws, stream=None):
     _check(load().moe_ffn_up(ctypes.byref(cfg), _ptr(xd), _ptr(offsets), _ptr(W1), _ptr(b1),
                              _ptr(H), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def ffn_up_gather(cfg, x, row_token, offsets, W1, b1, H, ws, stream=None):
+    """moe_ffn_up_gather: the first GEMM on the rows x[row_token[row]]."""
+    _check(load().moe_ffn_up_gather(ctypes.byref(cfg), _ptr(x), _ptr(row_token), _ptr(offsets),
+                                    _ptr(W1), _ptr(b1), _ptr(H), _ptr(ws), ws.numel(),
+                                    _stream(stream)))
 
 
 def ffn_down(cfg, H, offsets, W2, b2, yd, ws, stream=None):
@@ -290,7 +300,11 @@ def forward_stages(cfg, inputs: dict, out: dict, ws, alpha=0.01, stream=None, ev
     mark(1)
     dispatch(cfg, inputs["x"], out["topk_ids"], out, ws, s)
     mark(2)
-    ffn_up(cfg, out["xd"], out["offsets"], inputs["W1"], inputs["b1"], out["H"], ws, s)
+    if cfg.fuse_dispatch:
+        ffn_up_gather(cfg, inputs["x"], out["row_token"], out["offsets"], inputs["W1"],
+                      inputs["b1"], out["H"], ws, s)
+    else:
+        ffn_up(cfg, out["xd"], out["offsets"], inputs["W1"], inputs["b1"], out["H"], ws, s)
     mark(3)
     ffn_down(cfg, out["H"], out["offsets"], inputs["W2"], inputs["b2"], out["yd"], ws, s)
     mark(4)

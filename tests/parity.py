@@ -67,13 +67,15 @@ def assert_float(got, ref, dtype, what=""):
 
 
 def run_gpu(wl, inp=None, expert_bias=False, alpha=1.0, stages=False, health=False,
-            reroute=False):
+            reroute=False, fuse_dispatch=False):
     """Run the layer through the C ABI; return (cfg, inputs, outputs, ws).
     An ``inp["sel_bias"]`` routes with the selection-only bias; ``health``
-    also asks for the routing-health indicators."""
+    also asks for the routing-health indicators; ``fuse_dispatch`` runs the
+    first GEMM on gathered token rows (no xd)."""
     if inp is None:
         inp = inputs.make_inputs(wl, "cuda", expert_bias=expert_bias)
-    cfg = moe.config_from_workload(wl, write_logits=True, reroute=reroute)
+    cfg = moe.config_from_workload(wl, write_logits=True, reroute=reroute,
+                                   fuse_dispatch=fuse_dispatch)
     ws = moe.workspace(cfg)
     out = moe.allocate(cfg, health=health)
     if stages:
@@ -170,8 +172,11 @@ def check_forward(wl, inp, out, alpha=1.0, full=False, max_rows_check=None, n_to
         tr = fl["slot_row"][toks].reshape(-1)
         rows = np.union1d(rows, tr[tr >= 0]).astype(np.int32)
     ridx = torch.as_tensor(rows, device="cuda", dtype=torch.long)
-    xd_rows = h(out["xd"].index_select(0, ridx)) if len(rows) else x[:0]
-    np.testing.assert_array_equal(xd_rows, x[fl["row_token"][rows]], "xd")
+    if out.get("xd") is not None:
+        xd_rows = h(out["xd"].index_select(0, ridx)) if len(rows) else x[:0]
+        np.testing.assert_array_equal(xd_rows, x[fl["row_token"][rows]], "xd")
+    else:  # fused dispatch: the first GEMM read the token rows themselves
+        xd_rows = x[fl["row_token"][rows]]
 
     # 5. expert FFN on those rows
     yd_ref = oracle_yd(wl, inp, xd_rows, rows, fl["offsets"]) if len(rows) else None

@@ -148,3 +148,23 @@ def test_new_entry_points_reject_null_arguments(lib):
 
 def test_selftest_rejects_bad_arguments(lib):
     assert lib.moe_selftest_wait_timeout(None, 0, 10**7, None) == moe.MOE_ERR_INVALID_ARG
+
+
+def test_fuse_dispatch_flag_and_gather_scope(lib):
+    # fuse_dispatch must be 0 or 1.  The gathering first GEMM exists for bf16
+    # layers on the regular tensor-core GEMM only: fp32 layers and layers with
+    # at most 64 rows per expert get MOE_ERR_UNSUPPORTED before any launch
+    # (the placeholder pointers below are never dereferenced).
+    bad = cfg_for(64, 64, 64, 8, 2, 1.0)
+    bad.fuse_dispatch = 2
+    n = ctypes.c_size_t(0)
+    assert lib.moe_workspace_size(ctypes.byref(bad), ctypes.byref(n)) == moe.MOE_ERR_INVALID_ARG
+    ok = cfg_for(4096, 1024, 4096, 8, 2, 1.25, fuse_dispatch=True)
+    assert lib.moe_ffn_up_gather(ctypes.byref(ok), None, None, None, None, None, None, None, 0,
+                                 None) == moe.MOE_ERR_INVALID_ARG
+    p = ctypes.c_void_p(1 << 20)
+    f32 = cfg_for(4096, 1024, 4096, 8, 2, 1.25, dtype="f32", fuse_dispatch=True)
+    dec = cfg_for(8, 2048, 1408, 64, 6, 1.0, fuse_dispatch=True)  # min(C, T·k) = 1
+    for cfg in (f32, dec):
+        assert lib.moe_ffn_up_gather(ctypes.byref(cfg), p, p, p, p, p, p, p, 1 << 30,
+                                     None) == moe.MOE_ERR_UNSUPPORTED
