@@ -72,8 +72,11 @@ extern "C" moe_status_t moe_dispatch_noalloc(const moe_config_t* cfg, const void
   size_t ws_bytes = 0;
   moe_status_t s = moe_workspace_size(cfg, &ws_bytes);
   if (s != MOE_OK) return s;
-  if (!x || !topk_ids || !counts || !kept || !offsets || !slot_row || !row_token || !xd)
+  if (!x || !topk_ids || !counts || !kept || !offsets || !slot_row || !row_token ||
+      (!xd && !cfg->fuse_dispatch))
     return report_error(MOE_ERR_INVALID_ARG, "moe_dispatch_noalloc: NULL tensor");
+  // With fuse_dispatch no row is copied (the first GEMM gathers the rows).
+  if (cfg->fuse_dispatch) xd = nullptr;
   if (cfg->reroute)
     return report_error(MOE_ERR_UNSUPPORTED,
                         "moe_dispatch_noalloc: reroute needs the workspace of moe_dispatch");

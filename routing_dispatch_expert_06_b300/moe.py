@@ -230,7 +230,7 @@ def dispatch_noalloc(cfg, x, topk_ids, out, status=None, stream=None):
     _check(load().moe_dispatch_noalloc(ctypes.byref(cfg), _ptr(x), _ptr(topk_ids),
                                        _ptr(out["counts"]), _ptr(out["kept"]),
                                        _ptr(out["offsets"]), _ptr(out["slot_row"]),
-                                       _ptr(out["row_token"]), _ptr(out["xd"]), _ptr(status),
+                                       _ptr(out["row_token"]), _ptr(out.get("xd")), _ptr(status),
                                        _stream(stream)))
 
 
