@@ -10,6 +10,8 @@
 #include <cstring>
 #include <string>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -26,6 +28,9 @@ static moe_status_t fail(moe_status_t code, const std::string& msg) {
 }
 
 moe_status_t report_error(moe_status_t code, const char* msg) { return fail(code, msg); }
+
+StageRange::StageRange(const char* name) { nvtxRangePushA(name); }
+StageRange::~StageRange() { nvtxRangePop(); }
 
 namespace {
 constexpr int kMaxDev = 64;
@@ -265,6 +270,7 @@ static moe_status_t route_impl(const moe_config_t* cfg, const void* x, const voi
                                int32_t* topk_ids, float* topk_w, float* psum, void* ws,
                                size_t ws_bytes, unsigned long long** psum_fixed_out,
                                void* stream) {
+  const StageRange range("moe_route");
   moe_status_t s = check_cfg(cfg);
   if (s != MOE_OK) return s;
   if (!x || !Wr || !br || !topk_ids || !topk_w || !psum)
@@ -348,6 +354,7 @@ moe_status_t moe_route_sel(const moe_config_t* cfg, const void* x, const void* W
 
 moe_status_t moe_routing_health(const moe_config_t* cfg, const int32_t* counts,
                                 const int32_t* kept, float* health, void* stream) {
+  const StageRange range("moe_routing_health");
   moe_status_t s = check_cfg(cfg);
   if (s != MOE_OK) return s;
   if (!counts || !kept || !health)
@@ -366,6 +373,7 @@ static moe_status_t dispatch_impl(const moe_config_t* cfg, const void* x,
                                   int32_t* offsets, int32_t* slot_row, int32_t* row_token,
                                   void* xd, void* ws, size_t ws_bytes, const AuxArgs* aux,
                                   void* stream) {
+  const StageRange range("moe_dispatch");
   moe_status_t s = check_cfg(cfg);
   if (s != MOE_OK) return s;
   if (!x || !topk_ids || !counts || !kept || !offsets || !slot_row || !row_token ||
@@ -399,6 +407,7 @@ moe_status_t moe_dispatch(const moe_config_t* cfg, const void* x, const int32_t*
 moe_status_t moe_ffn_up(const moe_config_t* cfg, const void* xd, const int32_t* offsets,
                         const void* W1, const float* b1, void* H, void* ws, size_t ws_bytes,
                         void* stream) {
+  const StageRange range("moe_ffn_up");
   moe_status_t s = check_cfg(cfg);
   if (s != MOE_OK) return s;
   if (!xd || !offsets || !W1 || !b1 || !H)
@@ -425,6 +434,7 @@ moe_status_t moe_ffn_up(const moe_config_t* cfg, const void* xd, const int32_t* 
 moe_status_t moe_ffn_up_gather(const moe_config_t* cfg, const void* x, const int32_t* row_token,
                                const int32_t* offsets, const void* W1, const float* b1, void* H,
                                void* ws, size_t ws_bytes, void* stream) {
+  const StageRange range("moe_ffn_up_gather");
   moe_status_t s = check_cfg(cfg);
   if (s != MOE_OK) return s;
   if (!x || !row_token || !offsets || !W1 || !b1 || !H)
@@ -446,6 +456,7 @@ moe_status_t moe_ffn_up_gather(const moe_config_t* cfg, const void* x, const int
 moe_status_t moe_ffn_down(const moe_config_t* cfg, const void* H, const int32_t* offsets,
                           const void* W2, const float* b2, void* yd, void* ws, size_t ws_bytes,
                           void* stream) {
+  const StageRange range("moe_ffn_down");
   moe_status_t s = check_cfg(cfg);
   if (s != MOE_OK) return s;
   if (!H || !offsets || !W2 || !b2 || !yd)
@@ -472,6 +483,7 @@ moe_status_t moe_ffn_down(const moe_config_t* cfg, const void* H, const int32_t*
 moe_status_t moe_expert_ffn(const moe_config_t* cfg, const void* xd, const int32_t* offsets,
                             const void* W1, const float* b1, const void* W2, const float* b2,
                             void* H, void* yd, void* ws, size_t ws_bytes, void* stream) {
+  const StageRange range("moe_expert_ffn");
   moe_status_t s = moe_ffn_up(cfg, xd, offsets, W1, b1, H, ws, ws_bytes, stream);
   if (s != MOE_OK) return s;
   return moe_ffn_down(cfg, H, offsets, W2, b2, yd, ws, ws_bytes, stream);
@@ -479,6 +491,7 @@ moe_status_t moe_expert_ffn(const moe_config_t* cfg, const void* xd, const int32
 
 moe_status_t moe_combine(const moe_config_t* cfg, const void* yd, const int32_t* slot_row,
                          const float* topk_w, void* y, void* stream) {
+  const StageRange range("moe_combine");
   moe_status_t s = check_cfg(cfg);
   if (s != MOE_OK) return s;
   if (!yd || !slot_row || !topk_w || !y)
@@ -492,6 +505,7 @@ moe_status_t moe_combine(const moe_config_t* cfg, const void* yd, const int32_t*
 
 moe_status_t moe_aux_stats(const moe_config_t* cfg, const int32_t* counts, const float* psum,
                            float alpha, float* f, float* pbar, float* l_aux, void* stream) {
+  const StageRange range("moe_aux_stats");
   moe_status_t s = check_cfg(cfg);
   if (s != MOE_OK) return s;
   if (!counts || !psum || !f || !pbar || !l_aux)
@@ -503,6 +517,7 @@ moe_status_t moe_aux_stats(const moe_config_t* cfg, const int32_t* counts, const
 
 moe_status_t moe_forward(const moe_config_t* cfg, const moe_tensors_t* t, float alpha, void* ws,
                          size_t ws_bytes, void* stream) {
+  const StageRange range("moe_forward");
   if (!t) return fail(MOE_ERR_INVALID_ARG, "moe_forward: tensors is NULL");
   if (!t->f || !t->pbar || !t->l_aux)
     return fail(MOE_ERR_INVALID_ARG, "moe_aux_stats: NULL tensor");

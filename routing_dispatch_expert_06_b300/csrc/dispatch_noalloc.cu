@@ -67,6 +67,7 @@ extern "C" moe_status_t moe_dispatch_noalloc(const moe_config_t* cfg, const void
                                              int32_t* kept, int32_t* offsets, int32_t* slot_row,
                                              int32_t* row_token, void* xd, int32_t* status,
                                              void* stream) {
+  const StageRange range("moe_dispatch_noalloc");
   // Argument checks shared with the other entry points (they set the message
   // returned by moe_last_error).
   size_t ws_bytes = 0;

@@ -15,6 +15,17 @@ void count_launch();
 // Records msg as the calling thread's moe_last_error() text; returns code.
 moe_status_t report_error(moe_status_t code, const char* msg);
 
+// An NVTX range named after a library call, open for the call's lifetime, so
+// a profiler's timeline shows each stage (and moe_forward's stages nested in
+// it) by name.  Opened before the argument checks.  Without a tool attached
+// each push and pop is one test of a null function pointer.
+struct StageRange {
+  explicit StageRange(const char* name);
+  ~StageRange();
+  StageRange(const StageRange&) = delete;
+  StageRange& operator=(const StageRange&) = delete;
+};
+
 // Host-side launch helpers that query the driver once per device (or per
 // kernel) and then answer from a cache, so a stage call costs little more
 // than its launches.
