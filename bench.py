@@ -154,6 +154,48 @@ def algorithmic(wl, n_kept: int, t_kept: int, fused: bool = False):
     )
 
 
+def gemm_tile_rows(kept, E: int, pair: bool = True, tail_split_min_experts: int = 128) -> int:
+    """Rows the regular tensor-core grouped GEMM computes for experts holding
+    ``kept`` rows: tiles never straddle two experts, so each expert's rows are
+    rounded up to whole tiles (256 rows for a CTA pair, 128 for one CTA; with
+    E >= 128 an expert's last 1..128 rows go to one 128-row tile)."""
+    total = 0
+    for r in (int(v) for v in kept):
+        if r <= 0:
+            continue
+        if not pair:
+            total += -(-r // 128) * 128
+        elif E >= tail_split_min_experts:
+            whole, rem = divmod(r, 256)
+            total += whole * 256 + (256 if rem > 128 else 128 if rem > 0 else 0)
+        else:
+            total += -(-r // 256) * 256
+    return total
+
+
+def routing_stats(counts, kept, slot_row, T: int, k: int, E: int, regular_gemm: bool):
+    """Load and drop figures of one forward pass (the monitoring list of
+    [MoE 模型原理 §4.4] and the evaluation list of §13): slots dropped by
+    the capacity, tokens with no kept slot, the hottest expert's load over the
+    mean, the dispatch buffer's padding (none: it is ragged) and the regular
+    GEMM's tile waste (rows computed in partial tiles over kept rows; None
+    for the swapped decode GEMM and the CUDA-core GEMM, tiled otherwise)."""
+    counts = [int(v) for v in counts]
+    kept = [int(v) for v in kept]
+    n_kept = sum(kept)
+    t_kept = sum(1 for row in slot_row if any(int(v) >= 0 for v in row))
+    tile_rows = gemm_tile_rows(kept, E) if regular_gemm else None
+    return dict(
+        dropped_slots=T * k - n_kept,
+        dropped_slot_share=(T * k - n_kept) / (T * k),
+        overflow_tokens=T - t_kept,
+        load_max_over_mean=max(counts) * E / (T * k),
+        padding_rows=0,
+        gemm_tile_rows=tile_rows,
+        tile_waste=(tile_rows / n_kept - 1.0) if (tile_rows is not None and n_kept) else None,
+    )
+
+
 # ------------------------------------------------------------ CPU oracle ----
 
 def host_inputs(wl, inp=None, max_tokens=8192):
@@ -403,6 +445,10 @@ def main():
     slot = out["slot_row"].cpu()
     t_kept = int((slot >= 0).any(dim=1).sum())
     alg = algorithmic(wl, n_kept, t_kept, fused=args.fuse_dispatch)
+    C = moe.capacity(cfg)
+    regular_gemm = wl.dtype == "bf16" and min(C, wl.T * wl.k) > 64
+    routing = routing_stats(out["counts"].cpu().tolist(), out["kept"].cpu().tolist(),
+                            slot.tolist(), wl.T, wl.k, wl.E, regular_gemm)
     peaks = load_peaks()
     mean = {k: v / K for k, v in stage_ms.items()}
     ffn_ms = mean["ffn_up"] + mean["ffn_down"]
@@ -481,6 +527,7 @@ def main():
         hbm_peak_gbs=peaks["hbm"],
         kept_rows=n_kept,
         experts_touched=touched,
+        routing=routing,
         # With few rows per expert the grouped FFN is bound by reading the
         # touched experts' W1 and W2: their bytes over the FFN time.
         ffn_weight_gbs=touched * 2 * wl.d * wl.d_ff * b / (ffn_ms * 1e-3) / 1e9,
