@@ -168,3 +168,22 @@ def test_fuse_dispatch_flag_and_gather_scope(lib):
     for cfg in (f32, dec):
         assert lib.moe_ffn_up_gather(ctypes.byref(cfg), p, p, p, p, p, p, p, 1 << 30,
                                      None) == moe.MOE_ERR_UNSUPPORTED
+
+
+def test_fuse_dispatch_host_checks(lib):
+    # moe_dispatch takes a NULL xd only with fuse_dispatch: without it the call
+    # is refused as a NULL tensor; with it the call gets past the tensor checks
+    # and stops at the (too small) workspace, before any launch.  moe_forward
+    # refuses fuse_dispatch on an fp32 layer before any launch.
+    p = ctypes.c_void_p(1 << 20)
+    cfg = cfg_for(4096, 1024, 4096, 8, 2, 1.25)
+    args = [p] * 7 + [None, p, 16]  # x, ids, counts, kept, offsets, slot_row, row_token, xd, ws
+    assert lib.moe_dispatch(ctypes.byref(cfg), *args, None) == moe.MOE_ERR_INVALID_ARG
+    fused = cfg_for(4096, 1024, 4096, 8, 2, 1.25, fuse_dispatch=True)
+    assert lib.moe_dispatch(ctypes.byref(fused), *args, None) == moe.MOE_ERR_WORKSPACE
+    f32 = cfg_for(512, 128, 512, 8, 2, 1.0, dtype="f32", fuse_dispatch=True)
+    t = moe.Tensors()
+    for name in ("f", "pbar", "l_aux"):
+        setattr(t, name, 1 << 20)
+    assert lib.moe_forward(ctypes.byref(f32), ctypes.byref(t), ctypes.c_float(1.0), p, 1 << 30,
+                           None) == moe.MOE_ERR_UNSUPPORTED
