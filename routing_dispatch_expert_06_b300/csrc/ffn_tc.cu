@@ -33,7 +33,9 @@
 // pair launch before it completes.
 //
 //   warp 0     TMA producer: 128×64 A tile + (BN or BN/2)×64 B tile per stage,
-//              128-byte swizzle, a ring of as many stages as fit
+//              128-byte swizzle, a ring of as many stages as fit (GATHER:
+//              the whole warp gathers the A rows, four per lane, by TMA
+//              gather4 from the token matrix)
 //   warp 1     TMEM allocator and (in the even CTA of a pair) MMA issuer:
 //              tcgen05.mma K=16, fp32 accumulators in tensor memory, two
 //              accumulator buffers so the epilogue of one tile overlaps the
