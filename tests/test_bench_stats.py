@@ -38,3 +38,22 @@ def test_routing_stats():
     assert st["gemm_tile_rows"] == 512 and st["tile_waste"] == pytest.approx(512 / 6 - 1)
     st = bench.routing_stats(counts, kept, slot_row, T=4, k=2, E=2, regular_gemm=False)
     assert st["gemm_tile_rows"] is None and st["tile_waste"] is None
+
+
+def test_kernel_traffic_only_for_the_captured_source(tmp_path, monkeypatch):
+    # The ncu figure is reported only while the summary's recorded source hash
+    # matches the kernel source; after any edit it is null.
+    import hashlib
+
+    src = tmp_path / "kernel.cu"
+    src.write_text("// kernel v1\n")
+    sha = hashlib.sha256(src.read_bytes()).hexdigest()
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    (prof / "ffn_up_wl.md").write_text(
+        f"kernel_source_sha256: {sha}\ntraffic_bytes_per_launch: 117502464\n")
+    monkeypatch.setattr(bench, "PROFILES", str(prof))
+    assert bench.kernel_traffic("ffn_up", "wl", str(src)) == 117502464.0
+    assert bench.kernel_traffic("ffn_down", "wl", str(src)) is None  # no summary
+    src.write_text("// kernel v2\n")
+    assert bench.kernel_traffic("ffn_up", "wl", str(src)) is None
