@@ -1,10 +1,15 @@
 """Pins for the oracle's overflow reroute ([MoE 模型原理 §4.3], second policy:
 an overflowing slot goes to the next expert of the token's candidate list).
 
-The expected values come from the §4.2 worked example worked by hand, from
-the no-overflow special case (identical to the plain fill), from a stable
-argsort (the candidate ranks), and from invariants that any correct reroute
-must satisfy on random tiny batches.
+The expected values come from the §4.2 worked example worked by hand (k = 1),
+from two cases with k = 2 and k = 3 worked by hand from the reading of §4.3
+(tests/golden/wrblog_s4_3_reroute_k*.json: the m-th overflowing slot of a
+token goes to its candidate of rank k + m; offers are served first come in
+(token, rank) order into the room each expert has left), from the
+no-overflow special case (identical to the plain fill), from a stable argsort
+(the candidate ranks), and from a second formulation of the reroute written
+independently of the oracle's loop (a sorted queue of offers) on random tiny
+batches.
 """
 
 import json
@@ -122,3 +127,102 @@ def test_reroute_invariants_on_tiny_batches(seed):
     assert len(np.unique(kr)) == len(kr) == off[E]
     tok = np.repeat(np.arange(T), k).reshape(T, k)
     np.testing.assert_array_equal(fl["row_token"][kr], tok[rows >= 0])
+
+
+# ---- k > 1: hand-worked cases and an independent queue formulation ----
+
+def _golden_case(name):
+    g = golden(name)
+    return (g, np.array(g["topk_ids"], np.int32), np.array(g["cand"], np.int32))
+
+
+FIELDS = ["counts", "kept", "offsets", "slot_row", "row_token", "slot_expert"]
+
+
+@pytest.mark.parametrize("name", ["wrblog_s4_3_reroute_k2.json", "wrblog_s4_3_reroute_k3.json"])
+def test_reroute_hand_worked_k_above_one(name):
+    g, ids, cand = _golden_case(name)
+    fl = oracle.fill_reroute(ids, cand, g["E"], g["C"])
+    for key in FIELDS:
+        np.testing.assert_array_equal(fl[key], np.array(g[key]), key)
+
+
+def queue_reroute(ids, cand, E, C, rank_major=False, offer_by_rank=False):
+    """The reroute restated as a queue of offers (written for this test, not
+    from the oracle's loop).  First-fill positions come from a stable sort of
+    the slots by expert; each token's overflowing slots are numbered m = 0, 1,
+    ... in rank order and offer themselves to cand[t, m]; the offers, sorted
+    by (token, rank), take the room C - kept0 left on their expert, and
+    served rows follow the expert's own rows.  ``rank_major`` (serve by
+    (rank, token)) and ``offer_by_rank`` (offer slot r to cand[t, r]) are
+    the two plausible misreadings the hand-worked cases must reject."""
+    T, k = ids.shape
+    flat = ids.reshape(-1)
+    order = np.argsort(flat, kind="stable")
+    counts = np.bincount(flat, minlength=E)
+    first = np.concatenate([[0], np.cumsum(counts)])[:-1]
+    pos0 = np.empty(T * k, np.int64)
+    pos0[order] = np.arange(T * k) - first[flat[order]]
+    pos0 = pos0.reshape(T, k)
+    over = pos0 >= C
+    m = np.cumsum(over, axis=1) - 1
+    kept0 = np.minimum(counts, C)
+    room = C - kept0
+    tt, rr = np.nonzero(over)
+    mm = rr if offer_by_rank else m[tt, rr]
+    target = np.where(mm < k, cand[tt, np.minimum(mm, k - 1)], -1)
+    seq = np.lexsort((tt, rr)) if rank_major else np.lexsort((rr, tt))
+    served = np.zeros(E, np.int64)
+    dest = np.where(over, -1, ids).astype(np.int64)
+    pos1 = np.full((T, k), -1, np.int64)
+    for i in seq:
+        e2 = target[i]
+        if e2 >= 0 and served[e2] < room[e2]:
+            dest[tt[i], rr[i]] = e2
+            pos1[tt[i], rr[i]] = served[e2]
+            served[e2] += 1
+    kept = kept0 + served
+    offsets = np.concatenate([[0], np.cumsum(kept)])
+    slot_row = np.full((T, k), -1, np.int64)
+    row_token = np.full(int(offsets[E]), -1, np.int64)
+    for t in range(T):
+        for r in range(k):
+            e = dest[t, r]
+            if e < 0:
+                continue
+            row = offsets[e] + (pos0[t, r] if not over[t, r] else kept0[e] + pos1[t, r])
+            slot_row[t, r] = row
+            row_token[row] = t
+    return dict(counts=counts, kept=kept, offsets=offsets, slot_row=slot_row,
+                row_token=row_token, slot_expert=dest)
+
+
+@pytest.mark.parametrize("name", ["wrblog_s4_3_reroute_k2.json", "wrblog_s4_3_reroute_k3.json"])
+def test_queue_formulation_reproduces_hand_worked_cases_and_rejects_misreadings(name):
+    g, ids, cand = _golden_case(name)
+    q = queue_reroute(ids, cand, g["E"], g["C"])
+    for key in FIELDS:
+        np.testing.assert_array_equal(q[key], np.array(g[key]), key)
+    # Serving offers rank by rank, or offering slot r to the rank-(k + r)
+    # candidate, gives a different buffer on these cases.
+    for bad in (dict(rank_major=True), dict(offer_by_rank=True)):
+        if name.endswith("k3.json") and "offer_by_rank" in bad:
+            continue  # the k = 3 case has no overflow that isolates this slip
+        wrong = queue_reroute(ids, cand, g["E"], g["C"], **bad)
+        assert not np.array_equal(wrong["slot_row"], np.array(g["slot_row"])), bad
+
+
+@pytest.mark.parametrize("seed", range(60))
+def test_reroute_matches_queue_formulation_on_tiny_batches(seed):
+    rng = np.random.default_rng(500 + seed)
+    T = int(rng.integers(1, 16))
+    E = int(rng.integers(2, 7))
+    k = int(rng.integers(1, min(4, E) + 1))
+    C = int(rng.integers(0, 5))
+    s = rng.normal(size=(T, E)).astype(np.float32)
+    s[:, : max(1, E // 3)] += 1.5  # hot experts overflow
+    ids, _, _, _, cand = oracle.select(s, k, True, want_cand=True)
+    fl = oracle.fill_reroute(ids, cand, E, C)
+    q = queue_reroute(ids, cand, E, C)
+    for key in FIELDS:
+        np.testing.assert_array_equal(fl[key], q[key], key)
