@@ -18,8 +18,10 @@ torchrun every rank runs an independent replica on its own batch and
 ``value`` is the tokens of all ranks / the slowest rank's time.
 
 ``--impl reference`` times the CPU oracle (the plain C++ implementation the
-tests compare against) on the host cores, on a bounded sample of the same
-workload, and prints the same JSON line with "impl": "reference".
+tests compare against) on the host cores, W untimed and K timed forward passes
+over a bounded sample of the same workload (its first S tokens as one layer
+call, S from cpu_sample_tokens), and prints the same JSON line with
+"impl": "reference".  The GPU arm's cpu_baseline times the same sample.
 """
 
 from __future__ import annotations
@@ -198,44 +200,69 @@ def routing_stats(counts, kept, slot_row, T: int, k: int, E: int, regular_gemm: 
 
 # ------------------------------------------------------------ CPU oracle ----
 
-def host_inputs(wl, inp=None, max_tokens=8192):
-    """Host copies (numpy; bf16 as uint16 bits) of a workload's tensors: the
-    given device tensors, or a fresh CPU draw with the same recipe."""
-    if inp is None:
-        inp = inputs.make_inputs(wl.replace(T=min(wl.T, max_tokens)), "cpu")
-    out = {k: inputs.to_numpy(v) for k, v in inp.items() if k != "x"}
-    out["x"] = inputs.to_numpy(inp["x"][:max_tokens])
+def cpu_model() -> str:
+    """The host CPU's model name (from /proc/cpuinfo), or '' if unknown."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return ""
+
+
+def cpu_sample_tokens(wl, flop_budget: float = 1e11) -> int:
+    """Tokens S of the CPU oracle's timed sample: the largest power of two,
+    at most T, whose forward pass costs at most ``flop_budget`` of the
+    method's arithmetic (router 2·d·E plus expert FFN k·4·d·d_ff per token),
+    i.e. a few seconds of the oracle on a host's cores."""
+    per_token = 2 * wl.d * wl.E + wl.k * 4 * wl.d * wl.d_ff
+    S = 1
+    while S * 2 <= wl.T and S * 2 * per_token <= flop_budget:
+        S *= 2
+    return S
+
+
+def sample_text(wl, S: int) -> str:
+    return (f"the first {S} of the {wl.T} tokens of the {wl.name} batch (same seeded x and "
+            f"weights as the GPU run), routed and computed as one layer call of the C++ "
+            f"oracle (capacity over the {S} tokens)")
+
+
+def host_inputs(wl, inp, S: int):
+    """Host copies (numpy; bf16 as uint16 bits) of the workload's tensors,
+    with x cut to its first S tokens."""
+    out = {k: inputs.to_numpy(v) for k, v in inp.items() if k not in ("x", "sel_bias")}
+    out["x"] = inputs.to_numpy(inp["x"][:S])
     return out
 
 
-def cpu_oracle_sample(wl, host, budget_s: float = 15.0, seed_tokens: int = 8):
-    """Time the oracle's forward on a batch of S tokens of this workload (same
-    weights and input distribution; capacity scope = the S tokens).  S is
-    grown from a small probe until one run takes about budget_s / 4, so the
-    whole measurement stays within about budget_s.  Returns tokens/s."""
-    import oracle  # test infrastructure: only this CPU-baseline leg runs it
+def oracle_forward_seconds(wl, host) -> float:
+    """Wall time of one oracle forward pass over host["x"] (its own capacity
+    group)."""
+    import oracle  # test infrastructure: only the CPU-baseline legs run it
 
     act = oracle.ACT_RELU if wl.act == "relu" else oracle.ACT_GELU_TANH
+    t0 = time.perf_counter()
+    oracle.forward(host["x"], host["Wr"], host["br"], host["W1"], host["b1"], host["W2"],
+                   host["b2"], k=wl.k, capacity_factor=wl.capacity_factor,
+                   renormalize=wl.renormalize, act=act)
+    return time.perf_counter() - t0
 
-    def run(S):
-        t0 = time.perf_counter()
-        oracle.forward(host["x"][:S], host["Wr"], host["br"], host["W1"], host["b1"], host["W2"],
-                       host["b2"], k=wl.k, capacity_factor=wl.capacity_factor,
-                       renormalize=wl.renormalize, act=act)
-        return time.perf_counter() - t0
 
-    S = min(seed_tokens, host["x"].shape[0])
-    dt = run(S)
-    total = dt
-    cap = host["x"].shape[0]
-    while dt < budget_s / 4 and S < cap and total < budget_s:
-        S = min(cap, max(S * 2, int(S * (budget_s / 4) / max(dt, 1e-3))))
-        dt = run(S)
-        total += dt
+def cpu_oracle_sample(wl, inp):
+    """The oracle timed on the host cores on the bounded sample of this
+    workload (one untimed run, then one timed run).  Returns the bench line's
+    cpu_baseline object (tokens/s of the sample)."""
+    import oracle
+
+    S = cpu_sample_tokens(wl)
+    host = host_inputs(wl, inp, S)
+    oracle_forward_seconds(wl, host)
+    dt = oracle_forward_seconds(wl, host)
     return dict(value=S / dt, unit="tokens/s", cores=oracle.num_threads(), kind="oracle",
-                sample=f"one forward of the C++ oracle over a batch of {S} tokens of the "
-                       f"{wl.name} layer (same weights and x distribution; capacity over the "
-                       f"{S} tokens); {dt:.2f} s")
+                cpu_model=cpu_model(), sample=f"{sample_text(wl, S)}; {dt:.2f} s")
 
 
 def max_over_ranks(value, dist=None, device=None):
@@ -260,26 +287,45 @@ def replica_seed(seed, rank):
     return seed * 1000 + rank
 
 
+def bench_config(wl, args, world):
+    """The line's config object (the same on both arms)."""
+    return dict(workload=wl.name, T=wl.T, d=wl.d, d_ff=wl.d_ff, E=wl.E, k=wl.k,
+                capacity_factor=wl.capacity_factor, renormalize=wl.renormalize, act=wl.act,
+                parallelism=f"replicas{world}" if world > 1 else "single",
+                sel_bias=bool(args.sel_bias), health=bool(args.health),
+                reroute=bool(args.reroute), fuse_dispatch=bool(args.fuse_dispatch),
+                l2="flushed between steps (512 MiB write, then 512 MiB read)")
+
+
 def run_reference(args, wl, rank, world):
+    """The oracle arm: W untimed and K timed forward passes of the C++ oracle
+    on the host cores, each over the same bounded sample the GPU arm's
+    cpu_baseline uses (cpu_sample_tokens), inputs drawn by the same seeded
+    recipe (on the GPU when there is one, so the bytes are the GPU arm's).
+    ms_per_step is the measured mean seconds of one such forward."""
     if rank != 0:
         return 0
     import oracle
 
-    host = host_inputs(wl)
-    vals = []
-    info = None
-    for _ in range(args.steps):  # the oracle keeps no state, so warm-up steps are skipped
-        info = cpu_oracle_sample(wl, host, budget_s=max(4.0, 60.0 / max(args.steps, 1)))
-        vals.append(info["value"])
-    v = statistics.median(vals)
-    line = dict(metric=METRIC, value=v, unit="tokens/s", n_gpus=world, steps=args.steps,
-                warmup=args.warmup, ms_per_step=1e3 * wl.T / v, higher_is_better=True,
-                scaling="weak", vs_baseline=None, dtype="f64", data="synthetic",
-                config=dict(workload=wl.name, T=wl.T, d=wl.d, d_ff=wl.d_ff, E=wl.E, k=wl.k,
-                            capacity_factor=wl.capacity_factor, l2="n/a (CPU)"),
+    S = cpu_sample_tokens(wl)
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    inp = inputs.make_inputs(wl, dev)
+    host = host_inputs(wl, inp, S)
+    del inp
+    for _ in range(args.warmup):
+        oracle_forward_seconds(wl, host)
+    times = [oracle_forward_seconds(wl, host) for _ in range(args.steps)]
+    total = sum(times)
+    v = S * len(times) / total
+    cfg = bench_config(wl, args, world)
+    cfg["l2"] = "n/a (CPU)"
+    line = dict(metric=METRIC, value=v, unit="tokens/s", n_gpus=world, steps=len(times),
+                warmup=args.warmup, ms_per_step=1e3 * total / len(times), higher_is_better=True,
+                scaling="weak", vs_baseline=None, dtype="f64", data="synthetic", config=cfg,
                 impl="reference",
                 cpu_baseline=dict(value=v, unit="tokens/s", cores=oracle.num_threads(),
-                                  kind="oracle", sample=info["sample"]),
+                                  kind="oracle", cpu_model=cpu_model(),
+                                  sample=f"{sample_text(wl, S)}; each step one forward of it"),
                 e2e=dict(value=v, unit="tokens/s", h2d_bytes_per_step=0, d2h_bytes_per_step=0))
     print(json.dumps(line), flush=True)
     return 0
@@ -494,22 +540,25 @@ def main():
     value = job_tokens_per_s(world, wl.T, K, max_ms)
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_oracle_sample(wl, host_inputs(wl, inp))
+        cpu = cpu_oracle_sample(wl, inp)
     b = 2 if wl.dtype == "bf16" else 4
+    hbm = peaks["hbm"]
+    stage_gbs = dict(route=alg["route_bytes"] / (mean["route"] * 1e-3) / 1e9,
+                     dispatch=alg["dispatch_bytes"] / (mean["dispatch"] * 1e-3) / 1e9,
+                     combine=alg["combine_bytes"] / (mean["combine"] * 1e-3) / 1e9)
+    ffn_tflops = alg["ffn_up_flops"] * 2 / (ffn_ms * 1e-3) / 1e12
     line = dict(
         metric=METRIC, value=value, unit="tokens/s", n_gpus=world, steps=K, warmup=args.warmup,
         ms_per_step=max_ms / K, higher_is_better=True, scaling="weak", vs_baseline=None,
         dtype="bf16" if wl.dtype == "bf16" else "f32", data="synthetic",
-        config=dict(workload=wl.name, T=wl.T, d=wl.d, d_ff=wl.d_ff, E=wl.E, k=wl.k,
-                    capacity_factor=wl.capacity_factor, renormalize=wl.renormalize,
-                    act=wl.act, parallelism=f"replicas{world}" if world > 1 else "single",
-                    sel_bias=bool(args.sel_bias), health=bool(args.health),
-                    reroute=bool(args.reroute), fuse_dispatch=bool(args.fuse_dispatch),
-                    l2="flushed between steps (512 MiB write, then 512 MiB read)"),
-        roofline=dict(bound="tensor", kernel=f"{dom_kernel} (tcgen05 grouped GEMM)",
+        config=bench_config(wl, args, world),
+        roofline=dict(bound="tensor", kernel=f"{dom_kernel} (tcgen05 grouped GEMM"
+                      + (", pair-body and tail launches" if wl.E >= 128 else "") + ")",
                       achieved=dom_tflops, peak=peaks["bf16"], unit="TFLOP/s",
                       frac=dom_tflops / peaks["bf16"], traffic=traffic,
-                      peak_source=f"{peaks['source']} bf16 burst"),
+                      peak_source=f"{peaks['source']} bf16 burst",
+                      peak_sustained=peaks["bf16_sustained"],
+                      frac_sustained=dom_tflops / peaks["bf16_sustained"]),
         cpu_baseline=cpu,
         e2e=dict(value=world * wl.T / (e2e_ms * 1e-3), unit="tokens/s",
                  h2d_bytes_per_step=wl.T * wl.d * b, d2h_bytes_per_step=wl.T * wl.d * b + 4),
@@ -519,12 +568,14 @@ def main():
                "one graph per stage; eager_ms_per_step = moe_forward launched from Python",
         eager_ms_per_step=eager_ms,
         stages_ms={k: round(v, 5) for k, v in mean.items()},
-        ffn_tflops=alg["ffn_up_flops"] * 2 / (ffn_ms * 1e-3) / 1e12,
-        ffn_tc_frac=alg["ffn_up_flops"] * 2 / (ffn_ms * 1e-3) / 1e12 / peaks["bf16"],
-        dispatch_gbs=alg["dispatch_bytes"] / (mean["dispatch"] * 1e-3) / 1e9,
-        combine_gbs=alg["combine_bytes"] / (mean["combine"] * 1e-3) / 1e9,
-        route_gbs=alg["route_bytes"] / (mean["route"] * 1e-3) / 1e9,
-        hbm_peak_gbs=peaks["hbm"],
+        ffn_tflops=ffn_tflops,
+        ffn_tc_frac=ffn_tflops / peaks["bf16"],
+        ffn_tc_frac_sustained=ffn_tflops / peaks["bf16_sustained"],
+        dispatch_gbs=stage_gbs["dispatch"],
+        combine_gbs=stage_gbs["combine"],
+        route_gbs=stage_gbs["route"],
+        hbm_peak_gbs=hbm,
+        hbm_frac={k: v / hbm for k, v in stage_gbs.items()},
         kept_rows=n_kept,
         experts_touched=touched,
         routing=routing,

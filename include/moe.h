@@ -158,7 +158,12 @@ moe_status_t moe_route(const moe_config_t* cfg, const void* x, const void* Wr, c
  * S_t); kept, offsets, slot_row and row_token are final; a rerouted slot keeps
  * its combine weight.
  * With cfg->fuse_dispatch no row is copied: xd may be NULL and is not
- * written (moe_ffn_up_gather reads the rows from x). */
+ * written (moe_ffn_up_gather reads the rows from x).
+ * topk_ids need not be distinct within a token: every (t, r) is its own
+ * slot, and slots of one token that name the same expert take consecutive
+ * positions in rank order.  An id outside [0, E) names no expert: that slot
+ * is not counted, its slot_row is -1, and the workspace status word receives
+ * MOE_ERR_INVALID_ARG; every other slot is dispatched as if it were absent. */
 moe_status_t moe_dispatch(const moe_config_t* cfg, const void* x, const int32_t* topk_ids,
                           int32_t* counts, int32_t* kept, int32_t* offsets, int32_t* slot_row,
                           int32_t* row_token, void* xd, void* ws, size_t ws_bytes, void* stream);

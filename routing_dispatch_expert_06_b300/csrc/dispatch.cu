@@ -258,15 +258,24 @@ __device__ __forceinline__ void assign_body(int64_t T, int E, int k, int64_t C,
   }
   __syncthreads();
   // Walk the warp's tokens in order; lane r handles rank r of the token.
+  // Ranks of one token that name the same expert (possible only with ids a
+  // caller passes in) are separate slots: they take consecutive positions in
+  // rank order, the lanes of a group found with match.any.
   int32_t* my = wbase + warp * E;
   for (int j = 0; j < 32; ++j) {
     const int64_t t = chunk0 + warp * 32 + j;
     if (t >= T) break;
+    const int e = lane < k ? s_ids[(warp * 32 + j) * k + lane] : -1;
+    const bool valid = e >= 0 && e < E;
+    const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : E + lane);
+    const int32_t before = __popc(peers & ((1u << lane) - 1u));
+    const int32_t base = valid ? my[e] : 0;
+    __syncwarp();
+    if (valid && before == 0) my[e] = base + __popc(peers);
     if (lane < k) {
-      const int e = s_ids[(warp * 32 + j) * k + lane];
       int32_t row = -1;
-      if (e >= 0 && e < E) {
-        const int32_t pos = my[e]++;
+      if (valid) {
+        const int32_t pos = base + before;
         if (positions_only) {
           row = pos < off[e] ? pos : -1;  // off[e] holds the capacity here
         } else if (pos < C) {

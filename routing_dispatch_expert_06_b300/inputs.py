@@ -78,8 +78,9 @@ WORKLOADS = {
     ]
 }
 
-# Workload timed by default in the benchmark.
-DEFAULT_BENCH = "bf16_t4096_d1024_e8_top2"
+# Workload timed by default in the benchmark: the largest layer (T = 32768,
+# d = 7168, d_ff = 2048, E = 256, top-8).
+DEFAULT_BENCH = "bf16_t32768_d7168_e256_top8"
 
 
 def _router_bias(kind: str, E: int, gen: torch.Generator, device) -> torch.Tensor:

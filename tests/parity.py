@@ -87,19 +87,41 @@ def run_gpu(wl, inp=None, expert_bias=False, alpha=1.0, stages=False, health=Fal
     return cfg, inp, out, ws
 
 
-def sample_rows(offsets, E, per_expert=6, max_experts=None, seed=0):
+def tail_class(n_rows):
+    """Which tile shape covers an expert's last rows in the pair-body/tail
+    split of the tensor-core GEMM: 'whole' (rows % 256 == 0, only 256-row
+    pair tiles), 'tail' (1..128 rows left: a one-CTA 128-row tile) or
+    'pair_part' (129..255 left: a partly filled pair tile)."""
+    m = int(n_rows) % 256
+    return "whole" if m == 0 else ("tail" if m <= 128 else "pair_part")
+
+
+def sample_rows(offsets, E, per_expert=6, max_experts=None, seed=0, per_class=None):
     """Rows of the dispatch buffer to check: each chosen expert's first and
-    last rows, the rows around 128-row tile edges, and a few random ones."""
+    last rows, the rows around the 128- and 256-row tile edges (including the
+    edges of its last, partial tile), and a few random ones.  ``per_class``
+    picks up to that many experts of each tail_class before the random ones
+    (so every tile shape of the GEMM's split is covered)."""
     rng = np.random.default_rng(seed)
     experts = [e for e in range(E) if offsets[e + 1] > offsets[e]]
     if max_experts is not None and len(experts) > max_experts:
         keep = {experts[0], experts[-1]}
-        keep |= set(rng.choice(experts, max_experts - 2, replace=False).tolist())
+        if per_class:
+            for cls in ("whole", "tail", "pair_part"):
+                of = [e for e in experts if tail_class(offsets[e + 1] - offsets[e]) == cls]
+                if of:
+                    keep |= set(rng.choice(of, min(per_class, len(of)), replace=False).tolist())
+        rest = [e for e in experts if e not in keep]
+        n_more = max(0, min(len(rest), max_experts - len(keep)))
+        if n_more:
+            keep |= set(rng.choice(rest, n_more, replace=False).tolist())
         experts = sorted(keep)
     rows = set()
     for e in experts:
         a, b = int(offsets[e]), int(offsets[e + 1])
-        for r in (a, b - 1, a + 127, a + 128, a + 255, a + 256):
+        last_tile = a + ((b - a - 1) // 256) * 256
+        for r in (a, b - 1, a + 127, a + 128, a + 255, a + 256, last_tile - 1, last_tile,
+                  last_tile + 127, last_tile + 128):
             if a <= r < b:
                 rows.add(r)
         for r in rng.integers(a, b, size=min(per_expert, b - a)):
@@ -107,25 +129,33 @@ def sample_rows(offsets, E, per_expert=6, max_experts=None, seed=0):
     return np.array(sorted(rows), np.int32)
 
 
-def oracle_yd(wl, inp, xd_rows, rows, offsets):
+def oracle_yd(wl, inp, xd_rows, rows, offsets, experts_per_copy=16):
     """Oracle expert outputs for the given buffer rows (device xd row values),
-    copying to the host only the experts those rows belong to."""
+    copying to the host only the experts those rows belong to, a group of at
+    most ``experts_per_copy`` experts at a time (bounded host memory)."""
     E = wl.E
+    rows = np.asarray(rows)
     exp_of = np.searchsorted(offsets, rows, side="right") - 1
     experts = np.unique(exp_of)
-    sub_off = np.searchsorted(exp_of, experts, side="left").tolist() + [len(rows)]
-    sub_off = np.array(sub_off, np.int32)
-    idx = torch.as_tensor(experts, device=inp["W1"].device, dtype=torch.long)
-    W1 = h(inp["W1"].index_select(0, idx))
-    W2 = h(inp["W2"].index_select(0, idx))
-    b1 = h(inp["b1"].index_select(0, idx))
-    b2 = h(inp["b2"].index_select(0, idx))
     assert E >= len(experts)
-    return oracle.ffn_rows(xd_rows, sub_off, W1, b1, W2, b2, ACT[wl.act])
+    out = np.empty((len(rows), wl.d), np.float64)
+    for g0 in range(0, len(experts), experts_per_copy):
+        grp = experts[g0:g0 + experts_per_copy]
+        sel = np.nonzero(np.isin(exp_of, grp))[0]
+        sub_off = np.searchsorted(exp_of[sel], grp, side="left").tolist() + [len(sel)]
+        sub_off = np.array(sub_off, np.int32)
+        idx = torch.as_tensor(grp, device=inp["W1"].device, dtype=torch.long)
+        W1 = h(inp["W1"].index_select(0, idx))
+        W2 = h(inp["W2"].index_select(0, idx))
+        b1 = h(inp["b1"].index_select(0, idx))
+        b2 = h(inp["b2"].index_select(0, idx))
+        out[sel] = oracle.ffn_rows(xd_rows[sel], sub_off, W1, b1, W2, b2, ACT[wl.act])
+    return out
 
 
 def check_forward(wl, inp, out, alpha=1.0, full=False, max_rows_check=None, n_tokens=None,
-                  max_experts=None, e2e_tokens=64, seed=0, reroute=False):
+                  max_experts=None, e2e_tokens=64, seed=0, reroute=False, per_expert=6,
+                  per_class=None):
     """Compare every output of one forward pass with the oracle (routing with
     inp["sel_bias"] when present; out["health"] when present)."""
     sel_bias = h(inp["sel_bias"]) if inp.get("sel_bias") is not None else None
@@ -165,7 +195,8 @@ def check_forward(wl, inp, out, alpha=1.0, full=False, max_rows_check=None, n_to
         rows = np.arange(n, dtype=np.int32)
         toks = np.arange(T, dtype=np.int64)
     else:
-        rows = sample_rows(fl["offsets"], E, max_experts=max_experts, seed=seed)
+        rows = sample_rows(fl["offsets"], E, per_expert=per_expert, max_experts=max_experts,
+                           seed=seed, per_class=per_class)
         if max_rows_check is not None and len(rows) > max_rows_check:
             rows = np.sort(rng.choice(rows, max_rows_check, replace=False)).astype(np.int32)
         toks = np.sort(rng.choice(T, min(e2e_tokens, T), replace=False)).astype(np.int64)
@@ -222,4 +253,8 @@ def check_forward(wl, inp, out, alpha=1.0, full=False, max_rows_check=None, n_to
         ref = oracle.routing_health(fl["counts"], fl["kept"], T, k)
         np.testing.assert_allclose(h(out["health"]), ref, rtol=1e-4, atol=1e-6,
                                    err_msg="health")
-    return dict(n_rows=n, rows_checked=len(rows), tokens_e2e=len(toks))
+    exp_of = np.searchsorted(fl["offsets"], rows, side="right") - 1
+    return dict(n_rows=n, rows_checked=len(rows), tokens_e2e=len(toks),
+                experts_checked=len(np.unique(exp_of)) if len(rows) else 0,
+                classes_checked=sorted({tail_class(fl["kept"][e]) for e in np.unique(exp_of)})
+                if len(rows) else [])

@@ -59,3 +59,80 @@ def test_fully_dropped_tokens_output_zero():
     assert dropped.sum() > wl.T // 2  # the tiny capacity drops most tokens entirely
     y = inputs.as_f64(h(out["y"]))
     assert (y[dropped] == 0).all()
+
+
+# ---- caller-supplied expert ids: repeats within a token, ids out of range ----
+
+def _ids_case(T, E, k, seed):
+    """Host-built ids: a random distinct set per token, as a router gives."""
+    rng = np.random.default_rng(seed)
+    return np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32), rng
+
+
+def _dispatch_with(cfg, x, ids_host, noalloc=False):
+    import torch
+    ids = torch.as_tensor(ids_host, device="cuda")
+    out = moe.allocate(cfg)
+    ws = moe.workspace(cfg)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    if noalloc:
+        moe.dispatch_noalloc(cfg, x, ids, out, status)
+    else:
+        moe.dispatch(cfg, x, ids, out, ws)
+    torch.cuda.synchronize()
+    st = int(status.item()) if noalloc else moe.device_status(ws)
+    return out, st
+
+
+@pytest.mark.parametrize("noalloc", [False, True], ids=["workspace", "noalloc"])
+def test_repeated_expert_within_a_token_matches_oracle_fill(noalloc):
+    # Every (t, r) is its own slot; two ranks of one token naming the same
+    # expert take consecutive positions in rank order, exactly as the
+    # oracle's sequential fill gives them.
+    import oracle
+    T, E, k = 700, 8, 4
+    wl = wl_of("repeats", T, 64, 64, E, k, 1.0)
+    cfg = moe.config_from_workload(wl)
+    ids, rng = _ids_case(T, E, k, 5)
+    rep = rng.random(T) < 0.3
+    ids[rep, 2] = ids[rep, 0]          # rank 2 repeats rank 0
+    ids[rep[::-1], 3] = ids[rep[::-1], 1]
+    x = inputs.make_inputs(wl, "cuda")["x"]
+    out, st = _dispatch_with(cfg, x, ids, noalloc)
+    assert st == moe.MOE_OK
+    fl = oracle.fill(ids, E, moe.capacity(cfg))
+    for name in ["counts", "kept", "offsets", "slot_row"]:
+        np.testing.assert_array_equal(h(out[name]), fl[name], name)
+    n = int(fl["offsets"][E])
+    np.testing.assert_array_equal(h(out["row_token"])[:n], fl["row_token"])
+    np.testing.assert_array_equal(h(out["xd"])[:n], h(x)[fl["row_token"]])
+
+
+@pytest.mark.parametrize("noalloc", [False, True], ids=["workspace", "noalloc"])
+def test_out_of_range_ids_are_skipped_and_reported(noalloc):
+    # An id outside [0, E) names no expert: its slot is not counted, its
+    # slot_row is -1, the status word says MOE_ERR_INVALID_ARG, and every
+    # other slot is dispatched as if that slot were absent.  Expected values:
+    # the oracle's fill with the bad slots sent to an extra expert E placed
+    # after all real ones (same capacity C), which leaves experts 0..E-1,
+    # their rows and their offsets exactly as without those slots.
+    import oracle
+    T, E, k = 512, 8, 2
+    wl = wl_of("bad_ids", T, 64, 64, E, k, 1.0)
+    cfg = moe.config_from_workload(wl)
+    ids, rng = _ids_case(T, E, k, 6)
+    bad = rng.random((T, k)) < 0.05
+    ids[bad] = np.where(rng.random(bad.sum()) < 0.5, E, -3)
+    x = inputs.make_inputs(wl, "cuda")["x"]
+    out, st = _dispatch_with(cfg, x, ids, noalloc)
+    assert st == moe.MOE_ERR_INVALID_ARG
+    C = moe.capacity(cfg)
+    fl = oracle.fill(np.where(bad, E, ids).astype(np.int32), E + 1, C)
+    np.testing.assert_array_equal(h(out["counts"]), fl["counts"][:E])
+    np.testing.assert_array_equal(h(out["kept"]), fl["kept"][:E])
+    np.testing.assert_array_equal(h(out["offsets"]), fl["offsets"][:E + 1])
+    want = np.where(bad, -1, fl["slot_row"])
+    np.testing.assert_array_equal(h(out["slot_row"]), want)
+    n = int(fl["offsets"][E])
+    np.testing.assert_array_equal(h(out["row_token"])[:n], fl["row_token"][:n])
+    np.testing.assert_array_equal(h(out["xd"])[:n], h(x)[fl["row_token"][:n]])

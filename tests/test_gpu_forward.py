@@ -46,7 +46,8 @@ def test_bf16_t8192_d2048_e64_top6():
 def test_bf16_t16384_d4096_e8_top1():
     wl = W["bf16_t16384_d4096_e8_top1"]
     _, inp, out, _ = run_gpu(wl)
-    check_forward(wl, inp, out, n_tokens=2048, e2e_tokens=48, max_rows_check=400)
+    info = check_forward(wl, inp, out, n_tokens=2048, e2e_tokens=256, max_rows_check=400)
+    assert info["tokens_e2e"] >= 256
     # the dispatch buffer is in expert order, so the four groups of two
     # experts are contiguous: group g = rows offsets[2g] .. offsets[2g+2]
     off = h(out["offsets"])
@@ -54,9 +55,25 @@ def test_bf16_t16384_d4096_e8_top1():
 
 
 def test_bf16_t32768_d7168_e256_top8():
+    # The largest layer: 64 tokens end to end (every kept row of theirs), and
+    # over 1000 expert-output rows from at least 48 experts, at least four
+    # experts of each tile shape of the GEMM's pair-body/tail split (rows % 256
+    # = 0; 1..128; 129..255) with the rows at every tile edge.
     wl = W["bf16_t32768_d7168_e256_top8"]
     _, inp, out, _ = run_gpu(wl)
-    check_forward(wl, inp, out, n_tokens=384, e2e_tokens=4, max_experts=10, max_rows_check=200)
+    info = check_forward(wl, inp, out, n_tokens=384, e2e_tokens=64, max_experts=56,
+                         per_expert=12, per_class=6)
+    assert info["tokens_e2e"] >= 64
+    assert info["rows_checked"] >= 1000 and info["experts_checked"] >= 48
+    assert info["classes_checked"] == ["pair_part", "tail", "whole"]
+
+
+def test_fp32_gelu_full():
+    # The CUDA-core (fp32) expert GEMM with the tanh-form GELU, every output
+    # at the fp32 bar.
+    wl = W["fp32_t512_d128_e8_top2"].replace(act="gelu_tanh")
+    _, inp, out, _ = run_gpu(wl, expert_bias=True)
+    check_forward(wl, inp, out, full=True)
 
 
 def test_expert_bias_path():

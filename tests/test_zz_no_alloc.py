@@ -61,6 +61,51 @@ def test_noalloc_dispatch_matches_workspace_dispatch_twice(name):
         assert int(ref["offsets"][-1]) > 0
 
 
+def test_noalloc_dispatch_matches_oracle():
+    # Directly against the oracle's fill and permutation, on the device's
+    # routing of a small layer.
+    import oracle
+    wl = inputs.WORKLOADS["bf16_t4096_d1024_e8_top2"].replace(T=1000, capacity_factor=0.9)
+    cfg, inp, ref, ws = _route(wl, wl.seed)
+    got = moe.allocate(cfg)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    moe.dispatch_noalloc(cfg, inp["x"], ref["topk_ids"], got, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == moe.MOE_OK
+    ids = inputs.to_numpy(ref["topk_ids"])
+    fl = oracle.fill(ids, wl.E, moe.capacity(cfg))
+    for name in OUTPUTS:
+        np.testing.assert_array_equal(inputs.to_numpy(got[name]), fl[name], name)
+    n = int(fl["offsets"][-1])
+    assert 0 < n < wl.T * wl.k  # c = 0.9 drops some slots
+    np.testing.assert_array_equal(inputs.to_numpy(got["row_token"])[:n], fl["row_token"])
+    x = inputs.to_numpy(inp["x"])
+    np.testing.assert_array_equal(inputs.to_numpy(got["xd"])[:n], x[fl["row_token"]])
+
+
+def test_noalloc_fused_dispatch_matches_workspace_dispatch():
+    # With fuse_dispatch no row is copied (xd is NULL); every index output
+    # equals moe_dispatch's.
+    wl = inputs.WORKLOADS["bf16_t8192_d2048_e64_top6"].replace(T=3000)
+    inp = inputs.make_inputs(wl, "cuda")
+    cfg = moe.config_from_workload(wl, fuse_dispatch=True)
+    ws = moe.workspace(cfg)
+    ref = moe.allocate(cfg)
+    assert ref["xd"] is None
+    moe.route(cfg, inp["x"], inp["Wr"], inp["br"], ref, ws)
+    moe.dispatch(cfg, inp["x"], ref["topk_ids"], ref, ws)
+    for _ in range(2):
+        got = moe.allocate(cfg)
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        moe.dispatch_noalloc(cfg, inp["x"], ref["topk_ids"], got, status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == moe.MOE_OK
+        for name in OUTPUTS:
+            assert torch.equal(ref[name], got[name]), name
+        n = int(ref["offsets"][-1])
+        assert torch.equal(ref["row_token"][:n], got["row_token"][:n])
+
+
 def test_noalloc_rejects_oversize_before_launch():
     # ceil(T/256)*E above the fixed 262144-entry scratch
     cfg = moe.config(T=1 << 20, d=64, d_ff=64, E=128, k=1, capacity_factor=1.0)
