@@ -212,7 +212,7 @@ def cpu_model() -> str:
     return ""
 
 
-def cpu_sample_tokens(wl, flop_budget: float = 1e11) -> int:
+def cpu_sample_tokens(wl, flop_budget: float = 3e11) -> int:
     """Tokens S of the CPU oracle's timed sample: the largest power of two,
     at most T, whose forward pass costs at most ``flop_budget`` of the
     method's arithmetic (router 2·d·E plus expert FFN k·4·d·d_ff per token),
@@ -294,6 +294,7 @@ def bench_config(wl, args, world):
                 parallelism=f"replicas{world}" if world > 1 else "single",
                 sel_bias=bool(args.sel_bias), health=bool(args.health),
                 reroute=bool(args.reroute), fuse_dispatch=bool(args.fuse_dispatch),
+                fuse_combine=bool(args.fuse_combine),
                 l2="flushed between steps (512 MiB write, then 512 MiB read)")
 
 
@@ -359,6 +360,8 @@ def main():
                     help="offer overflowing slots to the token's next candidate")
     ap.add_argument("--fuse-dispatch", action="store_true",
                     help="no dispatch buffer: the first GEMM gathers the token rows")
+    ap.add_argument("--fuse-combine", action="store_true",
+                    help="the second GEMM also combines (no separate combine launch)")
     args = ap.parse_args()
     wl = inputs.WORKLOADS[args.workload]
 
@@ -391,7 +394,8 @@ def main():
         g = torch.Generator(device=dev).manual_seed(replica_seed(wl.seed, rank))
         inp["x"] = torch.randn(inp["x"].shape, generator=g, device=dev).to(inp["x"].dtype)
     cfg = moe.config_from_workload(wl, write_logits=False, reroute=args.reroute,
-                                   fuse_dispatch=args.fuse_dispatch)
+                                   fuse_dispatch=args.fuse_dispatch,
+                                   fuse_combine=args.fuse_combine)
     ws = moe.workspace(cfg, dev)
     out = moe.allocate(cfg, dev, health=args.health)
     stream = torch.cuda.current_stream(dev)
@@ -423,17 +427,25 @@ def main():
                                              inp["W1"], inp["b1"], out["H"], ws))
         if args.fuse_dispatch else
         (lambda: moe.ffn_up(cfg, out["xd"], out["offsets"], inp["W1"], inp["b1"], out["H"], ws)),
-        "ffn_down": lambda: moe.ffn_down(cfg, out["H"], out["offsets"], inp["W2"], inp["b2"],
-                                         out["yd"], ws),
-        "combine": lambda: moe.combine(cfg, out["yd"], out["slot_row"], out["topk_w"], out["y"]),
+        "ffn_down": (lambda: moe.ffn_down_combine(cfg, out["H"], out["offsets"],
+                                                  out["row_token"], out["slot_row"],
+                                                  out["topk_w"], inp["W2"], inp["b2"], out["yd"],
+                                                  out["y"], ws))
+        if args.fuse_combine else
+        (lambda: moe.ffn_down(cfg, out["H"], out["offsets"], inp["W2"], inp["b2"], out["yd"],
+                              ws)),
+        "combine": None if args.fuse_combine else
+        (lambda: moe.combine(cfg, out["yd"], out["slot_row"], out["topk_w"], out["y"])),
         "aux": lambda: moe.aux_stats(cfg, out["counts"], out["psum"], args.alpha, out["f"],
                                      out["pbar"], out["l_aux"]),
     }
-    g_stage = {name: capture(fn) for name, fn in stage_calls.items()}
+    # (with the combine fused into ffn_down there is no combine stage: 0 ms)
+    g_stage = {name: capture(fn) for name, fn in stage_calls.items() if fn is not None}
     for _ in range(2):
         g_full.replay()
         for name in STAGES:
-            g_stage[name].replay()
+            if name in g_stage:
+                g_stage[name].replay()
     torch.cuda.synchronize(dev)
 
     def ev():
@@ -461,7 +473,8 @@ def main():
         flush_l2()
         for i, name in enumerate(STAGES):
             sevs[s_][i].record(stream)
-            g_stage[name].replay()
+            if name in g_stage:
+                g_stage[name].replay()
         sevs[s_][6].record(stream)
     torch.cuda.synchronize(dev)
     # Eager reference: moe_forward launched from Python each step.
@@ -500,7 +513,8 @@ def main():
     ffn_ms = mean["ffn_up"] + mean["ffn_down"]
     dom = "ffn_up" if mean["ffn_up"] >= mean["ffn_down"] else "ffn_down"
     dom_tflops = alg[f"{dom}_flops"] / (mean[dom] * 1e-3) / 1e12
-    dom_kernel = "ffn_up_gather" if (dom == "ffn_up" and args.fuse_dispatch) else dom
+    dom_kernel = ("ffn_up_gather" if (dom == "ffn_up" and args.fuse_dispatch) else
+                  "ffn_down_combine" if (dom == "ffn_down" and args.fuse_combine) else dom)
     traffic = kernel_traffic(dom_kernel, wl.name, os.path.join(
         ROOT, "routing_dispatch_expert_06_b300", "csrc", "ffn_tc.cu"))
 
@@ -544,8 +558,9 @@ def main():
     b = 2 if wl.dtype == "bf16" else 4
     hbm = peaks["hbm"]
     stage_gbs = dict(route=alg["route_bytes"] / (mean["route"] * 1e-3) / 1e9,
-                     dispatch=alg["dispatch_bytes"] / (mean["dispatch"] * 1e-3) / 1e9,
-                     combine=alg["combine_bytes"] / (mean["combine"] * 1e-3) / 1e9)
+                     dispatch=alg["dispatch_bytes"] / (mean["dispatch"] * 1e-3) / 1e9)
+    if not args.fuse_combine:  # fused: the combine's bytes move inside ffn_down
+        stage_gbs["combine"] = alg["combine_bytes"] / (mean["combine"] * 1e-3) / 1e9
     ffn_tflops = alg["ffn_up_flops"] * 2 / (ffn_ms * 1e-3) / 1e12
     line = dict(
         metric=METRIC, value=value, unit="tokens/s", n_gpus=world, steps=K, warmup=args.warmup,
@@ -572,7 +587,7 @@ def main():
         ffn_tc_frac=ffn_tflops / peaks["bf16"],
         ffn_tc_frac_sustained=ffn_tflops / peaks["bf16_sustained"],
         dispatch_gbs=stage_gbs["dispatch"],
-        combine_gbs=stage_gbs["combine"],
+        combine_gbs=stage_gbs.get("combine"),
         route_gbs=stage_gbs["route"],
         hbm_peak_gbs=hbm,
         hbm_frac={k: v / hbm for k, v in stage_gbs.items()},

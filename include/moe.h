@@ -77,6 +77,7 @@ typedef struct moe_config {
   int32_t write_logits;     /* 1: moe_route also writes fp32 logits[T,E] */
   int32_t reroute;          /* 1: overflow goes to the next candidate (§4.3) */
   int32_t fuse_dispatch;    /* 1: no xd; the first GEMM gathers x rows (moe_ffn_up_gather) */
+  int32_t fuse_combine;     /* 1: the second GEMM also combines (moe_ffn_down_combine) */
 } moe_config_t;
 
 /* Every tensor of one forward pass (all device pointers). */
@@ -125,13 +126,17 @@ int64_t moe_max_rows(const moe_config_t* cfg);
  * status word, completion counters and the router's fixed-point column-sum
  * accumulators; per-chunk histograms; per-block probability partial sums; the
  * tensor-core router's fp32 partial logits, nsplit·T·E floats, nsplit > 1 only
- * for small T).  Host only.  A workspace serves one stream at a time. */
+ * for small T; with cfg->reroute the reroute's [T, k] arrays; with
+ * cfg->fuse_combine the combine's arrival counters, 2 int32 per token and
+ * 256-wide column tile of d).  Host only.  A workspace serves one stream at a
+ * time. */
 moe_status_t moe_workspace_size(const moe_config_t* cfg, size_t* bytes);
 
-/* Clear the workspace's 272 KiB header: the device status word, the counters
- * the kernels use to find the last block of a grid and the column-sum
- * accumulators (enqueued on stream; kernels leave them at zero).  Call once after allocating a
- * workspace, and after reading a nonzero status. */
+/* Clear the whole workspace (ws_bytes bytes, at least the 272 KiB header):
+ * the device status word, the counters the kernels use to find the last
+ * block of a grid and the column-sum accumulators (enqueued on stream;
+ * kernels leave them at zero).  Call once after allocating a workspace, and
+ * after reading a nonzero status. */
 moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, void* stream);
 
 /* [MoE 模型原理 §2.1–§2.2] Router: logits s = x W_rᵀ + b_r (fp32 accumulate),
@@ -215,6 +220,26 @@ moe_status_t moe_ffn_down(const moe_config_t* cfg, const void* H, const int32_t*
                           const void* W2, const float* b2, void* yd, void* ws, size_t ws_bytes,
                           void* stream);
 
+/* moe_ffn_down with the combine folded into the GEMM's epilogue (the fused
+ * combine of [MoE Gate 分布式通信 mianshidashi, 06]; [MoE 模型原理 §2.2, §5]):
+ * writes yd as moe_ffn_down does and y as moe_combine would from it, bit for
+ * bit.  A token's k rows are finished by different CTAs: a first small
+ * kernel sets a counter per token and column range of the workspace to the
+ * token's number of kept slots (and writes y = 0 for a token with none);
+ * each epilogue warp takes one count off per row it stored, and the warp
+ * whose decrement reaches zero sums the token's k rows of that range in rank
+ * order in fp32; no block waits on another.
+ *  - row_token, slot_row (from moe_dispatch) and topk_w (from moe_route) are
+ *    device pointers; H, W2, yd and y 16-byte aligned;
+ *  - cfg->fuse_combine must be 1 (MOE_ERR_INVALID_ARG otherwise: the
+ *    workspace then has no counters);
+ *  - bf16 layers on the tensor-core GEMM only: MOE_ERR_UNSUPPORTED (no
+ *    launch) for fp32 layers and for min(C, T·k) <= 64. */
+moe_status_t moe_ffn_down_combine(const moe_config_t* cfg, const void* H, const int32_t* offsets,
+                                  const int32_t* row_token, const int32_t* slot_row,
+                                  const float* topk_w, const void* W2, const float* b2, void* yd,
+                                  void* y, void* ws, size_t ws_bytes, void* stream);
+
 /* moe_ffn_up followed by moe_ffn_down. */
 moe_status_t moe_expert_ffn(const moe_config_t* cfg, const void* xd, const int32_t* offsets,
                             const void* W1, const float* b1, const void* W2, const float* b2,
@@ -260,6 +285,9 @@ moe_status_t moe_aux_stats(const moe_config_t* cfg, const int32_t* counts, const
  * t->xd may be NULL: the dispatch writes positions and row_token only and
  * the first GEMM runs as moe_ffn_up_gather (MOE_ERR_UNSUPPORTED, before any
  * launch, where that call is unsupported); every other output is identical.
+ * With cfg->fuse_combine the second GEMM runs as moe_ffn_down_combine and
+ * there is no separate combine launch (same y, bit for bit; same
+ * MOE_ERR_UNSUPPORTED rule).
  * If it returns an error after the router was enqueued, call
  * moe_workspace_init before the next call on that workspace. */
 moe_status_t moe_forward(const moe_config_t* cfg, const moe_tensors_t* t, float alpha, void* ws,

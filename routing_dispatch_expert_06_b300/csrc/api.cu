@@ -148,10 +148,19 @@ static moe_status_t check_cfg(const moe_config_t* c) {
   if (c->reroute != 0 && c->reroute != 1) return fail(MOE_ERR_INVALID_ARG, "reroute must be 0 or 1");
   if (c->fuse_dispatch != 0 && c->fuse_dispatch != 1)
     return fail(MOE_ERR_INVALID_ARG, "fuse_dispatch must be 0 or 1");
+  if (c->fuse_combine != 0 && c->fuse_combine != 1)
+    return fail(MOE_ERR_INVALID_ARG, "fuse_combine must be 0 or 1");
   return MOE_OK;
 }
 
 static size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+// Arrival counters of the combine folded into the second GEMM: one per token,
+// column tile and column half of that GEMM (N = d).
+static size_t combine_counters(const moe_config_t& c) {
+  const int bn = gemm_tc_bn(c.d);
+  return size_t(c.T) * 2 * size_t((c.d + bn - 1) / bn);
+}
 
 static WsLayout layout_of(const moe_config_t& c) {
   WsLayout L{};
@@ -170,6 +179,8 @@ static WsLayout layout_of(const moe_config_t& c) {
   L.reroute = off;
   if (c.reroute)
     off += 4 * align256(size_t(c.T) * c.k * sizeof(int32_t)) + 2 * align256(size_t(c.E) * 4);
+  L.combine_cnt = off;
+  if (c.fuse_combine) off += align256(combine_counters(c) * sizeof(int32_t));
   L.total = off;
   return L;
 }
@@ -184,6 +195,7 @@ struct Ws {
   unsigned long long* psum_fixed;
   RerouteBufs rr;  // all NULL unless cfg.reroute
   int32_t* cand;   // = rr.cand (written by the router)
+  int* combine_cnt;  // NULL unless cfg.fuse_combine
 };
 
 static moe_status_t get_ws(const moe_config_t& c, void* ws, size_t ws_bytes, Ws* out) {
@@ -203,6 +215,7 @@ static moe_status_t get_ws(const moe_config_t& c, void* ws, size_t ws_bytes, Ws*
   out->psum_fixed = reinterpret_cast<unsigned long long*>(b + L.status + kWsPsumFixed);
   out->rr = RerouteBufs{};
   out->cand = nullptr;
+  out->combine_cnt = c.fuse_combine ? reinterpret_cast<int*>(b + L.combine_cnt) : nullptr;
   if (c.reroute) {
     const size_t tk = align256(size_t(c.T) * c.k * sizeof(int32_t));
     char* r = b + L.reroute;
@@ -234,8 +247,8 @@ static bool use_tc_gemm(const moe_config_t& c) {
   return !(v && std::strcmp(v, "simt") == 0);
 }
 
-// The gathering first GEMM exists for the regular tcgen05 kernel only (bf16,
-// more than 64 rows per expert possible).
+// The gathering first GEMM and the combining second GEMM exist for the
+// regular tcgen05 kernel only (bf16, more than 64 rows per expert possible).
 static bool gather_supported(const moe_config_t& c) {
   return use_tc_gemm(c) && !gemm_swap_applies(rows_per_expert_max(&c));
 }
@@ -333,7 +346,7 @@ moe_status_t moe_workspace_size(const moe_config_t* cfg, size_t* bytes) {
 
 moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, void* stream) {
   if (!ws || ws_bytes < kWsHeaderBytes) return fail(MOE_ERR_INVALID_ARG, "workspace too small");
-  cudaError_t e = cudaMemsetAsync(ws, 0, kWsHeaderBytes, static_cast<cudaStream_t>(stream));
+  cudaError_t e = cudaMemsetAsync(ws, 0, ws_bytes, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_workspace_init");
 }
 
@@ -480,6 +493,33 @@ moe_status_t moe_ffn_down(const moe_config_t* cfg, const void* H, const int32_t*
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_ffn_down");
 }
 
+moe_status_t moe_ffn_down_combine(const moe_config_t* cfg, const void* H, const int32_t* offsets,
+                                  const int32_t* row_token, const int32_t* slot_row,
+                                  const float* topk_w, const void* W2, const float* b2, void* yd,
+                                  void* y, void* ws, size_t ws_bytes, void* stream) {
+  const StageRange range("moe_ffn_down_combine");
+  moe_status_t s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  if (!H || !offsets || !row_token || !slot_row || !topk_w || !W2 || !b2 || !yd || !y)
+    return fail(MOE_ERR_INVALID_ARG, "moe_ffn_down_combine: NULL tensor");
+  if (!aligned16(H) || !aligned16(W2) || !aligned16(yd) || !aligned16(y))
+    return fail(MOE_ERR_INVALID_ARG, "moe_ffn_down_combine: H, W2, yd, y must be 16-byte aligned");
+  if (!cfg->fuse_combine)
+    return fail(MOE_ERR_INVALID_ARG,
+                "moe_ffn_down_combine: needs cfg->fuse_combine (its workspace holds the counters)");
+  if (!gather_supported(*cfg))
+    return fail(MOE_ERR_UNSUPPORTED,
+                "moe_ffn_down_combine: needs bf16 and the tensor-core GEMM for more than 64 rows "
+                "per expert");
+  Ws w;
+  if ((s = get_ws(*cfg, ws, ws_bytes, &w)) != MOE_OK) return s;
+  cudaError_t e = launch_gemm_tc_combine(cfg->E, cfg->d, cfg->d_ff, moe_max_rows(cfg), offsets, H,
+                                         W2, b2, yd, cfg->T, cfg->k, row_token, slot_row, topk_w,
+                                         y, w.combine_cnt, w.status,
+                                         static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_ffn_down_combine");
+}
+
 moe_status_t moe_expert_ffn(const moe_config_t* cfg, const void* xd, const int32_t* offsets,
                             const void* W1, const float* b1, const void* W2, const float* b2,
                             void* H, void* yd, void* ws, size_t ws_bytes, void* stream) {
@@ -523,10 +563,10 @@ moe_status_t moe_forward(const moe_config_t* cfg, const moe_tensors_t* t, float 
     return fail(MOE_ERR_INVALID_ARG, "moe_aux_stats: NULL tensor");
   moe_status_t s = check_cfg(cfg);
   if (s != MOE_OK) return s;
-  if (cfg->fuse_dispatch && !gather_supported(*cfg))
+  if ((cfg->fuse_dispatch || cfg->fuse_combine) && !gather_supported(*cfg))
     return fail(MOE_ERR_UNSUPPORTED,
-                "moe_forward: fuse_dispatch needs bf16 and the tensor-core GEMM for more than 64 "
-                "rows per expert");
+                "moe_forward: fuse_dispatch and fuse_combine need bf16 and the tensor-core GEMM "
+                "for more than 64 rows per expert");
   unsigned long long* psum_fixed = nullptr;
   if ((s = route_impl(cfg, t->x, t->Wr, t->br, t->sel_bias, t->logits, t->topk_ids, t->topk_w,
                       t->psum, ws, ws_bytes, &psum_fixed, stream)) != MOE_OK)
@@ -538,16 +578,17 @@ moe_status_t moe_forward(const moe_config_t* cfg, const moe_tensors_t* t, float 
   if ((s = dispatch_impl(cfg, t->x, t->topk_ids, t->counts, t->kept, t->offsets, t->slot_row,
                          t->row_token, t->xd, ws, ws_bytes, &aux, stream)) != MOE_OK)
     return s;
-  if (cfg->fuse_dispatch) {
-    if ((s = moe_ffn_up_gather(cfg, t->x, t->row_token, t->offsets, t->W1, t->b1, t->H, ws,
-                               ws_bytes, stream)) != MOE_OK ||
-        (s = moe_ffn_down(cfg, t->H, t->offsets, t->W2, t->b2, t->yd, ws, ws_bytes, stream)) !=
-            MOE_OK)
-      return s;
-  } else if ((s = moe_expert_ffn(cfg, t->xd, t->offsets, t->W1, t->b1, t->W2, t->b2, t->H, t->yd,
-                                 ws, ws_bytes, stream)) != MOE_OK) {
+  s = cfg->fuse_dispatch ? moe_ffn_up_gather(cfg, t->x, t->row_token, t->offsets, t->W1, t->b1,
+                                              t->H, ws, ws_bytes, stream)
+                         : moe_ffn_up(cfg, t->xd, t->offsets, t->W1, t->b1, t->H, ws, ws_bytes,
+                                      stream);
+  if (s != MOE_OK) return s;
+  if (cfg->fuse_combine)
+    return moe_ffn_down_combine(cfg, t->H, t->offsets, t->row_token, t->slot_row, t->topk_w,
+                                t->W2, t->b2, t->yd, t->y, ws, ws_bytes, stream);
+  if ((s = moe_ffn_down(cfg, t->H, t->offsets, t->W2, t->b2, t->yd, ws, ws_bytes, stream)) !=
+      MOE_OK)
     return s;
-  }
   return moe_combine(cfg, t->yd, t->slot_row, t->topk_w, t->y, stream);
 }
 

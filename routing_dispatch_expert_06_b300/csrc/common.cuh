@@ -28,6 +28,7 @@ struct WsLayout {
   size_t psum_partial;  // fp32 [n_route_blocks, E] (warp router)
   size_t route_part;    // fp32 [nsplit, T, E] partial logits (tensor-core router)
   size_t reroute;       // reroute only: int32 cand, ids1, pos0, pos1 [T, k]; kept0, counts1 [E]
+  size_t combine_cnt;   // fuse_combine only: int32 [T, 2·column tiles] arrival counters
   size_t total;
   int64_t n_chunks;
   int64_t n_route_blocks;

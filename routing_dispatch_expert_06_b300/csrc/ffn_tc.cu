@@ -138,19 +138,184 @@ __device__ __forceinline__ float epi_act(float u) {
   return u;
 }
 
+// CK > 0: the second GEMM also runs the combine of [MoE 模型原理 §2.2, §5]
+// in its epilogue (the combine folded into the expert GEMM, the other half of
+// the fused permutation/dispatch kernel of [MoE Gate 分布式通信 mianshidashi,
+// 06]).  A token's k expert rows are finished by different CTAs.  Before the
+// GEMM, combine_prep_kernel sets every (token, column tile, column half)
+// counter to the token's number of kept slots and writes y = 0 for tokens
+// with none.  Each epilogue warp, once its rows of yd are stored and
+// released, takes one count off per row; the warp whose decrement reaches
+// zero sums the token's k rows of that column range in rank order in fp32
+// (the arithmetic of combine_kernel, so y is identical bit for bit to the
+// separate combine).  Nobody waits on anybody: the last arrival does the work.
+// CK (2, 4, 8 or 16) bounds k, which sizes the per-token registers.
+struct CombineArgs {
+  const int32_t* slot_row;  // [T, k]
+  const float* w;           // [T, k]
+  __nv_bfloat16* y;         // [T, N]
+  int* cnt;                 // [T, n_col_tiles, 2] arrivals still expected
+  int k;
+  int64_t T;
+};
+
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+
+// The combine part of an epilogue warp of a combining GEMM, after the warp has stored rows
+// row0 .. row0+31 of the tile, columns [c_lo, c_end) past n0: lane l arrives
+// for row row0 + l; each lane whose arrival was the token's last loads the
+// token's kept rows and weights (one round trip for all of them), then the
+// warp sums two tokens at a time (16 lanes × 8 columns each).
+template <int KMAX>
+__device__ __forceinline__ void combine_rows(int m_end, int n0, int row0, int lane, int half,
+                                             int c_lo, int c_end, int N, int BN, int64_t max_rows,
+                                             const int32_t* __restrict__ row_token,
+                                             const __nv_bfloat16* yd, const CombineArgs& cmb) {
+  // Release: every lane fences its own stores of yd, then the warp meets, so
+  // each row's stores (made by several lanes) are visible device-wide before
+  // the lane that owns the row arrives.
+  fence_acq_rel_gpu();
+  __syncwarp();
+  const int g = row0 + lane;
+  int64_t t = -1;
+  bool last = false;
+  if (g < m_end) {
+    const int32_t tt = row_token[g];
+    if (tt >= 0 && int64_t(tt) < cmb.T) {
+      t = tt;
+      const int n_tn = (N + BN - 1) / BN;
+      last = atomicAdd(cmb.cnt + (t * n_tn + n0 / BN) * 2 + half, -1) == 1;
+    }
+  }
+  // Acquire: the completing decrement came after every other arrival's
+  // release, so once the arriving lane has fenced and the warp has met, the
+  // rows read below (from L2) are complete.
+  fence_acq_rel_gpu();
+  __syncwarp();
+  unsigned m = __ballot_sync(0xffffffffu, last);
+  if (!m) return;
+  int32_t rows[KMAX];
+  float wts[KMAX];
+#pragma unroll
+  for (int r = 0; r < KMAX; ++r) {
+    rows[r] = -1;
+    wts[r] = 0.f;
+    if (last && r < cmb.k) {
+      const int32_t sr = cmb.slot_row[t * cmb.k + r];
+      if (sr >= 0 && int64_t(sr) < max_rows) {
+        rows[r] = sr;
+        wts[r] = cmb.w[t * cmb.k + r];
+      }
+    }
+  }
+  const int sub = lane & 15;
+  const int col = c_lo + 8 * sub;
+  const bool col_ok = col < c_end;
+  while (m) {
+    const int la = __ffs(m) - 1;
+    m &= m - 1;
+    int lb = la;
+    bool two = false;
+    if (m) {
+      lb = __ffs(m) - 1;
+      m &= m - 1;
+      two = true;
+    }
+    const int src = lane < 16 ? la : lb;
+    const int64_t tok = __shfl_sync(0xffffffffu, t, src);
+    const bool active = (lane < 16 || two) && col_ok;
+    float accv[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) accv[i] = 0.f;
+    // Ranks in groups of at most 8: all of a group's loads are issued before
+    // any arithmetic; the sum still runs r = 0, 1, ... in order.
+#pragma unroll
+    for (int r0 = 0; r0 < KMAX; r0 += 8) {
+      constexpr int G = KMAX < 8 ? KMAX : 8;
+      int32_t rr[G];
+      float ww[G];
+      uint4 buf[G];
+#pragma unroll
+      for (int j = 0; j < G; ++j) {
+        rr[j] = __shfl_sync(0xffffffffu, rows[r0 + j], src);
+        ww[j] = __shfl_sync(0xffffffffu, wts[r0 + j], src);
+        if (active && rr[j] >= 0)
+          buf[j] = __ldcg(reinterpret_cast<const uint4*>(yd + int64_t(rr[j]) * N + n0 + col));
+      }
+#pragma unroll
+      for (int j = 0; j < G; ++j) {
+        float f[8];
+        if (rr[j] >= 0) {
+          const __nv_bfloat162* hv = reinterpret_cast<const __nv_bfloat162*>(&buf[j]);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 p = __bfloat1622float2(hv[i]);
+            f[2 * i] = p.x;
+            f[2 * i + 1] = p.y;
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) f[i] = 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) accv[i] = fmaf(ww[j], f[i], accv[i]);
+      }
+    }
+    if (!active) continue;
+    uint4 o;
+    __nv_bfloat162* ho = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) ho[i] = __floats2bfloat162_rn(accv[2 * i], accv[2 * i + 1]);
+    *reinterpret_cast<uint4*>(cmb.y + tok * N + n0 + col) = o;
+  }
+}
+
+// Before a combining GEMM: cnt[t][nt][h] = kept slots of token t for every
+// column tile nt and half h, and y[t] = 0 for a token with no kept slot.  One
+// block per 256 tokens: each thread counts its token's kept slots, then the
+// block writes its tokens' counters as one contiguous run.
+__global__ void __launch_bounds__(256)
+    combine_prep_kernel(int64_t T, int k, int per_token, int64_t max_rows, int64_t row_vecs,
+                        const int32_t* __restrict__ slot_row, int* __restrict__ cnt,
+                        uint4* __restrict__ y) {
+  __shared__ int s_nk[256];
+  pdl_wait();
+  pdl_trigger();
+  const int64_t t0 = int64_t(blockIdx.x) * 256;
+  const int64_t t = t0 + threadIdx.x;
+  int nk = 0;
+  if (t < T)
+    for (int r = 0; r < k; ++r) {
+      const int32_t sr = slot_row[t * k + r];
+      nk += (sr >= 0 && int64_t(sr) < max_rows) ? 1 : 0;
+    }
+  s_nk[threadIdx.x] = nk;
+  __syncthreads();
+  const int64_t n_tok = T - t0 < 256 ? T - t0 : 256;
+  int* dst = cnt + t0 * per_token;
+  for (int64_t i = threadIdx.x; i < n_tok * per_token; i += 256) dst[i] = s_nk[i / per_token];
+  // y = 0 for the tokens of this block with no kept slot (a warp per token).
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int j = warp; j < n_tok; j += 8)
+    if (s_nk[j] == 0)
+      for (int64_t v = lane; v < row_vecs; v += 32) y[(t0 + j) * row_vecs + v] = make_uint4(0u, 0u, 0u, 0u);
+}
+
 // GATHER: the A rows are not read from a dispatch buffer but gathered from
 // the token matrix x [gx_rows, K] through row_token (A[row] = x[row_token[row]],
 // tmA a 64 × 1-box map over x): the permutation of [MoE 模型原理 §5] folded
 // into the first GEMM's operand load, the fused permutation/dispatch kernel
 // of [MoE Gate 分布式通信 mianshidashi, 06].  Every lane of warp 0 then
 // issues TMA gather4 copies of four rows each, while lane 0 still loads B.
-template <int ACT, bool PAIR, bool GATHER>
+template <int ACT, bool PAIR, bool GATHER, int CK>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    int E, int N, int K, int BN, const int32_t* __restrict__ offsets,
                    const float* __restrict__ bias, __nv_bfloat16* __restrict__ out,
                    int64_t max_rows, int32_t* status, int stages, int set,
-                   const int32_t* __restrict__ row_token, int64_t gx_rows) {
+                   const int32_t* __restrict__ row_token, int64_t gx_rows, CombineArgs cmb) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages];
   __shared__ uint64_t tfull_bar[2], tempty_bar[2], drain_bar;
@@ -499,6 +664,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::mbar_arrive(&tempty_bar[acc]);
       }
       if (++acc == 2) acc = 0, acc_phase ^= 1u;
+      if constexpr (CK > 0) {
+        const int c_end = min(c_hi, ncols);
+        if (c_lo < c_end)
+          combine_rows<CK>(c.m_end, c.n0, row0, lane, half, c_lo, c_end, N, BN, max_rows,
+                           row_token, out, cmb);
+      }
     }
   }
   tc::fence_before_sync();
@@ -563,14 +734,14 @@ struct Gather {
   int64_t gx_rows;
 };
 
-template <bool PAIR, bool GATHER>
+template <bool PAIR, bool GATHER, bool COMBINE>
 cudaError_t launch_variant(int act, const CUtensorMap& tmA, const CUtensorMap& tmB, int E, int N,
                            int K, int BN, const int32_t* offsets, const float* bias, void* out,
                            int64_t max_rows, int32_t* status, int set, const Gather& g,
-                           cudaStream_t st) {
+                           const CombineArgs& cmb, cudaStream_t st) {
   const int sms = device_sms();
-  const size_t static_smem =
-      kernel_static_smem(reinterpret_cast<const void*>(gemm_tc_kernel<kActNone, PAIR, false>));
+  const size_t static_smem = kernel_static_smem(
+      reinterpret_cast<const void*>(gemm_tc_kernel<kActNone, PAIR, false, 0>));
   // As many pipeline stages as fit beside the epilogue buffers and the
   // kernel's static shared memory.
   const int bn_cta = PAIR ? BN / 2 : BN;
@@ -614,44 +785,53 @@ cudaError_t launch_variant(int act, const CUtensorMap& tmA, const CUtensorMap& t
     cfg.numAttrs += 1;
     e = cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, E, N, K, BN, offsets, bias,
                            static_cast<__nv_bfloat16*>(out), max_rows, status, stages, set,
-                           g.row_token, g.gx_rows);
+                           g.row_token, g.gx_rows, cmb);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
   };
   if constexpr (GATHER) {
     // Only the first GEMM gathers, and it always has an activation.
-    return act == MOE_ACT_RELU        ? run(gemm_tc_kernel<MOE_ACT_RELU, PAIR, true>)
-           : act == MOE_ACT_GELU_TANH ? run(gemm_tc_kernel<MOE_ACT_GELU_TANH, PAIR, true>)
+    return act == MOE_ACT_RELU        ? run(gemm_tc_kernel<MOE_ACT_RELU, PAIR, true, 0>)
+           : act == MOE_ACT_GELU_TANH ? run(gemm_tc_kernel<MOE_ACT_GELU_TANH, PAIR, true, 0>)
                                       : cudaErrorInvalidValue;
+  } else if constexpr (COMBINE) {
+    // Only the second GEMM combines, and it has no activation; the combine
+    // holds up to 2, 4, 8 or 16 ranks per token.
+    if (act >= 0) return cudaErrorInvalidValue;
+    return cmb.k <= 2   ? run(gemm_tc_kernel<kActNone, PAIR, false, 2>)
+           : cmb.k <= 4 ? run(gemm_tc_kernel<kActNone, PAIR, false, 4>)
+           : cmb.k <= 8 ? run(gemm_tc_kernel<kActNone, PAIR, false, 8>)
+                        : run(gemm_tc_kernel<kActNone, PAIR, false, 16>);
   } else {
-    return act == MOE_ACT_RELU        ? run(gemm_tc_kernel<MOE_ACT_RELU, PAIR, false>)
-           : act == MOE_ACT_GELU_TANH ? run(gemm_tc_kernel<MOE_ACT_GELU_TANH, PAIR, false>)
-                                      : run(gemm_tc_kernel<kActNone, PAIR, false>);
+    return act == MOE_ACT_RELU        ? run(gemm_tc_kernel<MOE_ACT_RELU, PAIR, false, 0>)
+           : act == MOE_ACT_GELU_TANH ? run(gemm_tc_kernel<MOE_ACT_GELU_TANH, PAIR, false, 0>)
+                                      : run(gemm_tc_kernel<kActNone, PAIR, false, 0>);
   }
 }
 
-template <bool GATHER>
+template <bool GATHER, bool COMBINE>
 cudaError_t launch_sets(int act, const CUtensorMap& tmA, const CUtensorMap& tmB_cta,
                         const CUtensorMap* tmB_pair, int E, int N, int K, int BN,
                         const int32_t* offsets, const float* bias, void* out, int64_t max_rows,
-                        int32_t* status, const Gather& g, cudaStream_t st) {
+                        int32_t* status, const Gather& g, const CombineArgs& cmb,
+                        cudaStream_t st) {
   cudaError_t err;
   if (tmB_pair && E >= kTailSplitMinExperts) {
     // CTA pairs take every expert's whole 256-row tiles (and a last one with
     // more than 128 rows); one-CTA tiles take the remaining 1..128 rows, so
     // no pair computes a 128-row half that lies past its expert's end.
-    err = launch_variant<true, GATHER>(act, tmA, *tmB_pair, E, N, K, BN, offsets, bias, out,
-                                       max_rows, status, kPairBody, g, st);
+    err = launch_variant<true, GATHER, COMBINE>(act, tmA, *tmB_pair, E, N, K, BN, offsets, bias,
+                                                out, max_rows, status, kPairBody, g, cmb, st);
     if (err != cudaSuccess) return err;
     count_launch();
-    err = launch_variant<false, GATHER>(act, tmA, tmB_cta, E, N, K, BN, offsets, bias, out,
-                                        max_rows, status, kTail, g, st);
+    err = launch_variant<false, GATHER, COMBINE>(act, tmA, tmB_cta, E, N, K, BN, offsets, bias,
+                                                 out, max_rows, status, kTail, g, cmb, st);
   } else if (tmB_pair) {
-    err = launch_variant<true, GATHER>(act, tmA, *tmB_pair, E, N, K, BN, offsets, bias, out,
-                                       max_rows, status, kAllTiles, g, st);
+    err = launch_variant<true, GATHER, COMBINE>(act, tmA, *tmB_pair, E, N, K, BN, offsets, bias,
+                                                out, max_rows, status, kAllTiles, g, cmb, st);
   } else {
-    err = launch_variant<false, GATHER>(act, tmA, tmB_cta, E, N, K, BN, offsets, bias, out,
-                                        max_rows, status, kAllTiles, g, st);
+    err = launch_variant<false, GATHER, COMBINE>(act, tmA, tmB_cta, E, N, K, BN, offsets, bias,
+                                                 out, max_rows, status, kAllTiles, g, cmb, st);
   }
   if (err != cudaSuccess) return err;
   count_launch();
@@ -689,10 +869,11 @@ bool encode_b(EncodeTiledFn encode, CUtensorMap* m, const void* B, int E, int N,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool GATHER>
+template <bool GATHER, bool COMBINE>
 cudaError_t launch_gemm(int E, int N, int K, int64_t max_rows, const int32_t* offsets,
                         const void* A, int64_t a_rows, const void* B, const float* bias, int act,
-                        void* out, int32_t* status, const Gather& g, cudaStream_t st) {
+                        void* out, int32_t* status, const Gather& g, const CombineArgs& cmb,
+                        cudaStream_t st) {
   if (E > kMaxExperts) return cudaErrorInvalidValue;
   EncodeTiledFn encode = get_encode();
   if (!encode) return cudaErrorNotSupported;
@@ -702,8 +883,8 @@ cudaError_t launch_gemm(int E, int N, int K, int64_t max_rows, const int32_t* of
   if (!encode_b(encode, &tmB_cta, B, E, N, K, BN)) return cudaErrorInvalidValue;
   const bool pair = use_pair();
   if (pair && !encode_b(encode, &tmB_pair, B, E, N, K, BN / 2)) return cudaErrorInvalidValue;
-  return launch_sets<GATHER>(act, tmA, tmB_cta, pair ? &tmB_pair : nullptr, E, N, K, BN, offsets,
-                             bias, out, max_rows, status, g, st);
+  return launch_sets<GATHER, COMBINE>(act, tmA, tmB_cta, pair ? &tmB_pair : nullptr, E, N, K, BN,
+                                      offsets, bias, out, max_rows, status, g, cmb, st);
 }
 
 }  // namespace
@@ -712,8 +893,9 @@ cudaError_t launch_gemm_tc(int E, int N, int K, int64_t max_rows, const int32_t*
                            const void* A, const void* B, const float* bias, int act, void* out,
                            int32_t* status, cudaStream_t st) {
   const Gather none{nullptr, 0};
-  return launch_gemm<false>(E, N, K, max_rows, offsets, A, max_rows, B, bias, act, out, status,
-                            none, st);
+  const CombineArgs no_cmb{nullptr, nullptr, nullptr, nullptr, 0, 0};
+  return launch_gemm<false, false>(E, N, K, max_rows, offsets, A, max_rows, B, bias, act, out,
+                                   status, none, no_cmb, st);
 }
 
 cudaError_t launch_gemm_tc_gather(int E, int N, int K, int64_t max_rows, const int32_t* offsets,
@@ -722,7 +904,30 @@ cudaError_t launch_gemm_tc_gather(int E, int N, int K, int64_t max_rows, const i
                                   int32_t* status, cudaStream_t st) {
   if (act != MOE_ACT_RELU && act != MOE_ACT_GELU_TANH) return cudaErrorInvalidValue;
   const Gather g{row_token, T};
-  return launch_gemm<true>(E, N, K, max_rows, offsets, x, T, B, bias, act, out, status, g, st);
+  const CombineArgs no_cmb{nullptr, nullptr, nullptr, nullptr, 0, 0};
+  return launch_gemm<true, false>(E, N, K, max_rows, offsets, x, T, B, bias, act, out, status, g,
+                                  no_cmb, st);
+}
+
+int gemm_tc_bn(int N) { return pick_bn(N); }
+
+cudaError_t launch_gemm_tc_combine(int E, int N, int K, int64_t max_rows, const int32_t* offsets,
+                                   const void* A, const void* B, const float* bias, void* yd,
+                                   int64_t T, int k, const int32_t* row_token,
+                                   const int32_t* slot_row, const float* w, void* y, int* cnt,
+                                   int32_t* status, cudaStream_t st) {
+  if (N % 8 != 0) return cudaErrorInvalidValue;
+  const int BN = pick_bn(N);
+  const int per_token = 2 * ((N + BN - 1) / BN);
+  cudaError_t e = launch_pdl(combine_prep_kernel, dim3(unsigned((T + 255) / 256)), dim3(256), 0,
+                             st, T, k, per_token, max_rows, int64_t(N / 8), slot_row, cnt,
+                             static_cast<uint4*>(y));
+  count_launch();
+  if (e != cudaSuccess || (e = cudaGetLastError()) != cudaSuccess) return e;
+  const Gather g{row_token, 0};
+  const CombineArgs cmb{slot_row, w, static_cast<__nv_bfloat16*>(y), cnt, k, T};
+  return launch_gemm<false, true>(E, N, K, max_rows, offsets, A, max_rows, B, bias, -1, yd,
+                                  status, g, cmb, st);
 }
 
 }  // namespace moe

@@ -130,6 +130,17 @@ cudaError_t launch_gemm_tc_gather(int E, int N, int K, int64_t max_rows, const i
                                   const void* x, int64_t T, const int32_t* row_token,
                                   const void* B, const float* bias, int act, void* out,
                                   int32_t* status, cudaStream_t st);
+// The second GEMM with the combine folded into its epilogue:
+// yd[rows of e] = H W2[e]ᵀ + b2[e] as launch_gemm_tc, and
+// y[t] = Σ_r w[t,r]·yd[slot_row[t,r]] (kept slots, rank order, fp32; 0 if none)
+// by the last epilogue warp to finish a row of token t, per column range.
+// cnt: 2·ceil(N / gemm_tc_bn(N)) ints per token, zero on entry (left zero).
+int gemm_tc_bn(int N);
+cudaError_t launch_gemm_tc_combine(int E, int N, int K, int64_t max_rows, const int32_t* offsets,
+                                   const void* A, const void* B, const float* bias, void* yd,
+                                   int64_t T, int k, const int32_t* row_token,
+                                   const int32_t* slot_row, const float* w, void* y, int* cnt,
+                                   int32_t* status, cudaStream_t st);
 // The same GEMM with the operands' roles swapped (MMA M over weight rows, N
 // over an expert's rows), for layers where no expert holds more than
 // rows_per_expert_max <= 64 rows (gemm_swap_applies).

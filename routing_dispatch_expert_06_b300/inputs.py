@@ -71,6 +71,19 @@ WORKLOADS = {
                  "gelu_tanh", "bf16", 12, "zipf:0.8"),
         Workload("decode_bf16_t64_d2048_e64_top6", 64, 2048, 1408, 64, 6, 1.0, True,
                  "gelu_tanh", "bf16", 7, "zipf:0.8"),
+        # The largest layer's shapes (d = 7168, d_ff = 2048, top-8, N(0, 1)
+        # router bias) at 1/8 of its tokens and experts: the same capacity
+        # C = 1280 per expert, so the same per-expert row counts, on a few GB
+        # of device memory (for hardware-counter captures of its kernels).
+        Workload("bf16_t4096_d7168_e32_top8", 4096, 7168, 2048, 32, 8, 1.25, False,
+                 "gelu_tanh", "bf16", 13, "normal:1.0"),
+        # The largest layer's routing, dispatch and combine at full size (T =
+        # 32768, d = 7168, E = 256, top-8, same seed and router) with a
+        # narrow expert width d_ff = 64, so that the whole layer holds about
+        # 4 GB of device memory (for hardware-counter captures of those
+        # kernels; the expert GEMMs are not representative here).
+        Workload("narrow_bf16_t32768_d7168_e256_top8", 32768, 7168, 64, 256, 8, 1.25, False,
+                 "gelu_tanh", "bf16", 4, "normal:1.0"),
         # Dropless: c = E/k makes C = ceil(c·T·k/E) = T, so no expert can
         # overflow (every slot is kept).
         Workload("dropless_bf16_t8192_d2048_e64_top6", 8192, 2048, 1408, 64, 6, 64 / 6, True,

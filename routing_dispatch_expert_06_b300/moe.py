@@ -38,7 +38,7 @@ class Config(ctypes.Structure):
                 ("capacity_factor", ctypes.c_double), ("renormalize", ctypes.c_int32),
                 ("act", ctypes.c_int32), ("dtype", ctypes.c_int32),
                 ("write_logits", ctypes.c_int32), ("reroute", ctypes.c_int32),
-                ("fuse_dispatch", ctypes.c_int32)]
+                ("fuse_dispatch", ctypes.c_int32), ("fuse_combine", ctypes.c_int32)]
 
 
 _TENSOR_FIELDS = ["x", "Wr", "br", "W1", "b1", "W2", "b2", "logits", "topk_ids", "topk_w",
@@ -78,6 +78,7 @@ def load():
         "moe_ffn_up": (st, [cfgp, _P, _P, _P, _P, _P, _P, sz, _P]),
         "moe_ffn_up_gather": (st, [cfgp, _P, _P, _P, _P, _P, _P, _P, sz, _P]),
         "moe_ffn_down": (st, [cfgp, _P, _P, _P, _P, _P, _P, sz, _P]),
+        "moe_ffn_down_combine": (st, [cfgp, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, sz, _P]),
         "moe_expert_ffn": (st, [cfgp, _P, _P, _P, _P, _P, _P, _P, _P, _P, sz, _P]),
         "moe_combine": (st, [cfgp, _P, _P, _P, _P, _P]),
         "moe_aux_stats": (st, [cfgp, _P, _P, ctypes.c_float, _P, _P, _P, _P]),
@@ -124,18 +125,19 @@ def _stream(stream=None):
 
 
 def config(T, d, d_ff, E, k, capacity_factor, renormalize=True, act="gelu_tanh", dtype="bf16",
-           write_logits=False, reroute=False, fuse_dispatch=False) -> Config:
+           write_logits=False, reroute=False, fuse_dispatch=False, fuse_combine=False) -> Config:
     return Config(T=T, d=d, d_ff=d_ff, E=E, k=k, capacity_factor=float(capacity_factor),
                   renormalize=int(bool(renormalize)),
                   act=MOE_ACT_RELU if act == "relu" else MOE_ACT_GELU_TANH,
                   dtype=MOE_DT_BF16 if dtype == "bf16" else MOE_DT_F32,
                   write_logits=int(bool(write_logits)), reroute=int(bool(reroute)),
-                  fuse_dispatch=int(bool(fuse_dispatch)))
+                  fuse_dispatch=int(bool(fuse_dispatch)), fuse_combine=int(bool(fuse_combine)))
 
 
-def config_from_workload(wl, write_logits=False, reroute=False, fuse_dispatch=False) -> Config:
+def config_from_workload(wl, write_logits=False, reroute=False, fuse_dispatch=False,
+                         fuse_combine=False) -> Config:
     return config(wl.T, wl.d, wl.d_ff, wl.E, wl.k, wl.capacity_factor, wl.renormalize, wl.act,
-                  wl.dtype, write_logits, reroute, fuse_dispatch)
+                  wl.dtype, write_logits, reroute, fuse_dispatch, fuse_combine)
 
 
 def capacity(cfg: Config) -> int:
@@ -251,6 +253,14 @@ def ffn_down(cfg, H, offsets, W2, b2, yd, ws, stream=None):
                                _ptr(yd), _ptr(ws), ws.numel(), _stream(stream)))
 
 
+def ffn_down_combine(cfg, H, offsets, row_token, slot_row, topk_w, W2, b2, yd, y, ws,
+                     stream=None):
+    """moe_ffn_down_combine: the second GEMM with the combine in its epilogue."""
+    _check(load().moe_ffn_down_combine(ctypes.byref(cfg), _ptr(H), _ptr(offsets), _ptr(row_token),
+                                       _ptr(slot_row), _ptr(topk_w), _ptr(W2), _ptr(b2),
+                                       _ptr(yd), _ptr(y), _ptr(ws), ws.numel(), _stream(stream)))
+
+
 def expert_ffn(cfg, xd, offsets, W1, b1, W2, b2, H, yd, ws, stream=None):
     _check(load().moe_expert_ffn(ctypes.byref(cfg), _ptr(xd), _ptr(offsets), _ptr(W1), _ptr(b1),
                                  _ptr(W2), _ptr(b2), _ptr(H), _ptr(yd), _ptr(ws), ws.numel(),
@@ -306,9 +316,14 @@ def forward_stages(cfg, inputs: dict, out: dict, ws, alpha=0.01, stream=None, ev
     else:
         ffn_up(cfg, out["xd"], out["offsets"], inputs["W1"], inputs["b1"], out["H"], ws, s)
     mark(3)
-    ffn_down(cfg, out["H"], out["offsets"], inputs["W2"], inputs["b2"], out["yd"], ws, s)
+    if cfg.fuse_combine:
+        ffn_down_combine(cfg, out["H"], out["offsets"], out["row_token"], out["slot_row"],
+                         out["topk_w"], inputs["W2"], inputs["b2"], out["yd"], out["y"], ws, s)
+    else:
+        ffn_down(cfg, out["H"], out["offsets"], inputs["W2"], inputs["b2"], out["yd"], ws, s)
     mark(4)
-    combine(cfg, out["yd"], out["slot_row"], out["topk_w"], out["y"], s)
+    if not cfg.fuse_combine:
+        combine(cfg, out["yd"], out["slot_row"], out["topk_w"], out["y"], s)
     mark(5)
     aux_stats(cfg, out["counts"], out["psum"], alpha, out["f"], out["pbar"], out["l_aux"], s)
     if out.get("health") is not None:

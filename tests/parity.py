@@ -67,15 +67,16 @@ def assert_float(got, ref, dtype, what=""):
 
 
 def run_gpu(wl, inp=None, expert_bias=False, alpha=1.0, stages=False, health=False,
-            reroute=False, fuse_dispatch=False):
+            reroute=False, fuse_dispatch=False, fuse_combine=False):
     """Run the layer through the C ABI; return (cfg, inputs, outputs, ws).
     An ``inp["sel_bias"]`` routes with the selection-only bias; ``health``
     also asks for the routing-health indicators; ``fuse_dispatch`` runs the
-    first GEMM on gathered token rows (no xd)."""
+    first GEMM on gathered token rows (no xd); ``fuse_combine`` runs the
+    combine inside the second GEMM."""
     if inp is None:
         inp = inputs.make_inputs(wl, "cuda", expert_bias=expert_bias)
     cfg = moe.config_from_workload(wl, write_logits=True, reroute=reroute,
-                                   fuse_dispatch=fuse_dispatch)
+                                   fuse_dispatch=fuse_dispatch, fuse_combine=fuse_combine)
     ws = moe.workspace(cfg)
     out = moe.allocate(cfg, health=health)
     if stages:

@@ -187,3 +187,27 @@ def test_fuse_dispatch_host_checks(lib):
         setattr(t, name, 1 << 20)
     assert lib.moe_forward(ctypes.byref(f32), ctypes.byref(t), ctypes.c_float(1.0), p, 1 << 30,
                            None) == moe.MOE_ERR_UNSUPPORTED
+
+
+def test_fuse_combine_flag_scope_and_counters(lib):
+    # fuse_combine must be 0 or 1; it adds 2 int32 counters per token and
+    # 256-wide column tile of d to the workspace; moe_ffn_down_combine refuses
+    # NULL tensors, a config without the flag (no counters) and the layers the
+    # tensor-core GEMM does not run (fp32, at most 64 rows per expert), all
+    # before any launch (the placeholder pointers are never dereferenced).
+    bad = cfg_for(64, 64, 64, 8, 2, 1.0)
+    bad.fuse_combine = 2
+    n = ctypes.c_size_t(0)
+    assert lib.moe_workspace_size(ctypes.byref(bad), ctypes.byref(n)) == moe.MOE_ERR_INVALID_ARG
+    plain = cfg_for(32768, 7168, 2048, 256, 8, 1.25)
+    fused = cfg_for(32768, 7168, 2048, 256, 8, 1.25, fuse_combine=True)
+    assert moe.workspace_size(fused) - moe.workspace_size(plain) >= 32768 * 2 * 28 * 4
+    p = ctypes.c_void_p(1 << 20)
+    args = [p] * 9 + [p, 1 << 30, None]
+    assert lib.moe_ffn_down_combine(ctypes.byref(fused), *([None] * 9), p, 1 << 30,
+                                    None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_ffn_down_combine(ctypes.byref(plain), *args) == moe.MOE_ERR_INVALID_ARG
+    f32 = cfg_for(4096, 1024, 4096, 8, 2, 1.25, dtype="f32", fuse_combine=True)
+    dec = cfg_for(8, 2048, 1408, 64, 6, 1.0, fuse_combine=True)
+    for cfg in (f32, dec):
+        assert lib.moe_ffn_down_combine(ctypes.byref(cfg), *args) == moe.MOE_ERR_UNSUPPORTED
