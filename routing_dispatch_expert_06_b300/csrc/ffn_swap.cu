@@ -57,13 +57,17 @@ __device__ __forceinline__ float epi_act(float u) {
   return u;
 }
 
+// expert_max: only experts holding 1 .. expert_max rows are computed (the
+// others are left to the regular kernel); every expert with rows when it is
+// at least NT.  Each tile's MMA is as wide as its expert's rows rounded up to
+// 16 (at most NT), so a 3-row expert costs a 16-wide MMA.
 template <int ACT, int NT>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_swap_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB, int E, int N, int K,
                      const int32_t* __restrict__ offsets, const float* __restrict__ bias,
                      __nv_bfloat16* __restrict__ out, int64_t max_rows, int32_t* status,
-                     int stages) {
+                     int stages, int expert_max) {
   constexpr uint32_t kTmemCols = 2 * NT < 32 ? 32 : 2 * NT;  // two accumulators
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages];
@@ -104,8 +108,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // from the previous kernels.
   tc::grid_dependency_wait();
   tc::grid_launch_dependents();
-  // Prefix over experts of "has rows": warp 0 scans runs of experts, one run
-  // per lane.  Offsets are clamped to [0, max_rows].
+  // Prefix over experts with 1 .. expert_max rows: warp 0 scans runs of
+  // experts, one run per lane.  Offsets are clamped to [0, max_rows].
   if (warp == 0) {
     auto clamp_row = [&](int e) {
       const int32_t v = offsets[e];
@@ -114,10 +118,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int per = (E + 31) / 32;
     const int lo = lane * per, hi = min(E, lo + per);
     int run = 0;
+    auto takes = [&](int32_t a, int32_t b) { return b > a && b - a <= expert_max; };
     for (int e = lo; e < hi; ++e) {
       const int32_t a = clamp_row(e), b = clamp_row(e + 1);
       s_off[e] = a;
-      run += b > a ? 1 : 0;
+      run += takes(a, b) ? 1 : 0;
     }
     if (lane == 31) s_off[E] = clamp_row(E);
     int incl = run;
@@ -129,7 +134,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = incl - run;
     for (int e = lo; e < hi; ++e) {
       s_tp[e] = acc;
-      acc += clamp_row(e + 1) > clamp_row(e) ? 1 : 0;
+      acc += takes(clamp_row(e), clamp_row(e + 1)) ? 1 : 0;
     }
     if (lane == 31) s_tp[E] = incl;
   }
@@ -189,7 +194,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_wait(&full_bar[j % stages], uint32_t((j / stages) & 1), nullptr, kWaitLimitNs);
   } else if (warp == 1 && lane == 0) {
     // ---------------- MMA issuer ----------------
-    const uint32_t idesc = tc::idesc_bf16_f32(kTileN, NT);
     int stage = 0;
     uint32_t phase = 0;
     int acc = 0;
@@ -202,6 +206,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc::fence_after_sync();
       const uint32_t d_tmem = tmem_base + uint32_t(acc * NT);
+      int e, n0;
+      tile_expert(i, e, n0);
+      const int rows = s_off[e + 1] - s_off[e];
+      const int n_mma = rows >= NT ? NT : ((rows + 15) / 16) * 16;
+      const uint32_t idesc = tc::idesc_bf16_f32(kTileN, n_mma < 16 ? 16 : n_mma);
       for (int kb = 0; kb < nk; ++kb) {
         if (!tc::mbar_wait(&full_bar[stage], phase, abort_flag, kWaitLimitNs)) {
           give_up();
@@ -249,6 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t t_lane = tmem_base + (uint32_t(quarter * 32) << 16) + uint32_t(acc * NT);
 #pragma unroll
       for (int c0 = 0; c0 < NT; c0 += 16) {
+        if (c0 >= rows) break;  // columns past the expert's rows were not computed
         uint32_t r[16];
         tc::tmem_ld_x16(t_lane + uint32_t(c0), r);
         tc::tmem_ld_wait();
@@ -294,7 +304,7 @@ EncodeTiledFn get_encode() {
 template <int ACT, int NT>
 cudaError_t launch_nt(const CUtensorMap& tmA, const CUtensorMap& tmB, int E, int N, int K,
                       const int32_t* offsets, const float* bias, void* out, int64_t max_rows,
-                      int32_t* status, cudaStream_t st) {
+                      int32_t* status, int expert_max, int grid, cudaStream_t st) {
   auto kernel = gemm_swap_kernel<ACT, NT>;
   const void* kp = reinterpret_cast<const void*>(kernel);
   const size_t stage_bytes = size_t(kTileN) * kTileK * 2 + size_t(NT) * kTileK * 2;
@@ -305,26 +315,54 @@ cudaError_t launch_nt(const CUtensorMap& tmA, const CUtensorMap& tmB, int E, int
   const size_t smem = 1024 + size_t(stages) * stage_bytes;
   cudaError_t err = ensure_dynamic_smem(kp, smem);
   if (err != cudaSuccess) return err;
-  err = launch_pdl(kernel, dim3(unsigned(device_sms())), dim3(kThreads), smem, st, tmA, tmB, E,
-                   N, K, offsets, bias, static_cast<__nv_bfloat16*>(out), max_rows, status,
-                   stages);
+  err = launch_pdl(kernel, dim3(unsigned(grid)), dim3(kThreads), smem, st, tmA, tmB, E, N, K,
+                   offsets, bias, static_cast<__nv_bfloat16*>(out), max_rows, status, stages,
+                   expert_max);
   return err != cudaSuccess ? err : cudaGetLastError();
 }
 
 template <int NT>
 cudaError_t launch_act(int act, const CUtensorMap& tmA, const CUtensorMap& tmB, int E, int N,
                        int K, const int32_t* offsets, const float* bias, void* out,
-                       int64_t max_rows, int32_t* status, cudaStream_t st) {
+                       int64_t max_rows, int32_t* status, int expert_max, int grid,
+                       cudaStream_t st) {
   switch (act) {
     case MOE_ACT_RELU:
       return launch_nt<MOE_ACT_RELU, NT>(tmA, tmB, E, N, K, offsets, bias, out, max_rows, status,
-                                         st);
+                                         expert_max, grid, st);
     case MOE_ACT_GELU_TANH:
       return launch_nt<MOE_ACT_GELU_TANH, NT>(tmA, tmB, E, N, K, offsets, bias, out, max_rows,
-                                              status, st);
+                                              status, expert_max, grid, st);
     default:
-      return launch_nt<-1, NT>(tmA, tmB, E, N, K, offsets, bias, out, max_rows, status, st);
+      return launch_nt<-1, NT>(tmA, tmB, E, N, K, offsets, bias, out, max_rows, status,
+                               expert_max, grid, st);
   }
+}
+
+// Tensor maps of the swapped kernel: NT-row boxes over A [max_rows, K],
+// 128-row boxes over B [E, N, K].
+bool encode_maps(CUtensorMap* tmA, CUtensorMap* tmB, int E, int N, int K, int64_t max_rows,
+                 const void* A, const void* B, int NT) {
+  EncodeTiledFn encode = get_encode();
+  if (!encode) return false;
+  const cuuint32_t es[3] = {1, 1, 1};
+  {
+    const cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(max_rows)};
+    const cuuint64_t strides[1] = {cuuint64_t(K) * 2};
+    const cuuint32_t box[2] = {kTileK, cuuint32_t(NT)};
+    if (encode(tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(A), dims, strides, box,
+               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  }
+  const cuuint64_t dims[3] = {cuuint64_t(K), cuuint64_t(N), cuuint64_t(E)};
+  const cuuint64_t strides[2] = {cuuint64_t(K) * 2, cuuint64_t(N) * K * 2};
+  const cuuint32_t box[3] = {kTileK, kTileN, 1};
+  return encode(tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(B), dims, strides,
+                box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -343,38 +381,21 @@ cudaError_t launch_gemm_swap(int E, int N, int K, int64_t max_rows, int64_t rows
                              cudaStream_t st) {
   if (E > kMaxExperts || rows_per_expert_max < 1 || rows_per_expert_max > kMaxSwapRows)
     return cudaErrorInvalidValue;
-  EncodeTiledFn encode = get_encode();
-  if (!encode) return cudaErrorNotSupported;
   const int NT = rows_per_expert_max <= 16 ? 16 : rows_per_expert_max <= 32 ? 32 : 64;
-  const cuuint32_t es[3] = {1, 1, 1};
   CUtensorMap tmA, tmB;
-  {
-    const cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(max_rows)};
-    const cuuint64_t strides[1] = {cuuint64_t(K) * 2};
-    const cuuint32_t box[2] = {kTileK, cuuint32_t(NT)};
-    if (encode(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(A), dims, strides, box,
-               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
-  {
-    const cuuint64_t dims[3] = {cuuint64_t(K), cuuint64_t(N), cuuint64_t(E)};
-    const cuuint64_t strides[2] = {cuuint64_t(K) * 2, cuuint64_t(N) * K * 2};
-    const cuuint32_t box[3] = {kTileK, kTileN, 1};
-    if (encode(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(B), dims, strides, box,
-               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
+  if (!encode_maps(&tmA, &tmB, E, N, K, max_rows, A, B, NT)) return cudaErrorInvalidValue;
+  const int grid = device_sms();
+  const int all = int(rows_per_expert_max);
   cudaError_t err;
   if (NT == 16)
-    err = launch_act<16>(act, tmA, tmB, E, N, K, offsets, bias, out, max_rows, status, st);
+    err = launch_act<16>(act, tmA, tmB, E, N, K, offsets, bias, out, max_rows, status, all, grid,
+                         st);
   else if (NT == 32)
-    err = launch_act<32>(act, tmA, tmB, E, N, K, offsets, bias, out, max_rows, status, st);
+    err = launch_act<32>(act, tmA, tmB, E, N, K, offsets, bias, out, max_rows, status, all, grid,
+                         st);
   else
-    err = launch_act<64>(act, tmA, tmB, E, N, K, offsets, bias, out, max_rows, status, st);
+    err = launch_act<64>(act, tmA, tmB, E, N, K, offsets, bias, out, max_rows, status, all, grid,
+                         st);
   count_launch();
   return err;
 }
