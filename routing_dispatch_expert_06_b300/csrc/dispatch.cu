@@ -18,7 +18,8 @@
 //      block to finish when a completion counter is given, else by a
 //      separate kernel
 //   3. per chunk: expert offsets (scan of kept), per-warp bases, then each
-//      warp walks its 32 tokens in order: slot_row, row_token
+//      warp walks the slots of its 32 tokens in (token, rank) order, 32 slots
+//      per step: slot_row, row_token
 // and a fourth, bandwidth-bound pass copies each token row once from x and
 // writes it to every kept slot with 16-byte vectors.
 #include "common.cuh"
@@ -257,22 +258,27 @@ __device__ __forceinline__ void assign_body(int64_t T, int E, int k, int64_t C,
     }
   }
   __syncthreads();
-  // Walk the warp's tokens in order; lane r handles rank r of the token.
-  // Ranks of one token that name the same expert (possible only with ids a
-  // caller passes in) are separate slots: they take consecutive positions in
-  // rank order, the lanes of a group found with match.any.
+  // Walk the warp's slots in (token, rank) order, 32 at a time: warp w owns
+  // the slots of its 32 tokens, s = t·k + r, so step i takes slots
+  // 32·w·k + 32·i + lane (k steps).  A slot's position is its expert's count
+  // so far (my[e]) plus the number of earlier lanes of the step with the same
+  // expert (match.any groups; this also covers a token naming one expert at
+  // two ranks), and the group's first lane advances my[e] by the group size.
   int32_t* my = wbase + warp * E;
-  for (int j = 0; j < 32; ++j) {
-    const int64_t t = chunk0 + warp * 32 + j;
-    if (t >= T) break;
-    const int e = lane < k ? s_ids[(warp * 32 + j) * k + lane] : -1;
+  const int64_t chunk_slots = (T - chunk0 < kChunkTokens ? T - chunk0 : kChunkTokens) * k;
+  for (int it = 0; it < k; ++it) {
+    const int64_t ls = int64_t(warp) * 32 * k + int64_t(it) * 32 + lane;  // slot within chunk
+    const bool in = ls < chunk_slots;
+    const int e = in ? s_ids[ls] : -1;
     const bool valid = e >= 0 && e < E;
     const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : E + lane);
     const int32_t before = __popc(peers & ((1u << lane) - 1u));
     const int32_t base = valid ? my[e] : 0;
     __syncwarp();
     if (valid && before == 0) my[e] = base + __popc(peers);
-    if (lane < k) {
+    __syncwarp();
+    if (in) {
+      const int64_t s_glob = chunk0 * k + ls;
       int32_t row = -1;
       if (valid) {
         const int32_t pos = base + before;
@@ -280,12 +286,11 @@ __device__ __forceinline__ void assign_body(int64_t T, int E, int k, int64_t C,
           row = pos < off[e] ? pos : -1;  // off[e] holds the capacity here
         } else if (pos < C) {
           row = off[e] + pos;
-          row_token[row] = int32_t(t);
+          row_token[row] = int32_t(s_glob / k);
         }
       }
-      slot_row[t * k + lane] = row;
+      slot_row[s_glob] = row;
     }
-    __syncwarp();
   }
 }
 
