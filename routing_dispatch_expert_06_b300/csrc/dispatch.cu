@@ -36,15 +36,14 @@ static_assert(kDispatchThreads == kAuxThreads, "the last histogram block runs th
 // round into the room C - cap_base[e] left by the first), kept =
 // cap_base[e] + min(count, C - cap_base[e]).  A group of tpe lanes (a power
 // of two, as many as the block holds for E experts, at most 32) scans one
-// expert; each lane loads 8 consecutive chunk counts at once, so an expert's
-// n_chunks take ceil(n_chunks / (8·tpe)) rounds of overlapping loads.
-__device__ void scan_chunks_by_expert(int64_t n_chunks, int E, int64_t C,
-                                      int32_t* __restrict__ chunk_counts,
-                                      int32_t* __restrict__ counts, int32_t* __restrict__ kept,
-                                      const int32_t* __restrict__ cap_base) {
-  constexpr int U = 8;
-  int tpe = 32;
-  while (tpe > 1 && tpe * E > int(blockDim.x)) tpe >>= 1;
+// expert; each lane loads U consecutive chunk counts at once (U = 8, or 32
+// when a group has fewer than 4 lanes, i.e. many experts), so an expert's
+// n_chunks take ceil(n_chunks / (U·tpe)) rounds of overlapping loads.
+template <int U>
+__device__ void scan_chunks_rounds(int64_t n_chunks, int E, int64_t C, int tpe,
+                                   int32_t* __restrict__ chunk_counts,
+                                   int32_t* __restrict__ counts, int32_t* __restrict__ kept,
+                                   const int32_t* __restrict__ cap_base) {
   const int lane = threadIdx.x & 31;
   const int sub = lane & (tpe - 1);
   const int group = threadIdx.x / tpe;
@@ -82,6 +81,18 @@ __device__ void scan_chunks_by_expert(int64_t n_chunks, int E, int64_t C,
       kept[e] = base + int32_t(carry < room ? carry : room);
     }
   }
+}
+
+__device__ void scan_chunks_by_expert(int64_t n_chunks, int E, int64_t C,
+                                      int32_t* __restrict__ chunk_counts,
+                                      int32_t* __restrict__ counts, int32_t* __restrict__ kept,
+                                      const int32_t* __restrict__ cap_base) {
+  int tpe = 32;
+  while (tpe > 1 && tpe * E > int(blockDim.x)) tpe >>= 1;
+  if (tpe >= 4)
+    scan_chunks_rounds<8>(n_chunks, E, C, tpe, chunk_counts, counts, kept, cap_base);
+  else
+    scan_chunks_rounds<32>(n_chunks, E, C, tpe, chunk_counts, counts, kept, cap_base);
 }
 
 // Histogram of one chunk; with a completion counter, the last block to
