@@ -214,3 +214,83 @@ def test_selection_bias_ties_go_to_lower_index(impl):
     out = _route_sel(wl, inp, impl, sb)
     assert (h(out["topk_ids"]) == np.array([1, 2, 4, 7, 8], np.int32)).all()
     np.testing.assert_allclose(h(out["topk_w"]), 0.2, rtol=1e-6)
+
+
+# With 75 or more 128-token tiles each CTA of the tensor-core router reduces a
+# whole tile (one split over d), so the selection kernel reads one partial per
+# token.  Every lane layout of the selection at that size: E <= 8 (8 lanes per
+# token), <= 16, <= 32, 64 (2 columns per lane), 100 (4), 130 and 256 (8); a
+# ragged last tile, d not a multiple of 64, k = 12 = E and k = 16.
+ONE_SPLIT_CASES = [
+    (9601, 520, 256, 16, False, "normal:1.0"),
+    (12000, 1024, 8, 2, True, "zero"),
+    (9500, 136, 12, 12, True, "zipf:0.8"),
+    (10000, 200, 20, 3, True, "normal:1.0"),
+    (9999, 2048, 64, 6, True, "zipf:0.8"),
+    (9700, 256, 100, 4, False, "normal:1.0"),
+    (9700, 256, 130, 5, True, "normal:1.0"),
+]
+
+
+@pytest.mark.parametrize("case", ONE_SPLIT_CASES,
+                         ids=lambda c: f"t{c[0]}_d{c[1]}_e{c[2]}_k{c[3]}")
+def test_one_split_router_matches_oracle(case):
+    wl = _workload(*case)
+    inp = inputs.make_inputs(wl, "cuda")
+    _check(wl, inp, _route(wl, inp, "tc"))
+
+
+@pytest.mark.parametrize("case", [(9601, 520, 256, 8, False), (12000, 512, 8, 2, True),
+                                  (9999, 1024, 64, 6, True)],
+                         ids=lambda c: f"t{c[0]}_e{c[2]}_k{c[3]}")
+def test_one_split_router_with_selection_bias(case):
+    T, d, E, k, renorm = case
+    wl = _workload(T, d, E, k, renorm, "normal:1.0", seed=13)
+    inp = inputs.make_inputs(wl, "cuda")
+    sb = torch.randn(E, generator=torch.Generator("cuda").manual_seed(7), device="cuda") * 1.5
+    out = _route_sel(wl, inp, "tc", sb)
+    logits = h(out["logits"])
+    ids, w, psum, _ = oracle.select(logits, k, renorm, sel_bias=h(sb))
+    np.testing.assert_array_equal(h(out["topk_ids"]), ids, "topk_ids")
+    assert_rel_rms(h(out["topk_w"]), w, 1e-4, "topk_w")
+    assert_rel_rms(h(out["psum"]), psum, 1e-4, "psum")
+    plain, *_ = oracle.select(logits, k, renorm)
+    assert (plain != ids).any(axis=1).mean() > 0.1
+
+
+def test_one_split_router_breaks_ties_by_lower_index():
+    T, d, E, k = 9700, 128, 24, 5
+    wl = _workload(T, d, E, k, True, "zero")
+    inp = inputs.make_inputs(wl, "cuda")
+    inp["Wr"].zero_()
+    inp["br"].copy_(torch.tensor([0.5, 1.0, 1.0, 0.25, 1.0, 0.5] * 4, device="cuda"))
+    out = _route(wl, inp, "tc")
+    assert (h(out["topk_ids"]) == np.array([1, 2, 4, 7, 8], np.int32)).all()
+    np.testing.assert_allclose(h(out["topk_w"]), 0.2, rtol=1e-6)
+    _check(wl, inp, out)
+
+
+def test_one_split_router_repeats_column_sums_exactly():
+    # Integer column sums give the same bits on every call, and the whole
+    # layer (which converts them in the dispatch) agrees; ids repeat too.
+    wl = inputs.Workload("psum_fused", 10000, 512, 64, 64, 6, 1.0, True, "gelu_tanh", "bf16", 3,
+                         "normal:1.0")
+    inp = inputs.make_inputs(wl, "cuda")
+    cfg = moe.config_from_workload(wl)
+    ws = moe.workspace(cfg)
+    out = moe.allocate(cfg)
+    runs = []
+    for _ in range(3):
+        moe.route(cfg, inp["x"], inp["Wr"], inp["br"], out, ws)
+        torch.cuda.synchronize()
+        runs.append((h(out["psum"]).copy(), h(out["topk_ids"]).copy()))
+    assert moe.device_status(ws) == moe.MOE_OK
+    for p, i in runs[1:]:
+        np.testing.assert_array_equal(p.view(np.uint32), runs[0][0].view(np.uint32))
+        np.testing.assert_array_equal(i, runs[0][1])
+    moe.forward(cfg, inp, out, ws, 0.01)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(h(out["psum"]).view(np.uint32), runs[0][0].view(np.uint32))
+    ref_logits = oracle.router_logits(h(inp["x"]), h(inp["Wr"]), h(inp["br"]))
+    _, _, psum, _ = oracle.select(ref_logits, wl.k, True)
+    assert_rel_rms(runs[0][0], psum, 1e-4, "psum")
