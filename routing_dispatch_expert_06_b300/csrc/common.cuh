@@ -85,14 +85,24 @@ __device__ __forceinline__ void sum_partials_rows(int64_t nblk, int E, const flo
 // wherever the routine runs (the stand-alone statistics kernel, or the last
 // histogram block of a forward pass).  red: kAuxThreads floats of shared memory.
 constexpr int kAuxThreads = 256;
+// Statistics inputs: from L2 (written by other blocks), or (SHARED) from this
+// block's shared memory.
+template <bool SHARED, typename V>
+__device__ __forceinline__ V ld_stat(const V* p) {
+  if constexpr (SHARED)
+    return *p;
+  else
+    return __ldcg(p);
+}
+template <bool SHARED = false>
 __device__ __forceinline__ void aux_stats_block(int E, int64_t T, float alpha,
                                                 const int32_t* counts, const float* psum,
                                                 float* f, float* pbar, float* l_aux, float* red) {
   const int j = threadIdx.x;
   float prod = 0.f;
   for (int e = j; e < E; e += kAuxThreads) {
-    const float fi = float(__ldcg(counts + e)) / float(T);
-    const float pi = __ldcg(psum + e) / float(T);
+    const float fi = float(ld_stat<SHARED>(counts + e)) / float(T);
+    const float pi = ld_stat<SHARED>(psum + e) / float(T);
     f[e] = fi;
     pbar[e] = pi;
     prod = __fadd_rn(prod, __fmul_rn(fi, pi));
@@ -140,6 +150,7 @@ __device__ __forceinline__ float block_sum_fixed(float v, float* red) {
 //   health[0] = -Σ q ln q, q_i = counts_i/(T·k)   health[1] = var(counts)
 //   health[2] = var(kept)                          health[3] = 1 - Σkept/(T·k)
 // (population variances over the E experts).  Σ kept is an exact integer sum.
+template <bool SHARED = false>
 __device__ __forceinline__ void routing_health_block(int E, int64_t T, int k,
                                                      const int32_t* counts, const int32_t* kept,
                                                      float* health, float* red,
@@ -152,12 +163,12 @@ __device__ __forceinline__ void routing_health_block(int E, int64_t T, int k,
   float h = 0.f, vc = 0.f;
   unsigned long long ks = 0ull;
   for (int e = j; e < E; e += kAuxThreads) {
-    const int32_t c = __ldcg(counts + e);
+    const int32_t c = ld_stat<SHARED>(counts + e);
     const float q = float(double(c) / n);
     if (q > 0.f) h = __fadd_rn(h, -__fmul_rn(q, logf(q)));
     const float dc = float(c) - mc;
     vc = __fadd_rn(vc, __fmul_rn(dc, dc));
-    ks += unsigned(__ldcg(kept + e));
+    ks += unsigned(ld_stat<SHARED>(kept + e));
   }
   atomicAdd(s_kept, ks);
   h = block_sum_fixed(h, red);
@@ -166,7 +177,7 @@ __device__ __forceinline__ void routing_health_block(int E, int64_t T, int k,
   const float mk = float(double(kept_sum) / double(E));
   float vk = 0.f;
   for (int e = j; e < E; e += kAuxThreads) {
-    const float dk = float(__ldcg(kept + e)) - mk;
+    const float dk = float(ld_stat<SHARED>(kept + e)) - mk;
     vk = __fadd_rn(vk, __fmul_rn(dk, dk));
   }
   vk = block_sum_fixed(vk, red);

@@ -218,6 +218,48 @@ __device__ __forceinline__ void block_exclusive_scan(int E, const int32_t* __res
   __syncthreads();
 }
 
+// Walk warp w's slots of the chunk starting at token chunk0 in (token, rank)
+// order, 32 at a time: warp w owns the slots of its 32 tokens, s = t·k + r,
+// so step i takes slots 32·w·k + 32·i + lane (k steps).  A slot's position is
+// its expert's count so far (my[e], the warp's base on entry) plus the number
+// of earlier lanes of the step with the same expert (match.any groups; this
+// also covers a token naming one expert at two ranks), and the group's first
+// lane advances my[e] by the group size.  off: expert offsets (positions_only:
+// the per-expert capacity).
+__device__ __forceinline__ void walk_slots(int64_t T, int E, int k, int64_t C, int64_t chunk0,
+                                           const int32_t* s_ids, int32_t* my, const int32_t* off,
+                                           int32_t* __restrict__ slot_row,
+                                           int32_t* __restrict__ row_token, int positions_only) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t chunk_slots = (T - chunk0 < kChunkTokens ? T - chunk0 : kChunkTokens) * k;
+  for (int it = 0; it < k; ++it) {
+    const int64_t ls = int64_t(warp) * 32 * k + int64_t(it) * 32 + lane;  // slot within chunk
+    const bool in = ls < chunk_slots;
+    const int e = in ? s_ids[ls] : -1;
+    const bool valid = e >= 0 && e < E;
+    const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : E + lane);
+    const int32_t before = __popc(peers & ((1u << lane) - 1u));
+    const int32_t base = valid ? my[e] : 0;
+    __syncwarp();
+    if (valid && before == 0) my[e] = base + __popc(peers);
+    __syncwarp();
+    if (in) {
+      const int64_t s_glob = chunk0 * k + ls;
+      int32_t row = -1;
+      if (valid) {
+        const int32_t pos = base + before;
+        if (positions_only) {
+          row = pos < off[e] ? pos : -1;  // off[e] holds the capacity here
+        } else if (pos < C) {
+          row = off[e] + pos;
+          row_token[row] = int32_t(s_glob / k);
+        }
+      }
+      slot_row[s_glob] = row;
+    }
+  }
+}
+
 __device__ __forceinline__ void assign_body(int64_t T, int E, int k, int64_t C,
                                             const int32_t* __restrict__ ids,
                                             const int32_t* __restrict__ chunk_base,
@@ -230,7 +272,7 @@ __device__ __forceinline__ void assign_body(int64_t T, int E, int k, int64_t C,
   int32_t* wbase = sm + E + 1;             // [8][E]
   int32_t* s_ids = wbase + 8 * E;          // [256·k]
   __shared__ int32_t part[kDispatchThreads];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5;
   const int64_t chunk0 = int64_t(blockIdx.x) * kChunkTokens;
   {
     // The chunk's ids, coalesced, once.
@@ -269,40 +311,8 @@ __device__ __forceinline__ void assign_body(int64_t T, int E, int k, int64_t C,
     }
   }
   __syncthreads();
-  // Walk the warp's slots in (token, rank) order, 32 at a time: warp w owns
-  // the slots of its 32 tokens, s = t·k + r, so step i takes slots
-  // 32·w·k + 32·i + lane (k steps).  A slot's position is its expert's count
-  // so far (my[e]) plus the number of earlier lanes of the step with the same
-  // expert (match.any groups; this also covers a token naming one expert at
-  // two ranks), and the group's first lane advances my[e] by the group size.
-  int32_t* my = wbase + warp * E;
-  const int64_t chunk_slots = (T - chunk0 < kChunkTokens ? T - chunk0 : kChunkTokens) * k;
-  for (int it = 0; it < k; ++it) {
-    const int64_t ls = int64_t(warp) * 32 * k + int64_t(it) * 32 + lane;  // slot within chunk
-    const bool in = ls < chunk_slots;
-    const int e = in ? s_ids[ls] : -1;
-    const bool valid = e >= 0 && e < E;
-    const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : E + lane);
-    const int32_t before = __popc(peers & ((1u << lane) - 1u));
-    const int32_t base = valid ? my[e] : 0;
-    __syncwarp();
-    if (valid && before == 0) my[e] = base + __popc(peers);
-    __syncwarp();
-    if (in) {
-      const int64_t s_glob = chunk0 * k + ls;
-      int32_t row = -1;
-      if (valid) {
-        const int32_t pos = base + before;
-        if (positions_only) {
-          row = pos < off[e] ? pos : -1;  // off[e] holds the capacity here
-        } else if (pos < C) {
-          row = off[e] + pos;
-          row_token[row] = int32_t(s_glob / k);
-        }
-      }
-      slot_row[s_glob] = row;
-    }
-  }
+  walk_slots(T, E, k, C, chunk0, s_ids, wbase + warp * E, off, slot_row, row_token,
+             positions_only);
 }
 
 __global__ void __launch_bounds__(kDispatchThreads)
@@ -318,24 +328,91 @@ __global__ void __launch_bounds__(kDispatchThreads)
               cap_base, sm);
 }
 
-// A call with a single chunk (T <= 256, e.g. a decode step): histogram, scan,
-// statistics and positions in one block, so one launch instead of two.  The
-// block's own global writes (chunk base, counts, kept) are visible to it
-// after the barrier.
+// A call with a single chunk (T <= 256, e.g. a decode step): one block does
+// the whole dispatch from shared memory — ids, the warps' histograms (whose
+// sum is counts and whose prefix over warps gives each warp's base; the
+// single chunk's base is 0), kept, offsets, the statistics and the positions
+// — so its only global round trips are the loads of ids and of the router's
+// fixed-point column sums (issued together) and the stores.  Dynamic shared
+// memory: off[E+1] | wbase[8][E] | ids[256·k] | counts[E] | kept[E] | psum[E].
 __global__ void __launch_bounds__(kDispatchThreads)
-    dispatch_one_chunk_kernel(int64_t T, int E, int k, int64_t C,
-                              const int32_t* __restrict__ ids, int32_t* __restrict__ chunk_counts,
-                              int32_t* status, int* counter, int32_t* __restrict__ counts,
-                              int32_t* __restrict__ kept, AuxArgs aux,
-                              int32_t* __restrict__ offsets, int32_t* __restrict__ slot_row,
-                              int32_t* __restrict__ row_token) {
+    dispatch_small_kernel(int64_t T, int E, int k, int64_t C, const int32_t* __restrict__ ids,
+                          int32_t* status, int32_t* __restrict__ counts,
+                          int32_t* __restrict__ kept, AuxArgs aux,
+                          int32_t* __restrict__ offsets, int32_t* __restrict__ slot_row,
+                          int32_t* __restrict__ row_token) {
   extern __shared__ int32_t sm[];
+  int32_t* off = sm;                                   // [E+1]
+  int32_t* wbase = off + E + 1;                        // [8][E]
+  int32_t* s_ids = wbase + 8 * E;                      // [256·k]
+  int32_t* s_cnt = s_ids + kChunkTokens * k;           // [E]
+  int32_t* s_kept = s_cnt + E;                         // [E]
+  float* s_psum = reinterpret_cast<float*>(s_kept + E);  // [E]
+  __shared__ int32_t part[kDispatchThreads];
+  __shared__ float s_red[kAuxThreads];
+  __shared__ unsigned long long s_kept_sum;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  for (int i = tid; i < 8 * E; i += kDispatchThreads) wbase[i] = 0;
   pdl_wait();
   pdl_trigger();
-  histogram_body(T, E, k, ids, chunk_counts, status, counter, C, counts, kept, aux, 0, nullptr,
-                 sm);
+  const int64_t n_ids = T * k;
+  for (int64_t i = tid; i < n_ids; i += kDispatchThreads) s_ids[i] = ids[i];
+  if (aux.f) {
+    // psum from the router's fixed-point column sums (as psum_from_fixed,
+    // with every copy's load issued before the first add), else as given.
+    for (int c = tid; c < E; c += kDispatchThreads) {
+      float p;
+      if (aux.psum_fixed) {
+        unsigned long long v[kPsumReplicas];
+#pragma unroll
+        for (int r = 0; r < kPsumReplicas; ++r) v[r] = __ldcg(aux.psum_fixed + r * kPsumFixedMaxE + c);
+        unsigned long long fx = 0;
+#pragma unroll
+        for (int r = 0; r < kPsumReplicas; ++r) fx += v[r];
+#pragma unroll
+        for (int r = 0; r < kPsumReplicas; ++r) __stcg(aux.psum_fixed + r * kPsumFixedMaxE + c, 0ull);
+        p = float(double(fx) * kPsumFixInv);
+        aux.psum[c] = p;
+      } else {
+        p = __ldcg(aux.psum + c);
+      }
+      s_psum[c] = p;
+    }
+  }
   __syncthreads();
-  assign_body(T, E, k, C, ids, chunk_counts, kept, offsets, slot_row, row_token, 0, nullptr, sm);
+  if (tid < T)
+    for (int r = 0; r < k; ++r) {
+      const int e = s_ids[tid * k + r];
+      if (e >= 0 && e < E)
+        atomicAdd(&wbase[warp * E + e], 1);
+      else
+        set_status(status, MOE_ERR_INVALID_ARG);
+    }
+  __syncthreads();
+  // counts, kept, and wbase[w][e] <- counts of e in warps before w.
+  for (int e = tid; e < E; e += kDispatchThreads) {
+    int32_t acc = 0;
+    for (int w = 0; w < 8; ++w) {
+      const int32_t v = wbase[w * E + e];
+      wbase[w * E + e] = acc;
+      acc += v;
+    }
+    const int32_t kp = int32_t(acc < C ? acc : C);
+    s_cnt[e] = acc;
+    s_kept[e] = kp;
+    counts[e] = acc;
+    kept[e] = kp;
+  }
+  __syncthreads();
+  if (aux.f)
+    aux_stats_block<true>(E, T, aux.alpha, s_cnt, s_psum, aux.f, aux.pbar, aux.l_aux, s_red);
+  if (aux.health) {
+    __syncthreads();
+    routing_health_block<true>(E, T, k, s_cnt, s_kept, aux.health, s_red, &s_kept_sum);
+  }
+  block_exclusive_scan(E, s_kept, off, part);
+  for (int e = tid; e <= E; e += kDispatchThreads) offsets[e] = off[e];
+  walk_slots(T, E, k, C, 0, s_ids, wbase + warp * E, off, slot_row, row_token, 0);
 }
 
 // Overflow reroute, step 2: the m-th slot of token t that the first fill
@@ -465,13 +542,13 @@ cudaError_t launch_dispatch(const moe_config_t& c, int64_t C, const void* x,
     count_launch();
     return e != cudaSuccess ? e : cudaGetLastError();
   };
-  if (!rr && counter && n_chunks == 1) {
-    err = ensure_dynamic_smem(reinterpret_cast<const void*>(dispatch_one_chunk_kernel),
-                              assign_smem);
+  if (!rr && n_chunks == 1) {
+    const size_t small_smem = assign_smem + size_t(3 * c.E) * 4;
+    err = ensure_dynamic_smem(reinterpret_cast<const void*>(dispatch_small_kernel), small_smem);
     if (err != cudaSuccess) return err;
-    err = launch_pdl(dispatch_one_chunk_kernel, dim3(1), dim3(kDispatchThreads), assign_smem, st,
-                     c.T, c.E, c.k, C, ids, chunk_counts, status, counter, counts, kept, aux_v,
-                     offsets, slot_row, row_token);
+    err = launch_pdl(dispatch_small_kernel, dim3(1), dim3(kDispatchThreads), small_smem, st, c.T,
+                     c.E, c.k, C, ids, status, counts, kept, aux_v, offsets, slot_row,
+                     row_token);
     count_launch();
     if (err != cudaSuccess || (err = cudaGetLastError()) != cudaSuccess) return err;
   } else if (!rr) {

@@ -15,14 +15,18 @@
 //
 // One CTA per SM, persistent over tiles (expert e with rows, 128 weight rows),
 // expert-major with the weight-row tile fastest.  Warps:
-//   warp 0     TMA producer: B[e, n0 .. n0+127, k-block] (16 KiB) and
-//              A[offsets[e] .. +NT, k-block] per stage, 128-byte swizzle, a
-//              ring of up to 12 stages
+//   warp 0     TMA producer: per stage two 64-wide k-blocks of
+//              B[e, n0 .. n0+127, :] (2 × 16 KiB) and of A[offsets[e] .. +NT, :],
+//              128-byte swizzle, a ring of as many stages as fit (6 at NT = 16)
 //   warp 1     TMEM allocator and MMA issuer: tcgen05.mma.cta_group::1
 //              kind::f16, M = 128, N = NT, two accumulators of NT columns
 //   warps 2-5  epilogue, one per TMEM lane quarter: thread = weight row n,
 //              NT columns = the expert's rows; bias, σ, bf16; for each row j
 //              the warp stores 32 consecutive outputs (64 bytes)
+// Two k-blocks per stage halve the issuing thread's fixed work per k-block
+// (barrier wait, commit, loop): with NT = 16 its 4 MMAs cost nothing on the
+// tensor pipe, and one 64-wide k-block per stage measured ~600 clocks of that
+// thread's time, which held one SM to ~58 GB/s of weights.
 // Rows of the A tile past the expert's end (the next expert's rows, or past
 // the buffer: zero-filled by the copy engine) are computed and not stored.
 // Every wait is bounded (4 s): on a timeout the kernel records
@@ -41,6 +45,7 @@ namespace {
 
 constexpr int kTileN = 128;  // weight rows per tile (MMA M)
 constexpr int kTileK = 64;   // one 128-byte swizzle row of bf16
+constexpr int kBoxes = 2;    // 64-wide k-blocks per stage
 constexpr int kMaxStages = 12;
 constexpr int kEpiWarp0 = 2;
 constexpr int kEpiWarps = 4;
@@ -80,8 +85,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  const uint32_t b_bytes = kTileN * kTileK * 2;  // weight tile
-  const uint32_t a_bytes = NT * kTileK * 2;      // rows tile
+  constexpr uint32_t b_box = kTileN * kTileK * 2;  // weight box (16 KiB)
+  constexpr uint32_t a_box = NT * kTileK * 2;      // rows box
+  const uint32_t b_bytes = kBoxes * b_box;
+  const uint32_t a_bytes = kBoxes * a_box;
   uint8_t* sB = smem;
   uint8_t* sA = smem + stages * b_bytes;
 
@@ -145,7 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int n_tn = (N + kTileN - 1) / kTileN;
   const int64_t total = int64_t(s_tp[E]) * n_tn;
-  const int nk = (K + kTileK - 1) / kTileK;
+  const int nk = (K + kBoxes * kTileK - 1) / (kBoxes * kTileK);  // stages per tile
   volatile int* abort_flag = &s_abort;
   auto give_up = [&]() {
     *abort_flag = 1;
@@ -181,9 +188,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
+        // A second box past K (K/64 odd) reads zeros, which add nothing.
         tc::mbar_arrive_expect_tx(&full_bar[stage], a_bytes + b_bytes);
-        tc::tma_load_3d(&tmB, &full_bar[stage], sB + stage * b_bytes, kb * kTileK, n0, e);
-        tc::tma_load_2d(&tmA, &full_bar[stage], sA + stage * a_bytes, kb * kTileK, s_off[e]);
+#pragma unroll
+        for (int h = 0; h < kBoxes; ++h) {
+          const int kx = (kb * kBoxes + h) * kTileK;
+          tc::tma_load_3d(&tmB, &full_bar[stage], sB + stage * b_bytes + h * b_box, kx, n0, e);
+          tc::tma_load_2d(&tmA, &full_bar[stage], sA + stage * a_bytes + h * a_box, kx,
+                          s_off[e]);
+        }
         ++issued;
         if (++stage == stages) stage = 0, phase ^= 1u;
       }
@@ -221,9 +234,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t b0 = tc::smem_u32(sB + stage * b_bytes);
         const uint32_t a0 = tc::smem_u32(sA + stage * a_bytes);
 #pragma unroll
-        for (int j = 0; j < kTileK / 16; ++j)
-          tc::mma_bf16(d_tmem, tc::sdesc_kmajor_sw128(b0 + j * 32),
-                       tc::sdesc_kmajor_sw128(a0 + j * 32), idesc, (kb | j) != 0);
+        for (int j = 0; j < kBoxes * kTileK / 16; ++j) {
+          const uint32_t h = uint32_t(j / (kTileK / 16)), q = uint32_t(j % (kTileK / 16));
+          tc::mma_bf16(d_tmem, tc::sdesc_kmajor_sw128(b0 + h * b_box + q * 32),
+                       tc::sdesc_kmajor_sw128(a0 + h * a_box + q * 32), idesc, (kb | j) != 0);
+        }
         tc::mma_commit(&empty_bar[stage]);
         if (++stage == stages) stage = 0, phase ^= 1u;
       }
@@ -307,7 +322,7 @@ cudaError_t launch_nt(const CUtensorMap& tmA, const CUtensorMap& tmB, int E, int
                       int32_t* status, int expert_max, int grid, cudaStream_t st) {
   auto kernel = gemm_swap_kernel<ACT, NT>;
   const void* kp = reinterpret_cast<const void*>(kernel);
-  const size_t stage_bytes = size_t(kTileN) * kTileK * 2 + size_t(NT) * kTileK * 2;
+  const size_t stage_bytes = size_t(kBoxes) * (size_t(kTileN) + NT) * kTileK * 2;
   const size_t budget = size_t(device_smem_optin()) - kernel_static_smem(kp) - 1024;
   int stages = int(budget / stage_bytes);
   if (stages > kMaxStages) stages = kMaxStages;

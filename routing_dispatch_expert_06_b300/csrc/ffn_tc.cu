@@ -32,7 +32,9 @@
 // running, its CTAs take the SMs that pair CTAs leave, and it waits for the
 // pair launch before it completes.
 //
-//   warp 0     TMA producer: 128×64 A tile + (BN or BN/2)×64 B tile per stage,
+//   warp 0     TMA producer: 128×64 A tile + (BN or BN/2)×64 B tile per
+//              64-wide k-block, two k-blocks per stage in a pair (one for the
+//              one-CTA and gathering kernels; see stage_kblocks),
 //              128-byte swizzle, a ring of as many stages as fit (GATHER:
 //              the whole warp gathers the A rows, four per lane, by TMA
 //              gather4 from the token matrix)
@@ -80,6 +82,17 @@ constexpr int kMaxExperts = 1024;
 // it cost 3-15%.
 constexpr int kTailSplitMinExperts = 128;
 enum { kActNone = -1 };
+
+// 64-wide k-blocks per pipeline stage.  The MMA thread's fixed work per
+// stage (the barrier wait, the commit, the loop) plus its 4 MMAs per k-block
+// measured ~640 clocks per k-block with one k-block per stage, more than the
+// ~560 clocks a 256 × 256 × 64 pair MMA keeps the tensor pipe busy, so the
+// pair kernel stages two k-blocks (64 KiB per CTA, 3 stages).  The one-CTA
+// kernel (96 KiB per two k-blocks: only 2 stages would fit) and the gathering
+// producer keep one.
+__host__ __device__ constexpr int stage_kblocks(bool pair, bool gather) {
+  return pair && !gather ? 2 : 1;
+}
 
 struct TileCoord {
   int e, m0, m_end, n0;
@@ -330,8 +343,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   const int bn_cta = PAIR ? BN / 2 : BN;    // B rows staged by this CTA
-  const uint32_t a_bytes = kTileM * kTileK * 2;
-  const uint32_t b_bytes = uint32_t(bn_cta) * kTileK * 2;
+  constexpr int KB = stage_kblocks(PAIR, GATHER);
+  const uint32_t a_box = kTileM * kTileK * 2;             // one 64-wide k-block
+  const uint32_t b_box = uint32_t(bn_cta) * kTileK * 2;
+  const uint32_t a_bytes = KB * a_box;                     // one stage
+  const uint32_t b_bytes = KB * b_box;
   uint8_t* sA = smem;                      // stages × a_bytes
   uint8_t* sB = smem + stages * a_bytes;   // stages × b_bytes
   uint8_t* sE = sB + stages * b_bytes;     // kEpiWarps × kEpiBufBytes
@@ -410,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int n_tn = (N + BN - 1) / BN;
   const int64_t total = int64_t(s_mt[E]) * n_tn;
-  const int nk = (K + kTileK - 1) / kTileK;
+  const int nk = (K + KB * kTileK - 1) / (KB * kTileK);  // stages per tile
   const int64_t first_tile = PAIR ? blockIdx.x / 2 : blockIdx.x;
   const int64_t tile_step = PAIR ? gridDim.x / 2 : gridDim.x;
   volatile int* abort_flag = &s_abort;
@@ -501,13 +517,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           // expects the bytes of the whole pair.
           if (rank == 0) tc::mbar_arrive_expect_tx(&full_bar[stage], 2 * (a_bytes + b_bytes));
           const uint32_t bar = tc::mapa(tc::smem_u32(&full_bar[stage]), 0);
-          tc::tma_load_2d_pair(&tmA, bar, sA + stage * a_bytes, kb * kTileK, c.m0);
-          tc::tma_load_3d_pair(&tmB, bar, sB + stage * b_bytes, kb * kTileK,
-                               c.n0 + int(rank) * bn_cta, c.e);
+          // A k-block past K (K/64 odd) arrives as zeros, which add nothing.
+#pragma unroll
+          for (int h = 0; h < KB; ++h) {
+            const int kx = (kb * KB + h) * kTileK;
+            tc::tma_load_2d_pair(&tmA, bar, sA + stage * a_bytes + h * a_box, kx, c.m0);
+            tc::tma_load_3d_pair(&tmB, bar, sB + stage * b_bytes + h * b_box, kx,
+                                 c.n0 + int(rank) * bn_cta, c.e);
+          }
         } else {
           tc::mbar_arrive_expect_tx(&full_bar[stage], a_bytes + b_bytes);
-          tc::tma_load_2d(&tmA, &full_bar[stage], sA + stage * a_bytes, kb * kTileK, c.m0);
-          tc::tma_load_3d(&tmB, &full_bar[stage], sB + stage * b_bytes, kb * kTileK, c.n0, c.e);
+#pragma unroll
+          for (int h = 0; h < KB; ++h) {
+            const int kx = (kb * KB + h) * kTileK;
+            tc::tma_load_2d(&tmA, &full_bar[stage], sA + stage * a_bytes + h * a_box, kx, c.m0);
+            tc::tma_load_3d(&tmB, &full_bar[stage], sB + stage * b_bytes + h * b_box, kx, c.n0,
+                            c.e);
+          }
         }
         ++issued;
         if (++stage == stages) stage = 0, phase ^= 1u;
@@ -550,9 +576,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t a0 = tc::smem_u32(sA + stage * a_bytes);
         const uint32_t b0 = tc::smem_u32(sB + stage * b_bytes);
 #pragma unroll
-        for (int j = 0; j < kTileK / 16; ++j) {
-          const uint64_t ad = tc::sdesc_kmajor_sw128(a0 + j * 32);
-          const uint64_t bd = tc::sdesc_kmajor_sw128(b0 + j * 32);
+        for (int j = 0; j < KB * kTileK / 16; ++j) {
+          const uint32_t h = uint32_t(j / (kTileK / 16)), q = uint32_t(j % (kTileK / 16));
+          const uint64_t ad = tc::sdesc_kmajor_sw128(a0 + h * a_box + q * 32);
+          const uint64_t bd = tc::sdesc_kmajor_sw128(b0 + h * b_box + q * 32);
           if constexpr (PAIR)
             tc::mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | j) != 0);
           else
@@ -745,7 +772,8 @@ cudaError_t launch_variant(int act, const CUtensorMap& tmA, const CUtensorMap& t
   // As many pipeline stages as fit beside the epilogue buffers and the
   // kernel's static shared memory.
   const int bn_cta = PAIR ? BN / 2 : BN;
-  const size_t stage_bytes = size_t(kTileM) * kTileK * 2 + size_t(bn_cta) * kTileK * 2;
+  const size_t stage_bytes =
+      size_t(stage_kblocks(PAIR, GATHER)) * (size_t(kTileM) + bn_cta) * kTileK * 2;
   const size_t fixed = 1024 + size_t(kEpiWarps) * kEpiBufBytes;
   const size_t budget = size_t(device_smem_optin()) - static_smem;
   int stages = budget > fixed ? int((budget - fixed) / stage_bytes) : 0;
