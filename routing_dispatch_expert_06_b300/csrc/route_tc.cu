@@ -12,7 +12,8 @@
 // adds the splits in split order, so the result does not depend on which CTA
 // runs first.  A CTA walks units (tile, split) b, b + grid, ...  Warps:
 //   warp 0     TMA producer: x tile [128 × 64] and W_r tile [NP × 64] per
-//              stage (NP = E rounded up to a power of two >= 32; rows past E
+//              64-wide k-block, two k-blocks per stage when NP <= 64
+//              (NP = E rounded up to a power of two >= 32; rows past E
 //              and columns past d arrive as zeros from the copy engine's
 //              out-of-bounds fill)
 //   warp 1     TMEM allocator and MMA issuer: tcgen05.mma M=128, N=NP, K=16,
@@ -54,6 +55,13 @@ constexpr size_t kMinSmem = 120 * 1024;  // one CTA per SM (it may take all of T
 template <int G>
 constexpr int epi_threads() { return 128 * G; }
 
+// 64-wide k-blocks per pipeline stage.  The MMA thread's fixed work per stage
+// (barrier wait, commit, loop) with its 4 MMAs per k-block measured ~0.33 us
+// per k-block whatever N, which paced the narrow routers (E <= 64, stages of
+// 20-24 KiB); two k-blocks per stage halve that work at the same bytes in
+// flight.  At NP = 256 a stage already holds 48 KiB and only 4 fit.
+__host__ __device__ constexpr int route_stage_kblocks(int NP) { return NP <= 64 ? 2 : 1; }
+
 struct RouteTcArgs {
   int64_t T;
   int d, E, NP, stages;
@@ -71,6 +79,8 @@ __global__ void __launch_bounds__(64 + 128 * G, 1)
   constexpr int NP = G * NPG;
   constexpr int CH = 16;  // columns per tensor-memory load
   constexpr int kEpiThreads = epi_threads<G>();
+  constexpr int KB = route_stage_kblocks(NP);
+  static_assert(kSegBlocks % KB == 0, "segments hold whole stages");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages];
   __shared__ uint64_t tfull_bar[2], tempty_bar[2], drain_bar;
@@ -80,8 +90,10 @@ __global__ void __launch_bounds__(64 + 128 * G, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  const uint32_t a_bytes = kTileM * kTileK * 2;
-  const uint32_t b_bytes = uint32_t(NP) * kTileK * 2;
+  const uint32_t a_box = kTileM * kTileK * 2;
+  const uint32_t b_box = uint32_t(NP) * kTileK * 2;
+  const uint32_t a_bytes = KB * a_box;
+  const uint32_t b_bytes = KB * b_box;
   uint8_t* sA = smem;
   uint8_t* sB = smem + a.stages * a_bytes;
   const int nk = (a.d + kTileK - 1) / kTileK;
@@ -138,15 +150,21 @@ __global__ void __launch_bounds__(64 + 128 * G, 1)
       int seg_lo, seg_hi;
       seg_range(u, seg_lo, seg_hi);
       const int kb_hi = min(nk, seg_hi * kSegBlocks);
-      for (int kb = seg_lo * kSegBlocks; kb < kb_hi; ++kb) {
+      // Stage kb holds k-blocks KB·kb .. KB·kb + KB - 1; one past d (odd nk)
+      // arrives as zeros.
+      for (int kb = seg_lo * kSegBlocks / KB; kb * KB < kb_hi; ++kb) {
         if (!tc::mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, kWaitLimitNs)) {
           give_up();
           ok = false;
           break;
         }
         tc::mbar_arrive_expect_tx(&full_bar[stage], a_bytes + b_bytes);
-        tc::tma_load_2d(&tmX, &full_bar[stage], sA + stage * a_bytes, kb * kTileK, m0);
-        tc::tma_load_2d(&tmW, &full_bar[stage], sB + stage * b_bytes, kb * kTileK, 0);
+#pragma unroll
+        for (int h = 0; h < KB; ++h) {
+          const int kx = (kb * KB + h) * kTileK;
+          tc::tma_load_2d(&tmX, &full_bar[stage], sA + stage * a_bytes + h * a_box, kx, m0);
+          tc::tma_load_2d(&tmW, &full_bar[stage], sB + stage * b_bytes + h * b_box, kx, 0);
+        }
         ++issued;
         if (++stage == a.stages) stage = 0, phase ^= 1u;
       }
@@ -177,7 +195,7 @@ __global__ void __launch_bounds__(64 + 128 * G, 1)
         tc::fence_after_sync();
         const uint32_t d_tmem = tmem_base + buf * uint32_t(NP);
         const int kb_end = min(nk, (sg + 1) * kSegBlocks);
-        for (int kb = sg * kSegBlocks; kb < kb_end; ++kb) {
+        for (int kb = sg * kSegBlocks / KB; kb * KB < kb_end; ++kb) {
           if (!tc::mbar_wait(&full_bar[stage], phase, abort_flag, kWaitLimitNs)) {
             give_up();
             ok = false;
@@ -186,11 +204,14 @@ __global__ void __launch_bounds__(64 + 128 * G, 1)
           tc::fence_after_sync();
           const uint32_t a0 = tc::smem_u32(sA + stage * a_bytes);
           const uint32_t b0 = tc::smem_u32(sB + stage * b_bytes);
-          const bool first = kb == sg * kSegBlocks;
+          const bool first = kb * KB == sg * kSegBlocks;
 #pragma unroll
-          for (int j = 0; j < kTileK / 16; ++j)
-            tc::mma_bf16(d_tmem, tc::sdesc_kmajor_sw128(a0 + j * 32),
-                         tc::sdesc_kmajor_sw128(b0 + j * 32), idesc, (first && j == 0) ? 0u : 1u);
+          for (int j = 0; j < KB * kTileK / 16; ++j) {
+            const uint32_t h = uint32_t(j / (kTileK / 16)), q = uint32_t(j % (kTileK / 16));
+            tc::mma_bf16(d_tmem, tc::sdesc_kmajor_sw128(a0 + h * a_box + q * 32),
+                         tc::sdesc_kmajor_sw128(b0 + h * b_box + q * 32), idesc,
+                         (first && j == 0) ? 0u : 1u);
+          }
           tc::mma_commit(&empty_bar[stage]);
           if (++stage == a.stages) stage = 0, phase ^= 1u;
         }
@@ -301,7 +322,8 @@ cudaError_t launch_g(const CUtensorMap& tmX, const CUtensorMap& tmW, RouteTcArgs
   auto kernel = route_tc_kernel<NPG, G>;
   const void* kp = reinterpret_cast<const void*>(kernel);
   // As many stages as fit beside the kernel's static shared memory.
-  const size_t stage_bytes = size_t(kTileM) * kTileK * 2 + size_t(G * NPG) * kTileK * 2;
+  const size_t stage_bytes =
+      size_t(route_stage_kblocks(G * NPG)) * (size_t(kTileM) + G * NPG) * kTileK * 2;
   const size_t budget = size_t(device_smem_optin()) - kernel_static_smem(kp) - 1024;
   int stages = int(budget / stage_bytes);
   if (stages > kMaxStages) stages = kMaxStages;
