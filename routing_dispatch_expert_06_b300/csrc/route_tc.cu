@@ -10,7 +10,10 @@
 // one tile's reduction over d: each takes a contiguous run of its segments and
 // writes its own fp32 partial logits, part[split][t][e]; the select kernel
 // adds the splits in split order, so the result does not depend on which CTA
-// runs first.  A CTA walks units (tile, split) b, b + grid, ...  Warps:
+// runs first.  A CTA walks units (tile, split) b, b + grid, ...  With E > 128
+// and one split, clusters of two CTAs share 256-token tiles (PAIR, see the
+// kernel): 170 against 176 us of routing on the d = 7168, E = 256 layer.
+// Warps:
 //   warp 0     TMA producer: x tile [128 × 64] and W_r tile [NP × 64] per
 //              64-wide k-block, two k-blocks per stage when NP <= 64
 //              (NP = E rounded up to a power of two >= 32; rows past E
@@ -71,15 +74,25 @@ struct RouteTcArgs {
   int32_t* status;
 };
 
-// NPG = NP / G columns per epilogue thread.
-template <int NPG, int G>
+// NPG = NP / G columns per epilogue thread.  PAIR (NP = 256, one split):
+// clusters of two CTAs run the 2-SM MMA (cta_group::2, M = 256 tokens,
+// N = 256 experts) on 256-token tiles; each CTA stages its own 128 token rows
+// and half of W_r (tmW boxes of 128 rows), the copies of both complete on the
+// even CTA's barriers, the even CTA issues the MMAs and multicasts its
+// commits, and each CTA drains its own 128 rows of the accumulator.  Per SM
+// and k-block that is 32 KiB of operands instead of 48 KiB, so two k-blocks
+// per stage fit three times.
+template <int NPG, int G, bool PAIR>
 __global__ void __launch_bounds__(64 + 128 * G, 1)
     route_tc_kernel(const __grid_constant__ CUtensorMap tmX,
                     const __grid_constant__ CUtensorMap tmW, const RouteTcArgs a) {
   constexpr int NP = G * NPG;
   constexpr int CH = 16;  // columns per tensor-memory load
   constexpr int kEpiThreads = epi_threads<G>();
-  constexpr int KB = route_stage_kblocks(NP);
+  constexpr int KB = PAIR ? 2 : route_stage_kblocks(NP);
+  constexpr int BROWS = PAIR ? NP / 2 : NP;     // W_r rows staged by this CTA
+  constexpr int TILE = PAIR ? 2 * kTileM : kTileM;  // tokens per unit
+  static_assert(!PAIR || NP == 256, "pairs only for NP = 256");
   static_assert(kSegBlocks % KB == 0, "segments hold whole stages");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages];
@@ -88,19 +101,23 @@ __global__ void __launch_bounds__(64 + 128 * G, 1)
   __shared__ int s_abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = PAIR ? tc::cluster_ctarank() : 0u;  // 0 = the pair's MMA issuer
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   const uint32_t a_box = kTileM * kTileK * 2;
-  const uint32_t b_box = uint32_t(NP) * kTileK * 2;
+  const uint32_t b_box = uint32_t(BROWS) * kTileK * 2;
   const uint32_t a_bytes = KB * a_box;
   const uint32_t b_bytes = KB * b_box;
   uint8_t* sA = smem;
   uint8_t* sB = smem + a.stages * a_bytes;
   const int nk = (a.d + kTileK - 1) / kTileK;
   const int nseg = (nk + kSegBlocks - 1) / kSegBlocks;
-  const int64_t n_tiles = (a.T + kTileM - 1) / kTileM;
-  // Work unit u: tile u / nsplit, segments [seg_lo, seg_hi) of split u % nsplit.
+  const int64_t n_tiles = (a.T + TILE - 1) / TILE;
+  // Work unit u: tile u / nsplit, segments [seg_lo, seg_hi) of split u % nsplit
+  // (PAIR: nsplit = 1); CTA (pair) b takes units b, b + grid, ...
   const int64_t n_units = n_tiles * a.nsplit;
+  const int64_t unit0 = PAIR ? blockIdx.x / 2 : blockIdx.x;
+  const int64_t unit_step = PAIR ? gridDim.x / 2 : gridDim.x;
   auto seg_range = [&](int64_t u, int& lo, int& hi) {
     const int sp = int(u % a.nsplit);
     lo = int(int64_t(sp) * nseg / a.nsplit);
@@ -114,7 +131,8 @@ __global__ void __launch_bounds__(64 + 128 * G, 1)
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&tfull_bar[b], 1);
-      tc::mbar_init(&tempty_bar[b], kEpiThreads);
+      // PAIR: one arrival per epilogue warp of both CTAs, on the even CTA's.
+      tc::mbar_init(&tempty_bar[b], PAIR ? 2 * kEpiThreads / 32 : kEpiThreads);
     }
     tc::mbar_init(&drain_bar, 1);
     s_abort = 0;
@@ -122,9 +140,17 @@ __global__ void __launch_bounds__(64 + 128 * G, 1)
     tc::prefetch_tmap(&tmX);
     tc::prefetch_tmap(&tmW);
   }
+  // A pair allocates its tensor memory collectively, and the peer's barriers
+  // must be initialised before any copy or commit of the pair signals them.
+  if constexpr (PAIR) tc::cluster_sync();
   if (warp == 1) {
-    tc::tmem_alloc(&s_tmem, a.tmem_cols);
-    tc::tmem_relinquish();
+    if constexpr (PAIR) {
+      tc::tmem_alloc_pair(&s_tmem, a.tmem_cols);
+      tc::tmem_relinquish_pair();
+    } else {
+      tc::tmem_alloc(&s_tmem, a.tmem_cols);
+      tc::tmem_relinquish();
+    }
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -145,8 +171,8 @@ __global__ void __launch_bounds__(64 + 128 * G, 1)
     uint32_t phase = 0;
     int64_t issued = 0;
     bool ok = true;
-    for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-      const int32_t m0 = int32_t((u / a.nsplit) * kTileM);
+    for (int64_t u = unit0; u < n_units && ok; u += unit_step) {
+      const int32_t m0 = int32_t((u / a.nsplit) * TILE + int64_t(rank) * kTileM);
       int seg_lo, seg_hi;
       seg_range(u, seg_lo, seg_hi);
       const int kb_hi = min(nk, seg_hi * kSegBlocks);
@@ -158,36 +184,57 @@ __global__ void __launch_bounds__(64 + 128 * G, 1)
           ok = false;
           break;
         }
-        tc::mbar_arrive_expect_tx(&full_bar[stage], a_bytes + b_bytes);
+        if constexpr (PAIR) {
+          // Both CTAs' copies complete on the even CTA's full barrier, which
+          // expects the bytes of the whole pair.
+          if (rank == 0) tc::mbar_arrive_expect_tx(&full_bar[stage], 2 * (a_bytes + b_bytes));
+          const uint32_t bar = tc::mapa(tc::smem_u32(&full_bar[stage]), 0);
 #pragma unroll
-        for (int h = 0; h < KB; ++h) {
-          const int kx = (kb * KB + h) * kTileK;
-          tc::tma_load_2d(&tmX, &full_bar[stage], sA + stage * a_bytes + h * a_box, kx, m0);
-          tc::tma_load_2d(&tmW, &full_bar[stage], sB + stage * b_bytes + h * b_box, kx, 0);
+          for (int h = 0; h < KB; ++h) {
+            const int kx = (kb * KB + h) * kTileK;
+            tc::tma_load_2d_pair(&tmX, bar, sA + stage * a_bytes + h * a_box, kx, m0);
+            tc::tma_load_2d_pair(&tmW, bar, sB + stage * b_bytes + h * b_box, kx,
+                                 int(rank) * BROWS);
+          }
+        } else {
+          tc::mbar_arrive_expect_tx(&full_bar[stage], a_bytes + b_bytes);
+#pragma unroll
+          for (int h = 0; h < KB; ++h) {
+            const int kx = (kb * KB + h) * kTileK;
+            tc::tma_load_2d(&tmX, &full_bar[stage], sA + stage * a_bytes + h * a_box, kx, m0);
+            tc::tma_load_2d(&tmW, &full_bar[stage], sB + stage * b_bytes + h * b_box, kx, 0);
+          }
         }
         ++issued;
         if (++stage == a.stages) stage = 0, phase ^= 1u;
       }
     }
     // Drain: the last `stages` copies this thread issued must land before the
-    // CTA exits (on the normal path the MMA issuer has consumed them all).
-    const int64_t first = issued > a.stages ? issued - a.stages : 0;
-    for (int64_t i = first; i < issued; ++i)
-      tc::mbar_wait(&full_bar[i % a.stages], uint32_t((i / a.stages) & 1), nullptr, kWaitLimitNs);
-  } else if (warp == 1 && lane == 0) {
+    // CTA exits (on the normal path the MMA issuer has consumed them all).  In
+    // a pair the even CTA's full barriers track the copies of both CTAs.
+    if (rank == 0) {
+      const int64_t first = issued > a.stages ? issued - a.stages : 0;
+      for (int64_t i = first; i < issued; ++i)
+        tc::mbar_wait(&full_bar[i % a.stages], uint32_t((i / a.stages) & 1), nullptr,
+                      kWaitLimitNs);
+    }
+  } else if (warp == 1 && lane == 0 && rank == 0) {
     // ---------------- MMA issuer ----------------
-    const uint32_t idesc = tc::idesc_bf16_f32(kTileM, NP);
+    const uint32_t idesc = tc::idesc_bf16_f32(TILE, NP);
     int stage = 0;
     uint32_t phase = 0;
     uint32_t seg_count = 0;  // segments issued by this CTA (all tiles)
     bool ok = true;
-    for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+    for (int64_t u = unit0; u < n_units && ok; u += unit_step) {
       int seg_lo, seg_hi;
       seg_range(u, seg_lo, seg_hi);
       for (int sg = seg_lo; sg < seg_hi && ok; ++sg, ++seg_count) {
         const uint32_t buf = seg_count & 1u;
-        if (!tc::mbar_wait(&tempty_bar[buf], ((seg_count >> 1) & 1u) ^ 1u, abort_flag,
-                           kWaitLimitNs)) {
+        const uint32_t par = ((seg_count >> 1) & 1u) ^ 1u;
+        const bool free_acc =
+            PAIR ? tc::mbar_wait_cluster(&tempty_bar[buf], par, abort_flag, kWaitLimitNs)
+                 : tc::mbar_wait(&tempty_bar[buf], par, abort_flag, kWaitLimitNs);
+        if (!free_acc) {
           give_up();
           ok = false;
           break;
@@ -208,18 +255,32 @@ __global__ void __launch_bounds__(64 + 128 * G, 1)
 #pragma unroll
           for (int j = 0; j < KB * kTileK / 16; ++j) {
             const uint32_t h = uint32_t(j / (kTileK / 16)), q = uint32_t(j % (kTileK / 16));
-            tc::mma_bf16(d_tmem, tc::sdesc_kmajor_sw128(a0 + h * a_box + q * 32),
-                         tc::sdesc_kmajor_sw128(b0 + h * b_box + q * 32), idesc,
-                         (first && j == 0) ? 0u : 1u);
+            const uint64_t ad = tc::sdesc_kmajor_sw128(a0 + h * a_box + q * 32);
+            const uint64_t bd = tc::sdesc_kmajor_sw128(b0 + h * b_box + q * 32);
+            if constexpr (PAIR)
+              tc::mma_bf16_pair(d_tmem, ad, bd, idesc, (first && j == 0) ? 0u : 1u);
+            else
+              tc::mma_bf16(d_tmem, ad, bd, idesc, (first && j == 0) ? 0u : 1u);
           }
-          tc::mma_commit(&empty_bar[stage]);
+          if constexpr (PAIR)
+            tc::mma_commit_pair_mc(&empty_bar[stage], 0x3);
+          else
+            tc::mma_commit(&empty_bar[stage]);
           if (++stage == a.stages) stage = 0, phase ^= 1u;
         }
-        if (ok) tc::mma_commit(&tfull_bar[buf]);
+        if (ok) {
+          if constexpr (PAIR)
+            tc::mma_commit_pair_mc(&tfull_bar[buf], 0x3);
+          else
+            tc::mma_commit(&tfull_bar[buf]);
+        }
       }
     }
     // Drain: every MMA this thread issued completes before TMEM is freed.
-    tc::mma_commit(&drain_bar);
+    if constexpr (PAIR)
+      tc::mma_commit_pair(&drain_bar);
+    else
+      tc::mma_commit(&drain_bar);
     tc::mbar_wait(&drain_bar, 0, nullptr, kWaitLimitNs);
   } else if (warp >= 2) {
     // ---------------- epilogue ----------------
@@ -232,8 +293,8 @@ __global__ void __launch_bounds__(64 + 128 * G, 1)
     const uint32_t t_lane = tmem_base + (uint32_t(quarter * 32) << 16) + uint32_t(col0);
     uint32_t seg_count = 0;
     bool ok = true;
-    for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
-      const int64_t t = (u / a.nsplit) * kTileM + row;
+    for (int64_t u = unit0; u < n_units; u += unit_step) {
+      const int64_t t = (u / a.nsplit) * TILE + int64_t(rank) * kTileM + row;
       int seg_lo, seg_hi;
       seg_range(u, seg_lo, seg_hi);
       float v[NPG];
@@ -259,7 +320,13 @@ __global__ void __launch_bounds__(64 + 128 * G, 1)
             for (int j = 0; j < CH; ++j) v[c0 + j] += __uint_as_float(r[j]);
           }
           tc::fence_before_sync();
-          tc::mbar_arrive(&tempty_bar[buf]);
+          if constexpr (PAIR) {
+            // One arrival per warp on the even CTA's barrier.
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive_cluster(tc::mapa(tc::smem_u32(&tempty_bar[buf]), 0));
+          } else {
+            tc::mbar_arrive(&tempty_bar[buf]);
+          }
         }
       }
       if (ok && t < a.T && ncol > 0) {
@@ -279,10 +346,16 @@ __global__ void __launch_bounds__(64 + 128 * G, 1)
   }
   tc::fence_before_sync();
   __syncthreads();
+  // Neither CTA of a pair leaves (or frees its tensor memory) while the other
+  // may still signal its barriers or feed its MMAs.
+  if constexpr (PAIR) tc::cluster_sync();
   tc::fence_after_sync();
   if (warp == 1) {
     __syncwarp();
-    tc::tmem_dealloc(tmem_base, a.tmem_cols);
+    if constexpr (PAIR)
+      tc::tmem_dealloc_pair(tmem_base, a.tmem_cols);
+    else
+      tc::tmem_dealloc(tmem_base, a.tmem_cols);
   }
 }
 
@@ -316,14 +389,15 @@ bool encode_2d(EncodeTiledFn encode, CUtensorMap* m, const void* base, int64_t i
          CUDA_SUCCESS;
 }
 
-template <int NPG, int G>
+template <int NPG, int G, bool PAIR>
 cudaError_t launch_g(const CUtensorMap& tmX, const CUtensorMap& tmW, RouteTcArgs a,
-                     unsigned grid, cudaStream_t st) {
-  auto kernel = route_tc_kernel<NPG, G>;
+                     int64_t n_units, cudaStream_t st) {
+  auto kernel = route_tc_kernel<NPG, G, PAIR>;
   const void* kp = reinterpret_cast<const void*>(kernel);
   // As many stages as fit beside the kernel's static shared memory.
   const size_t stage_bytes =
-      size_t(route_stage_kblocks(G * NPG)) * (size_t(kTileM) + G * NPG) * kTileK * 2;
+      PAIR ? size_t(2) * (size_t(kTileM) + G * NPG / 2) * kTileK * 2
+           : size_t(route_stage_kblocks(G * NPG)) * (size_t(kTileM) + G * NPG) * kTileK * 2;
   const size_t budget = size_t(device_smem_optin()) - kernel_static_smem(kp) - 1024;
   int stages = int(budget / stage_bytes);
   if (stages > kMaxStages) stages = kMaxStages;
@@ -333,8 +407,34 @@ cudaError_t launch_g(const CUtensorMap& tmX, const CUtensorMap& tmW, RouteTcArgs
   if (smem < kMinSmem) smem = kMinSmem;
   cudaError_t err = ensure_dynamic_smem(kp, smem);
   if (err != cudaSuccess) return err;
-  kernel<<<grid, 64 + 128 * G, smem, st>>>(tmX, tmW, a);
-  return cudaGetLastError();
+  const int sms = device_sms();
+  if constexpr (!PAIR) {
+    const unsigned grid = unsigned(n_units < sms ? n_units : sms);
+    kernel<<<grid, 64 + 128 * G, smem, st>>>(tmX, tmW, a);
+    return cudaGetLastError();
+  } else {
+    // Persistent clusters of two: as many as can be resident, at most one per
+    // unit.
+    cudaLaunchConfig_t cfg{};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.blockDim = dim3(64 + 128 * G);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.gridDim = dim3(2);
+    int clusters = 0;
+    err = max_active_clusters(kp, cfg, &clusters);
+    if (err != cudaSuccess) return err;
+    if (clusters < 1) return cudaErrorInvalidConfiguration;
+    cfg.gridDim = dim3(unsigned(2 * (n_units < clusters ? n_units : clusters)));
+    err = cudaLaunchKernelEx(&cfg, kernel, tmX, tmW, a);
+    return err != cudaSuccess ? err : cudaGetLastError();
+  }
 }
 
 }  // namespace
@@ -377,18 +477,24 @@ cudaError_t launch_route_tc(const moe_config_t& c, const void* x, const void* Wr
   a.part = part;
   a.status = status;
 
+  // CTA pairs on 256-token tiles when one split covers d and E > 128.
+  const bool pair = NP == 256 && a.nsplit == 1;
+
   CUtensorMap tmX, tmW;
   if (!encode_2d(encode, &tmX, x, c.d, c.T, kTileK, kTileM)) return cudaErrorInvalidValue;
-  if (!encode_2d(encode, &tmW, Wr, c.d, c.E, kTileK, uint32_t(NP))) return cudaErrorInvalidValue;
-  const int64_t n_units = ((c.T + kTileM - 1) / kTileM) * a.nsplit;
-  const int sms = device_sms();
-  const unsigned grid = unsigned(n_units < sms ? n_units : sms);
+  if (!encode_2d(encode, &tmW, Wr, c.d, c.E, kTileK, uint32_t(pair ? NP / 2 : NP)))
+    return cudaErrorInvalidValue;
+  const int64_t tile = pair ? 2 * kTileM : kTileM;
+  const int64_t n_units = ((c.T + tile - 1) / tile) * a.nsplit;
   cudaError_t err;
   switch (NP) {
-    case 32: err = launch_g<16, 2>(tmX, tmW, a, grid, st); break;
-    case 64: err = launch_g<16, 4>(tmX, tmW, a, grid, st); break;
-    case 128: err = launch_g<32, 4>(tmX, tmW, a, grid, st); break;
-    default: err = launch_g<64, 4>(tmX, tmW, a, grid, st); break;
+    case 32: err = launch_g<16, 2, false>(tmX, tmW, a, n_units, st); break;
+    case 64: err = launch_g<16, 4, false>(tmX, tmW, a, n_units, st); break;
+    case 128: err = launch_g<32, 4, false>(tmX, tmW, a, n_units, st); break;
+    default:
+      err = pair ? launch_g<64, 4, true>(tmX, tmW, a, n_units, st)
+                 : launch_g<64, 4, false>(tmX, tmW, a, n_units, st);
+      break;
   }
   count_launch();
   return err;
