@@ -212,6 +212,24 @@ def test_pair_body_and_tail_tiles_match_one_sm_gemm():
         assert ((a - b).abs() <= 1e-2 + 2e-2 * b.abs()).all(), name
 
 
+ODD_K_CASES = [
+    # K/64 odd in both expert GEMMs (d = 960: 15 k-blocks, d_ff = 704: 11):
+    # the last pipeline stage of two k-blocks holds one past K, which the copy
+    # engine fills with zeros.  CTA pairs on every tile (E = 8), pairs on whole
+    # 256-row tiles plus one-CTA tails (E = 256), and the swapped decode kernel.
+    ("e8_pairs", W["bf16_t4096_d1024_e8_top2"].replace(T=1500, d=960, d_ff=704)),
+    ("e256_pairs_and_tails", W["bf16_t32768_d7168_e256_top8"].replace(
+        T=3000, d=320, d_ff=448, capacity_factor=2.0)),
+    ("decode_swapped", W["decode_bf16_t8_d2048_e64_top6"].replace(d=960, d_ff=704)),
+]
+
+
+@pytest.mark.parametrize("name,wl", ODD_K_CASES, ids=[c[0] for c in ODD_K_CASES])
+def test_odd_k_block_counts_match_oracle(name, wl):
+    _, inp, out, _ = run_gpu(wl, expert_bias=True)
+    check_forward(wl, inp, out, full=True)
+
+
 @pytest.mark.parametrize("name", [n for n in W if n.startswith("decode_")])
 def test_decode_regime(name):
     # A few tokens per call on the many-expert layers: every output is checked.

@@ -229,6 +229,9 @@ ONE_SPLIT_CASES = [
     (9999, 2048, 64, 6, True, "zipf:0.8"),
     (9700, 256, 100, 4, False, "normal:1.0"),
     (9700, 256, 130, 5, True, "normal:1.0"),
+    # E > 128: CTA pairs on 256-token tiles; T = 38·256 + 50, so the last
+    # tile's odd CTA has no token (its copies read zeros past T)
+    (9778, 200, 200, 8, False, "normal:1.0"),
 ]
 
 
