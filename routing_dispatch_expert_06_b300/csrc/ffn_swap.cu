@@ -233,11 +233,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::fence_after_sync();
         const uint32_t b0 = tc::smem_u32(sB + stage * b_bytes);
         const uint32_t a0 = tc::smem_u32(sA + stage * a_bytes);
+        const uint64_t bd0 = tc::sdesc_kmajor_sw128(b0), ad0 = tc::sdesc_kmajor_sw128(a0);
 #pragma unroll
         for (int j = 0; j < kBoxes * kTileK / 16; ++j) {
           const uint32_t h = uint32_t(j / (kTileK / 16)), q = uint32_t(j % (kTileK / 16));
-          tc::mma_bf16(d_tmem, tc::sdesc_kmajor_sw128(b0 + h * b_box + q * 32),
-                       tc::sdesc_kmajor_sw128(a0 + h * a_box + q * 32), idesc, (kb | j) != 0);
+          tc::mma_bf16(d_tmem, tc::sdesc_advance(bd0, h * b_box + q * 32),
+                       tc::sdesc_advance(ad0, h * a_box + q * 32), idesc, (kb | j) != 0);
         }
         tc::mma_commit(&empty_bar[stage]);
         if (++stage == stages) stage = 0, phase ^= 1u;

@@ -252,11 +252,12 @@ __global__ void __launch_bounds__(64 + 128 * G, 1)
           const uint32_t a0 = tc::smem_u32(sA + stage * a_bytes);
           const uint32_t b0 = tc::smem_u32(sB + stage * b_bytes);
           const bool first = kb * KB == sg * kSegBlocks;
+          const uint64_t ad0 = tc::sdesc_kmajor_sw128(a0), bd0 = tc::sdesc_kmajor_sw128(b0);
 #pragma unroll
           for (int j = 0; j < KB * kTileK / 16; ++j) {
             const uint32_t h = uint32_t(j / (kTileK / 16)), q = uint32_t(j % (kTileK / 16));
-            const uint64_t ad = tc::sdesc_kmajor_sw128(a0 + h * a_box + q * 32);
-            const uint64_t bd = tc::sdesc_kmajor_sw128(b0 + h * b_box + q * 32);
+            const uint64_t ad = tc::sdesc_advance(ad0, h * a_box + q * 32);
+            const uint64_t bd = tc::sdesc_advance(bd0, h * b_box + q * 32);
             if constexpr (PAIR)
               tc::mma_bf16_pair(d_tmem, ad, bd, idesc, (first && j == 0) ? 0u : 1u);
             else

@@ -291,6 +291,13 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
   return d;
 }
 
+// The descriptor of an address `bytes` (a multiple of 16) further on: the
+// start address field holds addr >> 4 in its low 14 bits, and shared-memory
+// offsets stay below 256 KiB, so the field cannot carry into the next one.
+__device__ __forceinline__ uint64_t sdesc_advance(uint64_t desc, uint32_t bytes) {
+  return desc + uint64_t(bytes >> 4);
+}
+
 // 32 TMEM lanes (one per thread of the warp) × 32 consecutive 32-bit columns.
 __device__ __forceinline__ void tmem_ld_x32(uint32_t taddr, uint32_t* r) {
   asm volatile(
