@@ -71,6 +71,17 @@ constexpr int kMaxStages = 8;
 constexpr int kEpiWarp0 = 2;
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
+// The gathering producer runs in kGatherWarps warps (warp 0 and the warps
+// after the epilogue): one warp issuing the 32 gather4 copies of every stage
+// was the limit.  Warp g serves one k-block half of one pipeline stage (stage
+// g / KB, half g % KB) and nothing else, so a warp waits for a stage's release
+// only after it issued that stage's previous use itself: the barrier is then
+// at most one phase behind and its parity wait cannot mistake an older phase
+// for the one awaited.  The launch keeps stages·KB <= kGatherWarps.
+constexpr int kGatherWarps = 6;
+constexpr int threads_for(bool gather) {
+  return 32 * (kEpiWarp0 + kEpiWarps + (gather ? kGatherWarps - 1 : 0));
+}
 constexpr int kEpiBufBytes = 32 * 64;   // per epilogue warp: 32 rows × 32 bf16
 constexpr uint32_t kTmemCols = 512;
 constexpr int kAccCols = 256;           // each of the two accumulators owns 256 columns
@@ -88,8 +99,9 @@ enum { kActNone = -1 };
 // measured ~640 clocks per k-block with one k-block per stage, more than the
 // ~560 clocks a 256 × 256 × 64 pair MMA keeps the tensor pipe busy, so the
 // pair kernel stages two k-blocks (64 KiB per CTA, 3 stages).  The one-CTA
-// kernel (96 KiB per two k-blocks: only 2 stages would fit) and the gathering
-// producer keep one.
+// kernel (96 KiB per two k-blocks: only 2 stages would fit) keeps one, and so
+// does the gathering kernel, whose copies, not its MMA thread, set the pace
+// (two k-blocks per stage measured 4-8% slower there).
 __host__ __device__ constexpr int stage_kblocks(bool pair, bool gather) {
   return pair && !gather ? 2 : 1;
 }
@@ -323,7 +335,7 @@ __global__ void __launch_bounds__(256)
 // of [MoE Gate 分布式通信 mianshidashi, 06].  Every lane of warp 0 then
 // issues TMA gather4 copies of four rows each, while lane 0 still loads B.
 template <int ACT, bool PAIR, bool GATHER, int CK>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_for(GATHER), 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    int E, int N, int K, int BN, const int32_t* __restrict__ offsets,
                    const float* __restrict__ bias, __nv_bfloat16* __restrict__ out,
@@ -436,14 +448,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     set_status(status, MOE_ERR_TIMEOUT);
   };
 
-  if (warp == 0 && GATHER) {
+  if (GATHER && (warp == 0 || warp >= kEpiWarp0 + kEpiWarps)) {
     // ---------------- gathering producer (whole warp) ----------------
     // Lane j gathers rows 4j .. 4j+3 of the 128-row A tile with one TMA
     // gather4 per k-block into bytes [512j, 512j + 512) of the stage: the
     // same 128-byte-swizzled layout a 64 × 128 box would write (each stage is
     // 1024-byte aligned).  Rows past the expert's end read token row 0 (they
     // are computed but never stored); lane 0 waits for the slot, posts the
-    // stage's byte count and loads B.
+    // stage's byte count and loads B.  Gathering warp gw (warp 0, then the
+    // warps after the epilogue) serves the stages s with s mod kGatherWarps
+    // == gw (all warps walk the same iteration sequence).
+    const int gw = warp == 0 ? 0 : warp - (kEpiWarp0 + kEpiWarps) + 1;
+    const int my_stage = gw / KB, my_half = gw % KB;
+    const int nk64 = (K + kTileK - 1) / kTileK;  // 64-wide k-blocks
     int stage = 0;
     uint32_t phase = 0;
     int64_t issued = 0;
@@ -459,6 +476,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         t4[q] = (t >= 0 && int64_t(t) < gx_rows) ? t : 0;
       }
       for (int kb = 0; kb < nk; ++kb) {
+        if (stage != my_stage) {  // another warp's stage
+          ++issued;
+          if (++stage == stages) stage = 0, phase ^= 1u;
+          continue;
+        }
         int free_slot = 1;
         if (lane == 0)
           free_slot = tc::mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, kWaitLimitNs);
@@ -467,32 +489,43 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        uint8_t* dst = sA + stage * a_bytes + lane * 512;
+        // This warp's k-block of the stage; a half past K (K/64 odd) is
+        // neither copied nor multiplied, and the stage's byte count (posted
+        // by the half-0 warp) leaves it out.
+        const int kblk = kb * KB + my_half;
+        const int halves = min(KB, nk64 - kb * KB);
+        const uint32_t stage_tx = uint32_t(halves) * (a_box + b_box);
+        uint8_t* dst = sA + stage * a_bytes + my_half * a_box + lane * 512;
+        uint8_t* dstB = sB + stage * b_bytes + my_half * b_box;
         if constexpr (PAIR) {
           const uint32_t bar = tc::mapa(tc::smem_u32(&full_bar[stage]), 0);
           if (lane == 0) {
-            if (rank == 0) tc::mbar_arrive_expect_tx(&full_bar[stage], 2 * (a_bytes + b_bytes));
-            tc::tma_load_3d_pair(&tmB, bar, sB + stage * b_bytes, kb * kTileK,
-                                 c.n0 + int(rank) * bn_cta, c.e);
+            if (rank == 0 && my_half == 0) tc::mbar_arrive_expect_tx(&full_bar[stage], 2 * stage_tx);
+            if (kblk < nk64)
+              tc::tma_load_3d_pair(&tmB, bar, dstB, kblk * kTileK, c.n0 + int(rank) * bn_cta,
+                                   c.e);
           }
           __syncwarp();
-          tc::tma_gather4_pair(&tmA, bar, dst, kb * kTileK, t4[0], t4[1], t4[2], t4[3]);
+          if (kblk < nk64)
+            tc::tma_gather4_pair(&tmA, bar, dst, kblk * kTileK, t4[0], t4[1], t4[2], t4[3]);
         } else {
           if (lane == 0) {
-            tc::mbar_arrive_expect_tx(&full_bar[stage], a_bytes + b_bytes);
-            tc::tma_load_3d(&tmB, &full_bar[stage], sB + stage * b_bytes, kb * kTileK, c.n0,
-                            c.e);
+            if (my_half == 0) tc::mbar_arrive_expect_tx(&full_bar[stage], stage_tx);
+            if (kblk < nk64)
+              tc::tma_load_3d(&tmB, &full_bar[stage], dstB, kblk * kTileK, c.n0, c.e);
           }
           __syncwarp();
-          tc::tma_gather4(&tmA, &full_bar[stage], dst, kb * kTileK, t4[0], t4[1], t4[2], t4[3]);
+          if (kblk < nk64)
+            tc::tma_gather4(&tmA, &full_bar[stage], dst, kblk * kTileK, t4[0], t4[1], t4[2],
+                            t4[3]);
         }
         ++issued;
         if (++stage == stages) stage = 0, phase ^= 1u;
       }
     }
-    // Drain as the TMA producer does: the last `stages` stages land before
-    // the CTA exits.
-    if (rank == 0 && lane == 0) {
+    // Drain as the TMA producer does: the last `stages` stages (of every
+    // gathering warp) land before the CTA exits.
+    if (gw == 0 && rank == 0 && lane == 0) {
       const int64_t first = issued > stages ? issued - stages : 0;
       for (int64_t j = first; j < issued; ++j)
         tc::mbar_wait(&full_bar[j % stages], uint32_t((j / stages) & 1), nullptr, kWaitLimitNs);
@@ -576,8 +609,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t a0 = tc::smem_u32(sA + stage * a_bytes);
         const uint32_t b0 = tc::smem_u32(sB + stage * b_bytes);
         const uint64_t ad0 = tc::sdesc_kmajor_sw128(a0), bd0 = tc::sdesc_kmajor_sw128(b0);
+        // The gathering producer copies no k-block past K (K/64 odd).
+        const int mma_steps =
+            GATHER ? min(KB, (K + kTileK - 1) / kTileK - kb * KB) * (kTileK / 16) : KB * kTileK / 16;
 #pragma unroll
         for (int j = 0; j < KB * kTileK / 16; ++j) {
+          if (GATHER && j >= mma_steps) break;
           const uint32_t h = uint32_t(j / (kTileK / 16)), q = uint32_t(j % (kTileK / 16));
           const uint64_t ad = tc::sdesc_advance(ad0, h * a_box + q * 32);
           const uint64_t bd = tc::sdesc_advance(bd0, h * b_box + q * 32);
@@ -605,7 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     else
       tc::mma_commit(&drain_bar);
     tc::mbar_wait(&drain_bar, 0, nullptr, kWaitLimitNs);
-  } else if (warp >= kEpiWarp0) {
+  } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + kEpiWarps) {
     // ---------------- epilogue ----------------
     const int quarter = warp & 3;              // TMEM lanes [32·quarter, 32·quarter+32)
     const int half = (warp - kEpiWarp0) >> 2;  // columns [c_lo, c_hi) of the tile
@@ -779,6 +816,9 @@ cudaError_t launch_variant(int act, const CUtensorMap& tmA, const CUtensorMap& t
   const size_t budget = size_t(device_smem_optin()) - static_smem;
   int stages = budget > fixed ? int((budget - fixed) / stage_bytes) : 0;
   if (stages > kMaxStages) stages = kMaxStages;
+  // Every stage half needs its own gathering warp.
+  if (GATHER && stages * stage_kblocks(PAIR, true) > kGatherWarps)
+    stages = kGatherWarps / stage_kblocks(PAIR, true);
   if (stages < 2) return cudaErrorInvalidValue;
   const size_t smem = fixed + size_t(stages) * stage_bytes;
   auto run = [&](auto kernel) {
@@ -787,7 +827,7 @@ cudaError_t launch_variant(int act, const CUtensorMap& tmA, const CUtensorMap& t
     unsigned grid = unsigned(sms);
     cudaLaunchConfig_t cfg{};
     cudaLaunchAttribute attr[2];
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(threads_for(GATHER));
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     if constexpr (PAIR) {

@@ -60,6 +60,11 @@ CASES = {
         wl=W["bf16_t4096_d1024_e8_top2"].replace(T=2000, d=1000, d_ff=512,
                                                  capacity_factor=0.8),
         e2e_tokens=128),
+    # K = d = 960: 15 64-wide k-blocks, so the last pipeline stage of two
+    # holds one (the gathering producer copies no k-block past K); the
+    # second GEMM's K = d_ff = 704 has 11
+    "t1500_d960_e8_top2_odd_k": dict(
+        wl=W["bf16_t4096_d1024_e8_top2"].replace(T=1500, d=960, d_ff=704), e2e_tokens=128),
     # 256 experts: pair launch on whole 256-row tiles plus the overlapped
     # one-CTA tail launch, every remainder size
     "t12000_d256_e256_top8_tail": dict(
