@@ -301,6 +301,15 @@ moe_status_t moe_forward(const moe_config_t* cfg, const moe_tensors_t* t, float 
 moe_status_t moe_selftest_wait_timeout(void* ws, size_t ws_bytes, int64_t limit_ns,
                                        void* stream);
 
+/* Self-test of the one-pass dispatch's grid barrier (moe_dispatch with
+ * T > 256 and no reroute runs one cooperative grid whose blocks meet at a
+ * barrier in the workspace header): two blocks wait for three arrivals, give
+ * up after limit_ns nanoseconds (1e6 <= limit_ns <= 4e9; the dispatch's own
+ * limit is 4 s), record MOE_ERR_TIMEOUT in the workspace status word and
+ * return; the barrier's counters return to zero.  For tests. */
+moe_status_t moe_selftest_grid_barrier_timeout(void* ws, size_t ws_bytes, int64_t limit_ns,
+                                               void* stream);
+
 /* Read the workspace's device status word (a blocking copy; call after the
  * stream that used ws has been synchronised).  *status is MOE_OK or the
  * first asynchronous error recorded. */

@@ -189,6 +189,7 @@ struct Ws {
   int32_t* status;
   int* route_counter;     // grid-completion counters (inside the status block)
   int* dispatch_counter;
+  int* dispatch_barrier;  // int [2] for the one-pass dispatch's grid barrier
   int32_t* chunk_counts;
   float* psum_partial;
   float* route_part;
@@ -209,6 +210,7 @@ static moe_status_t get_ws(const moe_config_t& c, void* ws, size_t ws_bytes, Ws*
   out->status = reinterpret_cast<int32_t*>(b + L.status);
   out->route_counter = reinterpret_cast<int*>(b + L.status + kWsRouteCounter);
   out->dispatch_counter = reinterpret_cast<int*>(b + L.status + kWsDispatchCounter);
+  out->dispatch_barrier = reinterpret_cast<int*>(b + L.status + kWsDispatchBarrier);
   out->chunk_counts = reinterpret_cast<int32_t*>(b + L.chunk_counts);
   out->psum_partial = reinterpret_cast<float*>(b + L.psum_partial);
   out->route_part = reinterpret_cast<float*>(b + L.route_part);
@@ -402,7 +404,7 @@ static moe_status_t dispatch_impl(const moe_config_t* cfg, const void* x,
   const int64_t C = capacity_of(cfg->T, cfg->k, cfg->E, cfg->capacity_factor);
   cudaError_t e = launch_dispatch(*cfg, C, x, topk_ids, counts, kept, offsets, slot_row,
                                   row_token, xd, w.chunk_counts, w.status, w.dispatch_counter,
-                                  aux, cfg->reroute ? &w.rr : nullptr,
+                                  w.dispatch_barrier, aux, cfg->reroute ? &w.rr : nullptr,
                                   static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_dispatch");
 }
@@ -601,6 +603,19 @@ moe_status_t moe_selftest_wait_timeout(void* ws, size_t ws_bytes, int64_t limit_
   cudaError_t e = launch_wait_timeout_selftest(static_cast<int32_t*>(ws), uint64_t(limit_ns),
                                                static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_selftest_wait_timeout");
+}
+
+moe_status_t moe_selftest_grid_barrier_timeout(void* ws, size_t ws_bytes, int64_t limit_ns,
+                                               void* stream) {
+  if (!ws || ws_bytes < kWsHeaderBytes)
+    return fail(MOE_ERR_INVALID_ARG, "moe_selftest_grid_barrier_timeout: workspace too small");
+  if (limit_ns < 1000000 || limit_ns > 4000000000LL)
+    return fail(MOE_ERR_INVALID_ARG, "moe_selftest_grid_barrier_timeout: limit_ns out of range");
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  cudaError_t e = launch_grid_barrier_timeout_selftest(
+      reinterpret_cast<int*>(b + kWsDispatchBarrier), reinterpret_cast<int32_t*>(b),
+      uint64_t(limit_ns), static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_selftest_grid_barrier_timeout");
 }
 
 moe_status_t moe_get_device_status(const void* ws, int32_t* status) {

@@ -41,6 +41,7 @@ constexpr int kPsumReplicas = 32;       // copies of the accumulator, spread ove
 constexpr int kPsumFixedMaxE = 1024;
 constexpr size_t kWsRouteCounter = 64;
 constexpr size_t kWsDispatchCounter = 128;
+constexpr size_t kWsDispatchBarrier = 192;  // int [2]: arrivals, departures
 constexpr size_t kWsPsumFixed = 16384;  // uint64 [kPsumReplicas][kPsumFixedMaxE]
 constexpr size_t kWsHeaderBytes =
     kWsPsumFixed + size_t(kPsumReplicas) * kPsumFixedMaxE * sizeof(unsigned long long);
@@ -254,6 +255,54 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 // Record the first asynchronous error in the status word.
 __device__ __forceinline__ void set_status(int32_t* status, int32_t code) {
   if (status) atomicCAS(status, 0, code);
+}
+
+// Grid-wide barrier of a cooperative launch (every block resident at once):
+// each block arrives on bar[0], then waits until `expect` blocks have arrived.
+// The wait is bounded: after limit_ns it records MOE_ERR_TIMEOUT and returns
+// false, so a block that never arrives cannot hang the grid.  Every block
+// then calls grid_barrier_depart (also after a timeout); the last to depart
+// resets both counters, ready for the next launch.  s_ok: one int of shared
+// memory.
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ bool grid_barrier_wait(int* bar, int expect, int32_t* status,
+                                                  uint64_t limit_ns, int* s_ok) {
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    atomicAdd(bar, 1);
+    uint64_t t0;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+    int ok = 1;
+    while (ld_acquire_gpu(bar) < expect) {
+      uint64_t t;
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+      if (t - t0 > limit_ns) {
+        ok = 0;
+        set_status(status, MOE_ERR_TIMEOUT);
+        break;
+      }
+      __nanosleep(64);
+    }
+    *s_ok = ok;
+  }
+  __syncthreads();
+  __threadfence();
+  return *s_ok != 0;
+}
+__device__ __forceinline__ void grid_barrier_depart(int* bar) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(bar + 1, 1) == int(gridDim.x) - 1) {
+      atomicExch(bar, 0);
+      atomicExch(bar + 1, 0);
+    }
+  }
 }
 
 template <typename T>

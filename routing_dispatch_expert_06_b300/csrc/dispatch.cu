@@ -22,6 +22,9 @@
 //      per step: slot_row, row_token
 // and a fourth, bandwidth-bound pass copies each token row once from x and
 // writes it to every kept slot with 16-byte vectors.
+#include <cstdlib>
+#include <cstring>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -415,6 +418,124 @@ __global__ void __launch_bounds__(kDispatchThreads)
   walk_slots(T, E, k, C, 0, s_ids, wbase + warp * E, off, slot_row, row_token, 0);
 }
 
+// T > 256 in one launch: a cooperative grid (every block resident) of one
+// block per 256-token chunk plus one summary block.  Each chunk block counts
+// its chunk (the warps' histograms in shared memory), publishes the chunk's
+// counts and meets the others at a bounded grid barrier; then it reads all
+// chunks' counts, forms kept, the expert offsets and its own chunk's base per
+// expert (the counts of the chunks before it) and walks its slots.  The
+// summary block (the last one) loads the router's column sums before the
+// barrier, and after it writes counts, kept and offsets and runs the
+// statistics, in parallel with the chunk blocks' walks.  The results are those
+// of histogram_kernel + assign_kernel.  Dynamic shared memory: off[E+1] |
+// wbase[8][E] | ids[256·k] | counts[E] | kept[E] | psum[E].
+__global__ void __launch_bounds__(kDispatchThreads)
+    dispatch_onepass_kernel(int64_t T, int E, int k, int64_t C, const int32_t* __restrict__ ids,
+                            int32_t* __restrict__ chunk_counts, int32_t* status, int* bar,
+                            int expect, uint64_t limit_ns, int32_t* __restrict__ counts,
+                            int32_t* __restrict__ kept, AuxArgs aux,
+                            int32_t* __restrict__ offsets, int32_t* __restrict__ slot_row,
+                            int32_t* __restrict__ row_token) {
+  extern __shared__ int32_t sm[];
+  int32_t* off = sm;                                     // [E+1]
+  int32_t* wbase = off + E + 1;                          // [8][E]
+  int32_t* s_ids = wbase + 8 * E;                        // [256·k]
+  int32_t* s_cnt = s_ids + kChunkTokens * k;             // [E]
+  int32_t* s_kept = s_cnt + E;                           // [E]
+  float* s_psum = reinterpret_cast<float*>(s_kept + E);  // [E]
+  __shared__ int32_t part[kDispatchThreads];
+  __shared__ float s_red[kAuxThreads];
+  __shared__ unsigned long long s_kept_sum;
+  __shared__ int s_ok;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int nb = int(gridDim.x) - 1;                     // chunk blocks
+  const bool summary = int(blockIdx.x) == nb;
+  const int64_t chunk0 = int64_t(blockIdx.x) * kChunkTokens;
+  for (int i = tid; i < 8 * E; i += kDispatchThreads) wbase[i] = 0;
+  pdl_wait();
+  pdl_trigger();
+  if (summary) {
+    // psum from the router's fixed-point column sums (psum_from_fixed's
+    // arithmetic), or as given; independent of the counts, so before the
+    // barrier.
+    if (aux.f)
+      for (int c = tid; c < E; c += kDispatchThreads) {
+        float pv;
+        if (aux.psum_fixed) {
+          unsigned long long fx = 0;
+#pragma unroll 8
+          for (int r = 0; r < kPsumReplicas; ++r) fx += __ldcg(aux.psum_fixed + r * kPsumFixedMaxE + c);
+#pragma unroll 8
+          for (int r = 0; r < kPsumReplicas; ++r) __stcg(aux.psum_fixed + r * kPsumFixedMaxE + c, 0ull);
+          pv = float(double(fx) * kPsumFixInv);
+          aux.psum[c] = pv;
+        } else {
+          pv = __ldcg(aux.psum + c);
+        }
+        s_psum[c] = pv;
+      }
+  } else {
+    const int64_t n_tok = T - chunk0 < kChunkTokens ? T - chunk0 : kChunkTokens;
+    for (int64_t i = tid; i < n_tok * k; i += kDispatchThreads) s_ids[i] = ids[chunk0 * k + i];
+    __syncthreads();
+    if (tid < n_tok)
+      for (int r = 0; r < k; ++r) {
+        const int e = s_ids[tid * k + r];
+        if (e >= 0 && e < E)
+          atomicAdd(&wbase[warp * E + e], 1);
+        else
+          set_status(status, MOE_ERR_INVALID_ARG);
+      }
+    __syncthreads();
+    // wbase[w][e] <- counts of e in warps before w; the chunk's count of e.
+    for (int e = tid; e < E; e += kDispatchThreads) {
+      int32_t acc = 0;
+      for (int w = 0; w < 8; ++w) {
+        const int32_t v = wbase[w * E + e];
+        wbase[w * E + e] = acc;
+        acc += v;
+      }
+      __stcg(chunk_counts + int64_t(blockIdx.x) * E + e, acc);
+    }
+  }
+  if (grid_barrier_wait(bar, expect, status, limit_ns, &s_ok)) {
+    // Every chunk's counts: the totals, and (chunk blocks) this chunk's base
+    // per expert.
+    for (int e = tid; e < E; e += kDispatchThreads) {
+      int32_t tot = 0, base = 0;
+#pragma unroll 8
+      for (int b = 0; b < nb; ++b) {
+        const int32_t v = __ldcg(chunk_counts + int64_t(b) * E + e);
+        base += b < int(blockIdx.x) ? v : 0;
+        tot += v;
+      }
+      const int32_t kp = int32_t(tot < C ? tot : C);
+      s_cnt[e] = tot;
+      s_kept[e] = kp;
+      if (summary) {
+        counts[e] = tot;
+        kept[e] = kp;
+      } else {
+        for (int w = 0; w < 8; ++w) wbase[w * E + e] += base;
+      }
+    }
+    __syncthreads();
+    block_exclusive_scan(E, s_kept, off, part);
+    if (summary) {
+      for (int e = tid; e <= E; e += kDispatchThreads) offsets[e] = off[e];
+      if (aux.f)
+        aux_stats_block<true>(E, T, aux.alpha, s_cnt, s_psum, aux.f, aux.pbar, aux.l_aux, s_red);
+      if (aux.health) {
+        __syncthreads();
+        routing_health_block<true>(E, T, k, s_cnt, s_kept, aux.health, s_red, &s_kept_sum);
+      }
+    } else {
+      walk_slots(T, E, k, C, chunk0, s_ids, wbase + warp * E, off, slot_row, row_token, 0);
+    }
+  }
+  grid_barrier_depart(bar);
+}
+
 // Overflow reroute, step 2: the m-th slot of token t that the first fill
 // dropped (pos0 < 0), in rank order, is offered to cand[t*k + m]; other slots
 // offer nothing (-1).  One thread per token.
@@ -512,10 +633,28 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// The one-pass dispatch (dispatch_onepass_kernel) when every chunk's block
+// can be resident at once (MOE_DISPATCH_ONEPASS=0 turns it off, a
+// cross-check in tests).
+constexpr uint64_t kGridBarrierLimitNs = 4000000000ull;  // 4 s
+bool onepass_fits(const moe_config_t& c, int64_t n_chunks) {
+  const char* v = std::getenv("MOE_DISPATCH_ONEPASS");
+  if (v && std::strcmp(v, "0") == 0) return false;
+  const size_t smem = size_t(c.E + 1 + 8 * c.E + kChunkTokens * c.k + 3 * c.E) * 4;
+  if (ensure_dynamic_smem(reinterpret_cast<const void*>(dispatch_onepass_kernel), smem) !=
+      cudaSuccess)
+    return false;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dispatch_onepass_kernel,
+                                                    kDispatchThreads, smem) != cudaSuccess)
+    return false;
+  return n_chunks + 1 <= int64_t(per_sm) * device_sms();
+}
+
 cudaError_t launch_dispatch(const moe_config_t& c, int64_t C, const void* x,
                             const int32_t* ids, int32_t* counts, int32_t* kept,
                             int32_t* offsets, int32_t* slot_row, int32_t* row_token, void* xd,
-                            int32_t* chunk_counts, int32_t* status, int* counter,
+                            int32_t* chunk_counts, int32_t* status, int* counter, int* grid_bar,
                             const AuxArgs* aux, const RerouteBufs* rr, cudaStream_t st) {
   if (rr && !counter) return cudaErrorInvalidValue;
   const int64_t n_chunks = (c.T + kChunkTokens - 1) / kChunkTokens;
@@ -549,6 +688,27 @@ cudaError_t launch_dispatch(const moe_config_t& c, int64_t C, const void* x,
     err = launch_pdl(dispatch_small_kernel, dim3(1), dim3(kDispatchThreads), small_smem, st, c.T,
                      c.E, c.k, C, ids, status, counts, kept, aux_v, offsets, slot_row,
                      row_token);
+    count_launch();
+    if (err != cudaSuccess || (err = cudaGetLastError()) != cudaSuccess) return err;
+  } else if (!rr && grid_bar && counter && onepass_fits(c, n_chunks)) {
+    const size_t smem = assign_smem + size_t(3 * c.E) * 4;
+    err = ensure_dynamic_smem(reinterpret_cast<const void*>(dispatch_onepass_kernel), smem);
+    if (err != cudaSuccess) return err;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(unsigned(n_chunks + 1));  // the chunks and the summary block
+    cfg.blockDim = dim3(kDispatchThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;  // every block resident: the grid barrier
+    attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    err = cudaLaunchKernelEx(&cfg, dispatch_onepass_kernel, c.T, c.E, c.k, C, ids, chunk_counts,
+                             status, grid_bar, int(n_chunks + 1), kGridBarrierLimitNs, counts, kept,
+                             aux_v, offsets, slot_row, row_token);
     count_launch();
     if (err != cudaSuccess || (err = cudaGetLastError()) != cudaSuccess) return err;
   } else if (!rr) {

@@ -95,7 +95,8 @@ extern "C" moe_status_t moe_dispatch_noalloc(const moe_config_t* cfg, const void
     return report_error(MOE_ERR_CUDA, "moe_dispatch_noalloc: cudaGetSymbolAddress failed");
   const int64_t C = moe_capacity(cfg);
   e = launch_dispatch(*cfg, C, x, topk_ids, counts, kept, offsets, slot_row, row_token, xd,
-                      scratch, status, nullptr, nullptr, nullptr, static_cast<cudaStream_t>(stream));
+                      scratch, status, nullptr, nullptr, nullptr, nullptr,
+                      static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MOE_OK
                           : report_error(MOE_ERR_CUDA, "moe_dispatch_noalloc: launch failed");
 }

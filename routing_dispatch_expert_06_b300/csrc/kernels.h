@@ -84,6 +84,8 @@ cudaError_t launch_route_select(const moe_config_t& c, const float* part, int ns
 // One block waits on an mbarrier nothing signals, gives up after limit_ns and
 // records MOE_ERR_TIMEOUT in *status (self-test of the bounded waits).
 cudaError_t launch_wait_timeout_selftest(int32_t* status, uint64_t limit_ns, cudaStream_t st);
+cudaError_t launch_grid_barrier_timeout_selftest(int* bar, int32_t* status, uint64_t limit_ns,
+                                                 cudaStream_t st);
 // One block: the routing-health indicators from counts and kept.
 cudaError_t launch_health(const moe_config_t& c, const int32_t* counts, const int32_t* kept,
                           float* health, cudaStream_t st);
@@ -105,11 +107,13 @@ struct RerouteBufs {
 // f / p̄ / L_aux statistics), or NULL for a separate scan kernel.  rr (needs
 // counter): the reroute variant (first fill as positions, offers, second
 // fill into the room left, final rows).  xd == NULL: positions and row_token
-// only, no row copy (the first GEMM then gathers its rows).
+// only, no row copy (the first GEMM then gathers its rows).  grid_bar: two
+// zeroed ints for the one-pass kernel's grid barrier (T > 256 without reroute,
+// when the whole grid fits on the device at once), or NULL.
 cudaError_t launch_dispatch(const moe_config_t& c, int64_t C, const void* x,
                             const int32_t* ids, int32_t* counts, int32_t* kept,
                             int32_t* offsets, int32_t* slot_row, int32_t* row_token, void* xd,
-                            int32_t* chunk_counts, int32_t* status, int* counter,
+                            int32_t* chunk_counts, int32_t* status, int* counter, int* grid_bar,
                             const AuxArgs* aux, const RerouteBufs* rr, cudaStream_t st);
 
 // Grouped GEMM on CUDA cores over ragged expert row ranges (fp32 or bf16):

@@ -85,6 +85,7 @@ def load():
         "moe_forward": (st, [cfgp, ctypes.POINTER(Tensors), ctypes.c_float, _P, sz, _P]),
         "moe_get_device_status": (st, [_P, ctypes.POINTER(ctypes.c_int32)]),
         "moe_selftest_wait_timeout": (st, [_P, sz, i64, _P]),
+        "moe_selftest_grid_barrier_timeout": (st, [_P, sz, i64, _P]),
         "moe_launch_count": (i64, []),
         "moe_status_string": (ctypes.c_char_p, [st]),
         "moe_last_error": (ctypes.c_char_p, []),
@@ -335,6 +336,14 @@ def selftest_wait_timeout(ws, limit_ns: int, stream=None):
     """moe_selftest_wait_timeout: a bounded wait that must give up and record
     MOE_ERR_TIMEOUT in the workspace status word."""
     _check(load().moe_selftest_wait_timeout(_ptr(ws), ws.numel(), int(limit_ns), _stream(stream)))
+
+
+def selftest_grid_barrier_timeout(ws, limit_ns: int, stream=None):
+    """moe_selftest_grid_barrier_timeout: the one-pass dispatch's grid barrier
+    waiting for a block that never arrives must give up and record
+    MOE_ERR_TIMEOUT in the workspace status word."""
+    _check(load().moe_selftest_grid_barrier_timeout(_ptr(ws), ws.numel(), int(limit_ns),
+                                                    _stream(stream)))
 
 
 def workspace_init(ws, stream=None):

@@ -148,6 +148,8 @@ def test_new_entry_points_reject_null_arguments(lib):
 
 def test_selftest_rejects_bad_arguments(lib):
     assert lib.moe_selftest_wait_timeout(None, 0, 10**7, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_selftest_grid_barrier_timeout(None, 0, 10**7, None) == \
+        moe.MOE_ERR_INVALID_ARG
 
 
 def test_fuse_dispatch_flag_and_gather_scope(lib):

@@ -335,3 +335,68 @@ def test_bounded_wait_gives_up_and_reports_timeout():
     torch.cuda.synchronize()
     assert moe.device_status(ws) == moe.MOE_OK
     check_forward(wl, inp, out, n_tokens=256)
+
+
+def test_grid_barrier_gives_up_and_reports_timeout():
+    # The one-pass dispatch's grid barrier, waiting for one block more than
+    # the grid holds, must give up after its limit and record MOE_ERR_TIMEOUT;
+    # its counters return to zero, so a whole layer with a one-pass dispatch
+    # (T > 256) then runs correctly on the same workspace.
+    import time
+
+    wl = W["bf16_t8192_d2048_e64_top6"].replace(T=3000)
+    cfg = moe.config_from_workload(wl, write_logits=True)
+    ws = moe.workspace(cfg)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    moe.selftest_grid_barrier_timeout(ws, 50_000_000)  # 50 ms
+    torch.cuda.synchronize()
+    assert time.time() - t0 < 5.0
+    assert moe.device_status(ws) == moe.MOE_ERR_TIMEOUT
+    moe.workspace_init(ws)
+    torch.cuda.synchronize()
+    inp = inputs.make_inputs(wl, "cuda")
+    out = moe.allocate(cfg)
+    moe.forward(cfg, inp, out, ws, 1.0)
+    torch.cuda.synchronize()
+    assert moe.device_status(ws) == moe.MOE_OK
+    check_forward(wl, inp, out, n_tokens=256)
+
+
+ONEPASS_CASES = [
+    ("e64_top6", W["bf16_t8192_d2048_e64_top6"].replace(T=3000), False),
+    ("e256_top8_ragged", W["bf16_t32768_d7168_e256_top8"].replace(T=12001, d=256, d_ff=512,
+                                                                  capacity_factor=2.0), True),
+    ("e8_top2_full", W["bf16_t4096_d1024_e8_top2"], False),
+    ("e1024_top16", inputs.Workload("e1024", 700, 64, 64, 1024, 16, 1.0, True, "gelu_tanh",
+                                    "bf16", 5, "normal:1.0"), True),
+]
+
+
+@pytest.mark.parametrize("name,wl,extras", ONEPASS_CASES, ids=[c[0] for c in ONEPASS_CASES])
+def test_one_pass_dispatch_equals_two_kernel_dispatch(name, wl, extras):
+    # With T > 256 (and no reroute) the dispatch is one cooperative grid
+    # (counts, capacity, offsets and positions in one launch behind a grid
+    # barrier); MOE_DISPATCH_ONEPASS=0 runs the histogram and assign kernels.
+    # Every integer output, the permuted rows and the statistics (with the
+    # selection bias and the routing-health outputs) must be identical.
+    inp = inputs.make_inputs(wl, "cuda")
+    if extras:
+        inp["sel_bias"] = inputs.selection_bias(wl, "cuda")
+    _, _, out1, ws1 = run_gpu(wl, inp=inp, health=extras)
+    os.environ["MOE_DISPATCH_ONEPASS"] = "0"
+    try:
+        _, _, out2, ws2 = run_gpu(wl, inp=inp, health=extras)
+    finally:
+        del os.environ["MOE_DISPATCH_ONEPASS"]
+    assert moe.device_status(ws1) == moe.MOE_OK and moe.device_status(ws2) == moe.MOE_OK
+    names = ["counts", "kept", "offsets", "slot_row", "psum", "f", "pbar", "l_aux", "y"]
+    if extras:
+        names.append("health")
+    for n_ in names:
+        assert torch.equal(out1[n_], out2[n_]), n_
+    n = int(h(out1["offsets"])[-1])
+    for n_ in ["row_token", "xd"]:
+        assert torch.equal(out1[n_][:n], out2[n_][:n]), n_
+    check_forward(wl, inp, out1, n_tokens=256, e2e_tokens=32)
+
