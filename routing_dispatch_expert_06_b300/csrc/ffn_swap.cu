@@ -205,15 +205,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t first = issued > stages ? issued - stages : 0;
     for (int64_t j = first; j < issued; ++j)
       tc::mbar_wait(&full_bar[j % stages], uint32_t((j / stages) & 1), nullptr, kWaitLimitNs);
-  } else if (warp == 1 && lane == 0) {
-    // ---------------- MMA issuer ----------------
+  } else if (warp == 1) {
+    // ---------------- MMA issuer (whole warp, one elected lane issues) -----
     int stage = 0;
     uint32_t phase = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
     for (int64_t i = blockIdx.x; i < total && ok; i += gridDim.x) {
-      if (!tc::mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort_flag, kWaitLimitNs)) {
+      // Waits are taken by every lane and agreed on, so the warp stays
+      // converged and its operands warp-uniform.
+      if (!__all_sync(0xffffffffu,
+                      tc::mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort_flag, kWaitLimitNs))) {
         give_up();
         break;
       }
@@ -225,7 +228,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n_mma = rows >= NT ? NT : ((rows + 15) / 16) * 16;
       const uint32_t idesc = tc::idesc_bf16_f32(kTileN, n_mma < 16 ? 16 : n_mma);
       for (int kb = 0; kb < nk; ++kb) {
-        if (!tc::mbar_wait(&full_bar[stage], phase, abort_flag, kWaitLimitNs)) {
+        if (!__all_sync(0xffffffffu,
+                        tc::mbar_wait(&full_bar[stage], phase, abort_flag, kWaitLimitNs))) {
           give_up();
           ok = false;
           break;
@@ -237,18 +241,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int j = 0; j < kBoxes * kTileK / 16; ++j) {
           const uint32_t h = uint32_t(j / (kTileK / 16)), q = uint32_t(j % (kTileK / 16));
-          tc::mma_bf16(d_tmem, tc::sdesc_advance(bd0, h * b_box + q * 32),
+          tc::mma_bf16_w(d_tmem, tc::sdesc_advance(bd0, h * b_box + q * 32),
                        tc::sdesc_advance(ad0, h * a_box + q * 32), idesc, (kb | j) != 0);
         }
-        tc::mma_commit(&empty_bar[stage]);
+        tc::mma_commit_w(&empty_bar[stage]);
         if (++stage == stages) stage = 0, phase ^= 1u;
       }
       if (!ok) break;
-      tc::mma_commit(&tfull_bar[acc]);
+      tc::mma_commit_w(&tfull_bar[acc]);
       if (++acc == 2) acc = 0, acc_phase ^= 1u;
     }
-    // Drain: every MMA this thread issued completes before TMEM is freed.
-    tc::mma_commit(&drain_bar);
+    // Drain: every MMA this warp issued completes before TMEM is freed.
+    tc::mma_commit_w(&drain_bar);
     tc::mbar_wait(&drain_bar, 0, nullptr, kWaitLimitNs);
   } else if (warp >= kEpiWarp0) {
     // ---------------- epilogue ----------------

@@ -580,8 +580,8 @@ __global__ void __launch_bounds__(threads_for(GATHER), 1)
       for (int64_t j = first; j < issued; ++j)
         tc::mbar_wait(&full_bar[j % stages], uint32_t((j / stages) & 1), nullptr, kWaitLimitNs);
     }
-  } else if (warp == 1 && lane == 0 && rank == 0) {
-    // ---------------- MMA issuer ----------------
+  } else if (warp == 1 && rank == 0) {
+    // ---------------- MMA issuer (whole warp, one elected lane issues) -----
     const uint32_t idesc = tc::idesc_bf16_f32(rows_per_tile, BN);
     int stage = 0;
     uint32_t phase = 0;
@@ -589,10 +589,13 @@ __global__ void __launch_bounds__(threads_for(GATHER), 1)
     uint32_t acc_phase = 0;
     bool ok = true;
     for (int64_t i = first_tile; i < total && ok; i += tile_step) {
-      const bool free_acc = PAIR ? tc::mbar_wait_cluster(&tempty_bar[acc], acc_phase ^ 1u,
-                                                         abort_flag, kWaitLimitNs)
-                                 : tc::mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort_flag,
-                                                 kWaitLimitNs);
+      // Waits are taken by every lane and agreed on, so the warp stays
+      // converged and its operands warp-uniform.
+      const bool free_acc = __all_sync(
+          0xffffffffu, PAIR ? tc::mbar_wait_cluster(&tempty_bar[acc], acc_phase ^ 1u, abort_flag,
+                                                    kWaitLimitNs)
+                            : tc::mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort_flag,
+                                            kWaitLimitNs));
       if (!free_acc) {
         give_up();
         break;
@@ -600,7 +603,8 @@ __global__ void __launch_bounds__(threads_for(GATHER), 1)
       tc::fence_after_sync();
       const uint32_t d_tmem = tmem_base + uint32_t(acc * kAccCols);
       for (int kb = 0; kb < nk; ++kb) {
-        if (!tc::mbar_wait(&full_bar[stage], phase, abort_flag, kWaitLimitNs)) {
+        if (!__all_sync(0xffffffffu,
+                        tc::mbar_wait(&full_bar[stage], phase, abort_flag, kWaitLimitNs))) {
           give_up();
           ok = false;
           break;
@@ -619,28 +623,28 @@ __global__ void __launch_bounds__(threads_for(GATHER), 1)
           const uint64_t ad = tc::sdesc_advance(ad0, h * a_box + q * 32);
           const uint64_t bd = tc::sdesc_advance(bd0, h * b_box + q * 32);
           if constexpr (PAIR)
-            tc::mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | j) != 0);
+            tc::mma_bf16_pair_w(d_tmem, ad, bd, idesc, (kb | j) != 0);
           else
-            tc::mma_bf16(d_tmem, ad, bd, idesc, (kb | j) != 0);
+            tc::mma_bf16_w(d_tmem, ad, bd, idesc, (kb | j) != 0);
         }
         if constexpr (PAIR)
-          tc::mma_commit_pair_mc(&empty_bar[stage], 0x3);
+          tc::mma_commit_pair_mc_w(&empty_bar[stage], 0x3);
         else
-          tc::mma_commit(&empty_bar[stage]);
+          tc::mma_commit_w(&empty_bar[stage]);
         if (++stage == stages) stage = 0, phase ^= 1u;
       }
       if (!ok) break;
       if constexpr (PAIR)
-        tc::mma_commit_pair_mc(&tfull_bar[acc], 0x3);
+        tc::mma_commit_pair_mc_w(&tfull_bar[acc], 0x3);
       else
-        tc::mma_commit(&tfull_bar[acc]);
+        tc::mma_commit_w(&tfull_bar[acc]);
       if (++acc == 2) acc = 0, acc_phase ^= 1u;
     }
-    // Drain: wait until every MMA this thread issued has completed.
+    // Drain: wait until every MMA this warp issued has completed.
     if constexpr (PAIR)
-      tc::mma_commit_pair(&drain_bar);
+      tc::mma_commit_pair_w(&drain_bar);
     else
-      tc::mma_commit(&drain_bar);
+      tc::mma_commit_w(&drain_bar);
     tc::mbar_wait(&drain_bar, 0, nullptr, kWaitLimitNs);
   } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + kEpiWarps) {
     // ---------------- epilogue ----------------

@@ -218,8 +218,8 @@ __global__ void __launch_bounds__(64 + 128 * G, 1)
         tc::mbar_wait(&full_bar[i % a.stages], uint32_t((i / a.stages) & 1), nullptr,
                       kWaitLimitNs);
     }
-  } else if (warp == 1 && lane == 0 && rank == 0) {
-    // ---------------- MMA issuer ----------------
+  } else if (warp == 1 && rank == 0) {
+    // ---------------- MMA issuer (whole warp, one elected lane issues) -----
     const uint32_t idesc = tc::idesc_bf16_f32(TILE, NP);
     int stage = 0;
     uint32_t phase = 0;
@@ -231,9 +231,12 @@ __global__ void __launch_bounds__(64 + 128 * G, 1)
       for (int sg = seg_lo; sg < seg_hi && ok; ++sg, ++seg_count) {
         const uint32_t buf = seg_count & 1u;
         const uint32_t par = ((seg_count >> 1) & 1u) ^ 1u;
-        const bool free_acc =
-            PAIR ? tc::mbar_wait_cluster(&tempty_bar[buf], par, abort_flag, kWaitLimitNs)
-                 : tc::mbar_wait(&tempty_bar[buf], par, abort_flag, kWaitLimitNs);
+        // Waits are taken by every lane and agreed on, so the warp stays
+        // converged and its operands warp-uniform.
+        const bool free_acc = __all_sync(
+            0xffffffffu, PAIR ? tc::mbar_wait_cluster(&tempty_bar[buf], par, abort_flag,
+                                                      kWaitLimitNs)
+                              : tc::mbar_wait(&tempty_bar[buf], par, abort_flag, kWaitLimitNs));
         if (!free_acc) {
           give_up();
           ok = false;
@@ -243,7 +246,8 @@ __global__ void __launch_bounds__(64 + 128 * G, 1)
         const uint32_t d_tmem = tmem_base + buf * uint32_t(NP);
         const int kb_end = min(nk, (sg + 1) * kSegBlocks);
         for (int kb = sg * kSegBlocks / KB; kb * KB < kb_end; ++kb) {
-          if (!tc::mbar_wait(&full_bar[stage], phase, abort_flag, kWaitLimitNs)) {
+          if (!__all_sync(0xffffffffu,
+                          tc::mbar_wait(&full_bar[stage], phase, abort_flag, kWaitLimitNs))) {
             give_up();
             ok = false;
             break;
@@ -259,29 +263,29 @@ __global__ void __launch_bounds__(64 + 128 * G, 1)
             const uint64_t ad = tc::sdesc_advance(ad0, h * a_box + q * 32);
             const uint64_t bd = tc::sdesc_advance(bd0, h * b_box + q * 32);
             if constexpr (PAIR)
-              tc::mma_bf16_pair(d_tmem, ad, bd, idesc, (first && j == 0) ? 0u : 1u);
+              tc::mma_bf16_pair_w(d_tmem, ad, bd, idesc, (first && j == 0) ? 0u : 1u);
             else
-              tc::mma_bf16(d_tmem, ad, bd, idesc, (first && j == 0) ? 0u : 1u);
+              tc::mma_bf16_w(d_tmem, ad, bd, idesc, (first && j == 0) ? 0u : 1u);
           }
           if constexpr (PAIR)
-            tc::mma_commit_pair_mc(&empty_bar[stage], 0x3);
+            tc::mma_commit_pair_mc_w(&empty_bar[stage], 0x3);
           else
-            tc::mma_commit(&empty_bar[stage]);
+            tc::mma_commit_w(&empty_bar[stage]);
           if (++stage == a.stages) stage = 0, phase ^= 1u;
         }
         if (ok) {
           if constexpr (PAIR)
-            tc::mma_commit_pair_mc(&tfull_bar[buf], 0x3);
+            tc::mma_commit_pair_mc_w(&tfull_bar[buf], 0x3);
           else
-            tc::mma_commit(&tfull_bar[buf]);
+            tc::mma_commit_w(&tfull_bar[buf]);
         }
       }
     }
-    // Drain: every MMA this thread issued completes before TMEM is freed.
+    // Drain: every MMA this warp issued completes before TMEM is freed.
     if constexpr (PAIR)
-      tc::mma_commit_pair(&drain_bar);
+      tc::mma_commit_pair_w(&drain_bar);
     else
-      tc::mma_commit(&drain_bar);
+      tc::mma_commit_w(&drain_bar);
     tc::mbar_wait(&drain_bar, 0, nullptr, kWaitLimitNs);
   } else if (warp >= 2) {
     // ---------------- epilogue ----------------
