@@ -195,7 +195,17 @@ moe_status_t moe_dispatch_noalloc(const moe_config_t* cfg, const void* x,
                                   void* xd, int32_t* status, void* stream);
 
 /* [MoE 模型原理 §1] First expert GEMM over the ragged groups given by
- * offsets: H[rows of e] = σ(xd[rows of e] W1[e]ᵀ + b1[e]). */
+ * offsets: H[rows of e] = σ(xd[rows of e] W1[e]ᵀ + b1[e]).
+ * Ordering: the GEMM kernels are launched with programmatic dependent launch.
+ * With at most 64 rows per expert (the swapped decode GEMM) the kernel reads
+ * offsets and starts copying weights as soon as it is scheduled, which can be
+ * before the previous kernel in the stream has finished (it still waits for
+ * that kernel before reading xd).  So offsets must not be written by a kernel
+ * that signals its dependents early (griddepcontrol.launch_dependents) before
+ * writing it; kernels that do not use griddepcontrol, copies, and every
+ * kernel of this library (each waits for its own predecessor before it
+ * signals) are fine.  The same holds for moe_ffn_down (which waits before
+ * reading H). */
 moe_status_t moe_ffn_up(const moe_config_t* cfg, const void* xd, const int32_t* offsets,
                         const void* W1, const float* b1, void* H, void* ws, size_t ws_bytes,
                         void* stream);

@@ -111,15 +111,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::tmem_alloc(&s_tmem, kTmemCols);
     tc::tmem_relinquish();
   }
-  // Launched with programmatic dependent launch: offsets and the A rows come
-  // from the previous kernels.
-  tc::grid_dependency_wait();
-  tc::grid_launch_dependents();
+  // Launched with programmatic dependent launch, so the grid may start while
+  // the previous kernel (the scatter, or the first GEMM) still runs.  The A
+  // rows come from that kernel and are read only after griddepcontrol.wait.
+  // offsets comes from a kernel before it, and every kernel of the layer
+  // waits for its own predecessor before it lets the next one start, so
+  // offsets is complete once this grid runs: the tile list, and (when every
+  // CTA has a tile) the first stages' weight copies, go ahead of the wait.
   // Prefix over experts with 1 .. expert_max rows: warp 0 scans runs of
-  // experts, one run per lane.  Offsets are clamped to [0, max_rows].
+  // experts, one run per lane.  Offsets are clamped to [0, max_rows] and read
+  // from L2 (no stale L1 line from an earlier launch).
   if (warp == 0) {
     auto clamp_row = [&](int e) {
-      const int32_t v = offsets[e];
+      const int32_t v = __ldcg(offsets + e);
       return int32_t(v < 0 ? 0 : (int64_t(v) > max_rows ? max_rows : v));
     };
     const int per = (E + 31) / 32;
@@ -154,6 +158,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t total = int64_t(s_tp[E]) * n_tn;
   const int nk = (K + kBoxes * kTileK - 1) / (kBoxes * kTileK);  // stages per tile
   volatile int* abort_flag = &s_abort;
+  // Early weight copies only when every CTA has a tile.  With fewer tiles
+  // than CTAs (T = 1 on the E = 64 layer: 66 and 96 tiles) they measured
+  // slower: the copies of a partial wave compete for HBM with the previous
+  // kernel's own weight stream, which is on the critical path.
+  const bool early_w = total >= int64_t(gridDim.x);
+  if (!early_w) {
+    tc::grid_dependency_wait();
+    tc::grid_launch_dependents();
+  }
   auto give_up = [&]() {
     *abort_flag = 1;
     set_status(status, MOE_ERR_TIMEOUT);
@@ -175,6 +188,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0 && lane == 0) {
     // ---------------- TMA producer ----------------
+    // The weight boxes of the first `stages` stages are issued before the
+    // previous kernel has finished (weights are inputs; each stage's full
+    // barrier already expects its A boxes too, so it cannot complete early).
+    int pre = 0;
+    if (early_w) {
+      int64_t i = blockIdx.x;
+      int kb = 0;
+      for (; pre < stages && i < total; ++pre) {
+        int e, n0;
+        tile_expert(i, e, n0);
+        tc::mbar_arrive_expect_tx(&full_bar[pre], a_bytes + b_bytes);
+#pragma unroll
+        for (int h = 0; h < kBoxes; ++h)
+          tc::tma_load_3d(&tmB, &full_bar[pre], sB + pre * b_bytes + h * b_box,
+                          (kb * kBoxes + h) * kTileK, n0, e);
+        if (++kb == nk) kb = 0, i += gridDim.x;
+      }
+    }
+    if (early_w) {
+      tc::grid_dependency_wait();
+      tc::grid_launch_dependents();
+    }
     int stage = 0;
     uint32_t phase = 0;
     int64_t issued = 0;
@@ -183,17 +218,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       int e, n0;
       tile_expert(i, e, n0);
       for (int kb = 0; kb < nk; ++kb) {
-        if (!tc::mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, kWaitLimitNs)) {
-          give_up();
-          ok = false;
-          break;
+        const bool early = issued < pre;  // weights already on their way
+        if (!early) {
+          if (!tc::mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, kWaitLimitNs)) {
+            give_up();
+            ok = false;
+            break;
+          }
+          // A second box past K (K/64 odd) reads zeros, which add nothing.
+          tc::mbar_arrive_expect_tx(&full_bar[stage], a_bytes + b_bytes);
         }
-        // A second box past K (K/64 odd) reads zeros, which add nothing.
-        tc::mbar_arrive_expect_tx(&full_bar[stage], a_bytes + b_bytes);
 #pragma unroll
         for (int h = 0; h < kBoxes; ++h) {
           const int kx = (kb * kBoxes + h) * kTileK;
-          tc::tma_load_3d(&tmB, &full_bar[stage], sB + stage * b_bytes + h * b_box, kx, n0, e);
+          if (!early)
+            tc::tma_load_3d(&tmB, &full_bar[stage], sB + stage * b_bytes + h * b_box, kx, n0, e);
           tc::tma_load_2d(&tmA, &full_bar[stage], sA + stage * a_bytes + h * a_box, kx,
                           s_off[e]);
         }
