@@ -393,19 +393,25 @@ __global__ void __launch_bounds__(threads_for(GATHER), 1)
       tc::tmem_relinquish();
     }
   }
-  // Launched with programmatic dependent launch: offsets and the A rows come
-  // from the previous kernels.  The tail launch instead starts while its pair
-  // launch runs (which has waited already) and waits at its end.
-  if (set != kTail) {
+  // Launched with programmatic dependent launch: the A rows come from the
+  // previous kernel, and the grid waits for it (griddepcontrol.wait) before
+  // anything but the tile list.  offsets comes from a kernel before that one
+  // (the dispatch, then the scatter or the first GEMM), and every kernel of
+  // the layer waits for its own predecessor before it lets the next start,
+  // so the tile list is built before the wait.  The gathering GEMM follows
+  // the dispatch itself and waits first.  The tail launch starts while its
+  // pair launch runs (which has waited already) and waits at its end.
+  if (GATHER && set != kTail) {
     tc::grid_dependency_wait();
     tc::grid_launch_dependents();
   }
   // Per-expert m-tile prefix: warp 0 scans runs of experts, one run per lane.
   // Row offsets are clamped to [0, max_rows] so that no tile can reach
-  // outside the buffers, whatever offsets holds.
+  // outside the buffers, whatever offsets holds; they are read through L2
+  // (no stale L1 line from an earlier launch).
   if (warp == 0) {
     auto clamp_row = [&](int e) {
-      const int32_t v = offsets[e];
+      const int32_t v = __ldcg(offsets + e);
       return int32_t(v < 0 ? 0 : (int64_t(v) > max_rows ? max_rows : v));
     };
     const int per = (E + 31) / 32;
@@ -430,6 +436,10 @@ __global__ void __launch_bounds__(threads_for(GATHER), 1)
       acc += tiles_in_set(b - a, set, rows_per_tile);
     }
     if (lane == 31) s_mt[E] = incl;
+  }
+  if (!GATHER && set != kTail) {
+    tc::grid_dependency_wait();
+    tc::grid_launch_dependents();
   }
   tc::fence_before_sync();
   __syncthreads();
