@@ -197,15 +197,17 @@ moe_status_t moe_dispatch_noalloc(const moe_config_t* cfg, const void* x,
 /* [MoE 模型原理 §1] First expert GEMM over the ragged groups given by
  * offsets: H[rows of e] = σ(xd[rows of e] W1[e]ᵀ + b1[e]).
  * Ordering: the GEMM kernels are launched with programmatic dependent launch.
- * With at most 64 rows per expert (the swapped decode GEMM) the kernel reads
- * offsets and starts copying weights as soon as it is scheduled, which can be
- * before the previous kernel in the stream has finished (it still waits for
- * that kernel before reading xd).  So offsets must not be written by a kernel
- * that signals its dependents early (griddepcontrol.launch_dependents) before
- * writing it; kernels that do not use griddepcontrol, copies, and every
- * kernel of this library (each waits for its own predecessor before it
- * signals) are fine.  The same holds for moe_ffn_down (which waits before
- * reading H). */
+ * The kernel reads offsets (and, with at most 64 rows per expert, starts
+ * copying weights) as soon as it is scheduled, which can be before the
+ * previous kernel in the stream has finished (it still waits for that kernel
+ * before reading xd).  So offsets must be complete when the kernel just
+ * before this call in the stream starts, or be written by a kernel that does
+ * not signal its dependents early (griddepcontrol.launch_dependents) or by a
+ * copy.  moe_dispatch ends with the row scatter, which starts only after the
+ * kernel that writes offsets has finished, and every kernel of this library
+ * waits for its predecessor before it signals: moe_dispatch → moe_ffn_up →
+ * moe_ffn_down meets the condition.  The same holds for moe_ffn_down (which
+ * waits before reading H). */
 moe_status_t moe_ffn_up(const moe_config_t* cfg, const void* xd, const int32_t* offsets,
                         const void* W1, const float* b1, void* H, void* ws, size_t ws_bytes,
                         void* stream);
