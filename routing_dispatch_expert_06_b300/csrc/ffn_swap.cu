@@ -160,8 +160,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = &s_abort;
   // Early weight copies only when every CTA has a tile.  With fewer tiles
   // than CTAs (T = 1 on the E = 64 layer: 66 and 96 tiles) they measured
-  // slower: the copies of a partial wave compete for HBM with the previous
-  // kernel's own weight stream, which is on the critical path.
+  // slower, in either GEMM (the first one's own run took 9.7 -> 12.3 us in
+  // the kernel timeline); the cause is not known, so such grids wait first.
   const bool early_w = total >= int64_t(gridDim.x);
   if (!early_w) {
     tc::grid_dependency_wait();
