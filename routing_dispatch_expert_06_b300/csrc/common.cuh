@@ -42,6 +42,7 @@ constexpr int kPsumFixedMaxE = 1024;
 constexpr size_t kWsRouteCounter = 64;
 constexpr size_t kWsDispatchCounter = 128;
 constexpr size_t kWsDispatchBarrier = 192;  // int [2]: arrivals, departures
+constexpr size_t kWsTailTiles = 256;        // int [2]: next tail tile, CTAs done
 constexpr size_t kWsPsumFixed = 16384;  // uint64 [kPsumReplicas][kPsumFixedMaxE]
 constexpr size_t kWsHeaderBytes =
     kWsPsumFixed + size_t(kPsumReplicas) * kPsumFixedMaxE * sizeof(unsigned long long);

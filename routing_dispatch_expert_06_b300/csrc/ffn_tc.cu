@@ -92,6 +92,14 @@ constexpr int kMaxExperts = 1024;
 // with E = 8 or 64 the few long-K tail tiles land on the critical path and
 // it cost 3-15%.
 constexpr int kTailSplitMinExperts = 128;
+// SMs the pair launch leaves to the tail launch when the GEMM is split.  The
+// tail tiles mostly stream weights (experts with at most 128 rows) while the
+// pair tiles are bound by the tensor pipe, so the tail launch's CTAs on these
+// SMs start with the pair launch (programmatic dependent launch) and overlap
+// the two; its remaining CTAs join as pair CTAs finish, taking tiles from a
+// shared counter.
+constexpr int kTailEarlySms = 28;
+constexpr int kTileQueue = 4;  // dynamic tail tiles published ahead of use
 enum { kActNone = -1 };
 
 // 64-wide k-blocks per pipeline stage.  The MMA thread's fixed work per
@@ -348,6 +356,8 @@ __global__ void __launch_bounds__(threads_for(GATHER), 1)
   __shared__ int s_abort;
   __shared__ int s_mt[kMaxExperts + 1];
   __shared__ int32_t s_off[kMaxExperts + 1];
+  __shared__ int64_t s_tq[kTileQueue];
+  __shared__ uint64_t tq_full[kTileQueue], tq_empty[kTileQueue];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = PAIR ? tc::cluster_ctarank() : 0u;  // 0 = the pair's MMA issuer
@@ -375,6 +385,10 @@ __global__ void __launch_bounds__(threads_for(GATHER), 1)
       tc::mbar_init(&tempty_bar[a], PAIR ? 2 * kEpiWarps : kEpiWarps);
     }
     tc::mbar_init(&drain_bar, 1);
+    for (int q = 0; q < kTileQueue; ++q) {
+      tc::mbar_init(&tq_full[q], 1);
+      tc::mbar_init(&tq_empty[q], 1 + kEpiWarps);  // the MMA warp and each epilogue warp
+    }
     s_abort = 0;
     tc::fence_mbar_init();
     tc::prefetch_tmap(&tmA);
@@ -456,6 +470,44 @@ __global__ void __launch_bounds__(threads_for(GATHER), 1)
   auto give_up = [&]() {
     *abort_flag = 1;
     set_status(status, MOE_ERR_TIMEOUT);
+  };
+  // Tile sequence of this CTA.  Static: first_tile, first_tile + tile_step,
+  // ...  Dynamic (the one-CTA tail launch): the producer thread takes the
+  // next tile from a counter in the workspace header and publishes it (or -1
+  // when none is left) in a shared-memory queue that the MMA warp and the
+  // epilogue warps read in the same order.
+  const bool dyn = !PAIR && !GATHER && set == kTail;
+  int* tail_ctr = reinterpret_cast<int*>(reinterpret_cast<char*>(status) + kWsTailTiles);
+  auto static_tile = [&](int n) -> int64_t {
+    const int64_t i = first_tile + int64_t(n) * tile_step;
+    return i < total ? i : -1;
+  };
+  auto publish_tile = [&](int n) -> int64_t {  // producer thread
+    if (!dyn) return static_tile(n);
+    const int q = n % kTileQueue;
+    if (!tc::mbar_wait(&tq_empty[q], uint32_t((n / kTileQueue) & 1) ^ 1u, abort_flag,
+                       kWaitLimitNs)) {
+      give_up();
+      return -1;
+    }
+    const int64_t t = atomicAdd(tail_ctr, 1);
+    const int64_t v = t < total ? t : -1;
+    s_tq[q] = v;
+    tc::mbar_arrive(&tq_full[q]);
+    return v;
+  };
+  auto read_tile = [&](int n) -> int64_t {  // a whole consumer warp
+    if (!dyn) return static_tile(n);
+    const int q = n % kTileQueue;
+    if (!__all_sync(0xffffffffu, tc::mbar_wait(&tq_full[q], uint32_t((n / kTileQueue) & 1),
+                                                abort_flag, kWaitLimitNs))) {
+      give_up();
+      return -1;
+    }
+    const int64_t v = s_tq[q];
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) tc::mbar_arrive(&tq_empty[q]);
+    return v;
   };
 
   if (GATHER && (warp == 0 || warp >= kEpiWarp0 + kEpiWarps)) {
@@ -546,7 +598,8 @@ __global__ void __launch_bounds__(threads_for(GATHER), 1)
     uint32_t phase = 0;
     int64_t issued = 0;
     bool ok = true;
-    for (int64_t i = first_tile; i < total && ok; i += tile_step) {
+    int n_tile = 0;
+    for (int64_t i = publish_tile(0); i >= 0 && ok; i = publish_tile(++n_tile)) {
       const TileCoord c =
           tile_coord(i, s_mt, E, n_tn, s_off, BN, rows_per_tile, int(rank), set);
       for (int kb = 0; kb < nk; ++kb) {
@@ -598,7 +651,8 @@ __global__ void __launch_bounds__(threads_for(GATHER), 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
-    for (int64_t i = first_tile; i < total && ok; i += tile_step) {
+    int n_tile = 0;
+    for (int64_t i = read_tile(0); i >= 0 && ok; i = read_tile(++n_tile)) {
       // Waits are taken by every lane and agreed on, so the warp stays
       // converged and its operands warp-uniform.
       const bool free_acc = __all_sync(
@@ -666,7 +720,8 @@ __global__ void __launch_bounds__(threads_for(GATHER), 1)
     const uint32_t buf_s = tc::smem_u32(buf);
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int64_t i = first_tile; i < total; i += tile_step) {
+    int n_tile = 0;
+    for (int64_t i = read_tile(0); i >= 0; i = read_tile(++n_tile)) {
       const TileCoord c =
           tile_coord(i, s_mt, E, n_tn, s_off, BN, rows_per_tile, int(rank), set);
       // The tensor-memory loads below are warp-collective: the whole warp
@@ -764,6 +819,15 @@ __global__ void __launch_bounds__(threads_for(GATHER), 1)
     else
       tc::tmem_dealloc(tmem_base, kTmemCols);
   }
+  // The last CTA of a dynamic tail launch to finish clears the tile counter
+  // for the next launch (every CTA has taken its last tile by now).
+  if (dyn && threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(tail_ctr + 1, 1) == int(gridDim.x) - 1) {
+      atomicExch(tail_ctr, 0);
+      atomicExch(tail_ctr + 1, 0);
+    }
+  }
   // A tail launch that started early does not finish before the pair launch
   // it overlapped: work after it in the stream sees every tile.
   if (set == kTail) tc::grid_dependency_wait();
@@ -858,6 +922,11 @@ cudaError_t launch_variant(int act, const CUtensorMap& tmA, const CUtensorMap& t
       if (e != cudaSuccess) return e;
       if (clusters < 1) return cudaErrorInvalidConfiguration;
       grid = unsigned(2 * clusters);
+      // Leave kTailEarlySms SMs to the dynamic tail launch that follows.
+      if (!GATHER && set == kPairBody && sms > 2 * kTailEarlySms) {
+        const unsigned cap = unsigned(sms - kTailEarlySms) & ~1u;
+        if (grid > cap) grid = cap;
+      }
     }
     cfg.gridDim = dim3(grid);
     // Programmatic dependent launch on every launch (see the kernel's
