@@ -92,12 +92,13 @@ constexpr int kMaxExperts = 1024;
 // with E = 8 or 64 the few long-K tail tiles land on the critical path and
 // it cost 3-15%.
 constexpr int kTailSplitMinExperts = 128;
-// SMs the pair launch leaves to the tail launch when the GEMM is split.  The
-// tail tiles mostly stream weights (experts with at most 128 rows) while the
-// pair tiles are bound by the tensor pipe, so the tail launch's CTAs on these
-// SMs start with the pair launch (programmatic dependent launch) and overlap
-// the two; its remaining CTAs join as pair CTAs finish, taking tiles from a
-// shared counter.
+// SMs the pair launch leaves to the tail launch when the GEMM is split and
+// the tail set has at least two tiles for each of them (decided on the
+// device from offsets).  The tail tiles mostly stream weights (experts with
+// at most 128 rows) while the pair tiles are bound by the tensor pipe, so the
+// tail launch's CTAs on these SMs start with the pair launch (programmatic
+// dependent launch) and overlap the two; its remaining CTAs join as pair
+// CTAs finish, taking tiles from a shared counter.
 constexpr int kTailEarlySms = 28;
 constexpr int kTileQueue = 4;  // dynamic tail tiles published ahead of use
 enum { kActNone = -1 };
@@ -357,6 +358,7 @@ __global__ void __launch_bounds__(threads_for(GATHER), 1)
   __shared__ int s_mt[kMaxExperts + 1];
   __shared__ int32_t s_off[kMaxExperts + 1];
   __shared__ int64_t s_tq[kTileQueue];
+  __shared__ int s_tail_mt;  // the tail set's row tiles (pair launches)
   __shared__ uint64_t tq_full[kTileQueue], tq_empty[kTileQueue];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -430,13 +432,16 @@ __global__ void __launch_bounds__(threads_for(GATHER), 1)
     };
     const int per = (E + 31) / 32;
     const int lo = lane * per, hi = min(E, lo + per);
-    int run = 0;
+    int run = 0, tail_run = 0;
     for (int e = lo; e < hi; ++e) {
       const int32_t a = clamp_row(e), b = clamp_row(e + 1);
       s_off[e] = a;
       run += tiles_in_set(b - a, set, rows_per_tile);
+      if (set == kPairBody) tail_run += tiles_in_set(b - a, kTail, kTileM);
     }
     if (lane == 31) s_off[E] = clamp_row(E);
+    tail_run = __reduce_add_sync(0xffffffffu, tail_run);
+    if (lane == 0) s_tail_mt = tail_run;
     int incl = run;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -463,8 +468,18 @@ __global__ void __launch_bounds__(threads_for(GATHER), 1)
   const int n_tn = (N + BN - 1) / BN;
   const int64_t total = int64_t(s_mt[E]) * n_tn;
   const int nk = (K + KB * kTileK - 1) / (KB * kTileK);  // stages per tile
-  const int64_t first_tile = PAIR ? blockIdx.x / 2 : blockIdx.x;
-  const int64_t tile_step = PAIR ? gridDim.x / 2 : gridDim.x;
+  int64_t first_tile = PAIR ? blockIdx.x / 2 : blockIdx.x;
+  int64_t tile_step = PAIR ? gridDim.x / 2 : gridDim.x;
+  if (PAIR && !GATHER && set == kPairBody) {
+    // When the tail launch that follows has work for kTailEarlySms SMs (two
+    // tiles each), the last kTailEarlySms / 2 clusters take no tile and leave
+    // at once, so the tail launch starts on their SMs beside this one.
+    const int64_t clusters = gridDim.x / 2;
+    if (int64_t(s_tail_mt) * n_tn >= 2 * kTailEarlySms && clusters > kTailEarlySms) {
+      tile_step = clusters - kTailEarlySms / 2;
+      if (first_tile >= tile_step) first_tile = total;
+    }
+  }
   volatile int* abort_flag = &s_abort;
 
   auto give_up = [&]() {
@@ -922,11 +937,6 @@ cudaError_t launch_variant(int act, const CUtensorMap& tmA, const CUtensorMap& t
       if (e != cudaSuccess) return e;
       if (clusters < 1) return cudaErrorInvalidConfiguration;
       grid = unsigned(2 * clusters);
-      // Leave kTailEarlySms SMs to the dynamic tail launch that follows.
-      if (!GATHER && set == kPairBody && sms > 2 * kTailEarlySms) {
-        const unsigned cap = unsigned(sms - kTailEarlySms) & ~1u;
-        if (grid > cap) grid = cap;
-      }
     }
     cfg.gridDim = dim3(grid);
     // Programmatic dependent launch on every launch (see the kernel's
